@@ -1,0 +1,345 @@
+"""Seeded synthetic workloads for the DSA indexer hot path.
+
+This module only *draws* inputs: random bits, normals, uniform integers,
+permutations, and the rounding of the drawn reals into the storage formats
+the kernels consume (bf16 bits, OCP E4M3 codes with a per-row scale, raw
+mxfp4 bytes).  It holds none of the method's arithmetic (no logits, no
+top-k, no mxfp4 decode), so the CPU oracle and the CUDA path can both take
+their inputs from here without sharing any of the computation they check.
+
+Generator: SplitMix64 (Steele, Lea, Flood, "Fast splittable pseudorandom
+number generators", OOPSLA 2014), used in counter mode so every named draw is
+an independent stream that does not shift when other draws are added:
+``x_i = mix(base(seed, stream) + (i + 1) * 0x9E3779B97F4A7C15)``.
+Normals come from the Box-Muller transform in float64, rounded to float32
+(numpy RNE) and then to bf16 (round to nearest even).  Uniform integers use a
+32x32->64 multiply-shift on the high 32 bits (bias <= range / 2**32).
+
+Workload shapes follow the five configurations of the DeepSeek-V4 indexer
+problem statement (xkernels issue #27 "Context": index_n_heads 64,
+index_head_dim 128; top-512 Flash / top-1024 Pro; xkernels issue #28,
+comment 2 "What it does": paged mxfp4 cache, E2M1 nibbles plus one E8M0 scale
+per 32 elements, padded slots sel_pos < 0).
+"""
+from __future__ import annotations
+
+import dataclasses
+import hashlib
+from typing import Optional
+
+import numpy as np
+
+H = 64
+D = 128
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_CHUNK = 1 << 22
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def _stream_base(seed: int, stream: str) -> np.uint64:
+    tag = int.from_bytes(hashlib.sha256(stream.encode()).digest()[:8], "little")
+    z = np.array([(seed * 0x9E3779B97F4A7C15 + tag) & (2**64 - 1)], dtype=np.uint64)
+    return _mix(z)[0]
+
+
+class Rng:
+    """Counter-mode SplitMix64 with named, independent streams."""
+
+    def __init__(self, seed: int):
+        self.seed = int(seed)
+
+    def u64(self, n: int, stream: str, start: int = 0) -> np.ndarray:
+        base = _stream_base(self.seed, stream)
+        i = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+        with np.errstate(over="ignore"):
+            return _mix(base + i * _GAMMA)
+
+    def uniform(self, n: int, stream: str, start: int = 0) -> np.ndarray:
+        """Doubles in [0, 1) from the top 53 bits."""
+        return (self.u64(n, stream, start) >> np.uint64(11)).astype(np.float64) * (2.0**-53)
+
+    def integers(self, lo: int, hi: int, n: int, stream: str) -> np.ndarray:
+        """Integers uniform on [lo, hi] (inclusive), multiply-shift on 32 bits."""
+        span = np.uint64(hi - lo + 1)
+        top = self.u64(n, stream) >> np.uint64(32)
+        return (lo + ((top * span) >> np.uint64(32)).astype(np.int64)).astype(np.int64)
+
+    def permutation(self, n: int, stream: str) -> np.ndarray:
+        """Uniform shuffle: order of n random 64-bit keys (ties broken by position)."""
+        return np.argsort(self.u64(n, stream), kind="stable").astype(np.int64)
+
+    def normal_into(self, out: np.ndarray, stream: str) -> None:
+        """Fill a float32 array with N(0,1) via Box-Muller in float64."""
+        flat = out.reshape(-1)
+        n = flat.size
+        pairs = (n + 1) // 2
+        for p0 in range(0, pairs, _CHUNK):
+            m = min(_CHUNK, pairs - p0)
+            u1 = self.uniform(m, stream + "/u1", p0)
+            u2 = self.uniform(m, stream + "/u2", p0)
+            r = np.sqrt(-2.0 * np.log1p(-u1))
+            th = (2.0 * np.pi) * u2
+            blk = np.empty(2 * m, dtype=np.float64)
+            blk[0::2] = r * np.cos(th)
+            blk[1::2] = r * np.sin(th)
+            lo = 2 * p0
+            hi = min(n, lo + 2 * m)
+            flat[lo:hi] = blk[: hi - lo].astype(np.float32)
+
+    def bytes_into(self, out: np.ndarray, stream: str) -> None:
+        """Fill a uint8 array with uniform random bytes."""
+        flat = out.reshape(-1)
+        n = flat.size
+        words = (n + 7) // 8
+        for w0 in range(0, words, _CHUNK):
+            m = min(_CHUNK, words - w0)
+            b = self.u64(m, stream, w0).view(np.uint8)
+            lo = 8 * w0
+            hi = min(n, lo + 8 * m)
+            flat[lo:hi] = b[: hi - lo]
+
+
+# ---------------------------------------------------------------- storage formats
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (nearest, ties to even) and return the 16-bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        r[nan] = np.uint16(0x7FC0)
+    return r
+
+
+def normal_bf16(rng: Rng, shape, stream: str) -> np.ndarray:
+    out = np.empty(shape, dtype=np.uint16)
+    flat = out.reshape(-1)
+    tmp = np.empty(min(flat.size, 2 * _CHUNK), dtype=np.float32)
+    # Draw in slices so multi-GB key pools never hold a float64 copy.
+    step = tmp.size
+    for s0 in range(0, flat.size, step):
+        m = min(step, flat.size - s0)
+        buf = tmp[:m]
+        rng.normal_into(buf, f"{stream}@{s0}")
+        flat[s0:s0 + m] = f32_to_bf16_bits(buf)
+    return out
+
+
+def quantize_e4m3_rows(x: np.ndarray):
+    """Per-row OCP E4M3 quantisation of a float32 array [..., R].
+
+    scale = max|x_row| / 448 (float32), code = E4M3(RNE, saturating)(x / scale);
+    an all-zero row gets scale 1.  The E4M3 rounding is torch's float32 ->
+    float8_e4m3fn conversion after clamping to +-448 (the format's largest
+    finite magnitude), which makes it saturating.
+    """
+    import torch
+
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    amax = np.abs(x).max(axis=-1)
+    scale = (amax / np.float32(448.0)).astype(np.float32)
+    scale[amax == 0] = np.float32(1.0)
+    y = np.clip(x / scale[..., None], np.float32(-448.0), np.float32(448.0)).astype(np.float32)
+    codes = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    return codes, scale
+
+
+# ---------------------------------------------------------------- workloads
+
+@dataclasses.dataclass
+class Workload:
+    """One batch of indexer + gather inputs (host arrays).
+
+    q         [T, H, D] uint16 (bf16 bits) or uint8 (E4M3 codes); T = B * next_n
+    q_scale   [T, H] float32 or None
+    weights   [T, H] float32
+    k_data    [rows, D] uint16 / uint8: the paged pool (nblk * block_size rows)
+              when block_table is set, else the contiguous keys of one sequence
+    k_scale   [rows] float32 or None
+    block_table [B, max_blocks] int32 or None (unused entries are -1)
+    kv_fp4    [nblk_g, block_size, D/2] uint8, low nibble = even element
+    kv_scale  [nblk_g, block_size, D/32] uint8 E8M0
+    gather_block_table [B, max_blocks_g] int32
+    """
+
+    name: str
+    B: int
+    next_n: int
+    context_lens: np.ndarray
+    causal: bool
+    topk: int
+    dtype: str
+    q: np.ndarray
+    q_scale: Optional[np.ndarray]
+    weights: np.ndarray
+    k_data: np.ndarray
+    k_scale: Optional[np.ndarray]
+    block_table: Optional[np.ndarray]
+    block_size: int
+    kv_fp4: Optional[np.ndarray] = None
+    kv_scale: Optional[np.ndarray] = None
+    gather_block_table: Optional[np.ndarray] = None
+    gather_pad_frac: float = 0.0
+    seed: int = 0
+
+    @property
+    def T(self) -> int:
+        return self.B * self.next_n
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.B else 0
+
+    def positions(self) -> np.ndarray:
+        """Absolute position p of every query row: L_b - next_n + i."""
+        L = np.repeat(self.context_lens.astype(np.int64), self.next_n)
+        i = np.tile(np.arange(self.next_n, dtype=np.int64), self.B)
+        return L - self.next_n + i
+
+    def visible_len(self) -> np.ndarray:
+        """Number of leading keys each query row may see (causal: p + 1, else L_b)."""
+        if self.causal:
+            return self.positions() + 1
+        return np.repeat(self.context_lens.astype(np.int64), self.next_n)
+
+
+def _page_pool(rng: Rng, context_lens: np.ndarray, block_size: int, stream: str):
+    """Deal a random permutation of all physical blocks to the sequences in order."""
+    nblocks = [(int(L) + block_size - 1) // block_size for L in context_lens]
+    total = int(sum(nblocks))
+    perm = rng.permutation(total, stream).astype(np.int32)
+    width = max(nblocks) if nblocks else 0
+    table = np.full((len(context_lens), max(width, 1)), -1, dtype=np.int32)
+    o = 0
+    for b, nb in enumerate(nblocks):
+        table[b, :nb] = perm[o:o + nb]
+        o += nb
+    return table, total
+
+
+def _mxfp4_pool(rng: Rng, nblk: int, block_size: int, stream: str, ff_frac: float = 0.01):
+    """Random nibble bytes; E8M0 scales uniform on 120..134 with ~1% set to 0xFF."""
+    fp4 = np.empty((nblk, block_size, D // 2), dtype=np.uint8)
+    rng.bytes_into(fp4, stream + "/nib")
+    n_sc = nblk * block_size * (D // 32)
+    sc = (120 + rng.integers(0, 14, n_sc, stream + "/sc")).astype(np.uint8)
+    ff = rng.uniform(n_sc, stream + "/ff") < ff_frac
+    sc[ff] = 0xFF
+    return fp4, sc.reshape(nblk, block_size, D // 32)
+
+
+def _weights(rng: Rng, T: int, stream: str) -> np.ndarray:
+    return (rng.uniform(T * H, stream).astype(np.float32) / np.float32(8.0)).reshape(T, H)
+
+
+def make_tiny(seed: int = 1, T: int = 64, L: int = 2048, topk: int = 512) -> Workload:
+    """T queries at positions L-T..L-1 over L contiguous bf16 keys, causal."""
+    rng = Rng(seed)
+    q = normal_bf16(rng, (T, H, D), "q")
+    k = normal_bf16(rng, (L, D), "k")
+    w = _weights(rng, T, "w")
+    lens = np.array([L], dtype=np.int32)
+    gtab, nblk = _page_pool(rng, lens, 64, "gather_table")
+    fp4, sc = _mxfp4_pool(rng, nblk, 64, "cache")
+    return Workload("tiny", 1, T, lens, True, topk, "bf16", q, None, w, k, None, None, 64,
+                    fp4, sc, gtab, 0.05, seed)
+
+
+def make_decode(seed: int, B: int, next_n: int, lmin: int, lmax: int, topk: int,
+                name: str, pad_frac: float, block_size: int = 64) -> Workload:
+    """Paged bf16 decode batch: B sequences, next_n causal query tokens each."""
+    rng = Rng(seed)
+    lens = rng.integers(lmin, lmax, B, "context_lens").astype(np.int32)
+    table, nblk = _page_pool(rng, lens, block_size, "block_table")
+    T = B * next_n
+    q = normal_bf16(rng, (T, H, D), "q")
+    k = normal_bf16(rng, (nblk * block_size, D), "k_pool")
+    w = _weights(rng, T, "w")
+    fp4, sc = _mxfp4_pool(rng, nblk, block_size, "cache")
+    return Workload(name, B, next_n, lens, True, topk, "bf16", q, None, w, k, None, table,
+                    block_size, fp4, sc, table, pad_frac, seed)
+
+
+def make_flash_decode(seed: int = 2, B: int = 64, lmin: int = 4096, lmax: int = 65536) -> Workload:
+    return make_decode(seed, B, 1, lmin, lmax, 512, "flash_decode", 0.0)
+
+
+def make_pro_mtp(seed: int = 3, B: int = 32, lmin: int = 32768, lmax: int = 131072) -> Workload:
+    return make_decode(seed, B, 2, lmin, lmax, 1024, "pro_mtp", 0.02)
+
+
+def make_prefill(seed: int = 4, T: int = 16384, topk: int = 512) -> Workload:
+    """One sequence, T = K, full causal mask, contiguous bf16 keys, no gather."""
+    rng = Rng(seed)
+    q = normal_bf16(rng, (T, H, D), "q")
+    k = normal_bf16(rng, (T, D), "k")
+    w = _weights(rng, T, "w")
+    lens = np.array([T], dtype=np.int32)
+    return Workload("prefill", 1, T, lens, True, topk, "bf16", q, None, w, k, None, None, 64,
+                    seed=seed)
+
+
+def make_fp8_chunked(seed: int = 5, T: int = 8192, L: int = 65536, topk: int = 1024,
+                     gather_blocks: Optional[int] = None) -> Workload:
+    """T E4M3 queries at positions L-T..L-1 over L contiguous E4M3 keys, causal,
+    per-row fp32 scales; then a gather of every selection from a paged mxfp4 pool."""
+    rng = Rng(seed)
+    T_rows = T
+    qf = np.empty((T_rows, H, D), dtype=np.float32)
+    rng.normal_into(qf, "q")
+    q, q_scale = quantize_e4m3_rows(qf)
+    del qf
+    kf = np.empty((L, D), dtype=np.float32)
+    rng.normal_into(kf, "k")
+    k, k_scale = quantize_e4m3_rows(kf)
+    del kf
+    w = _weights(rng, T_rows, "w")
+    lens = np.array([L], dtype=np.int32)
+    gtab, nblk = _page_pool(rng, lens, 64, "gather_table")
+    if gather_blocks is not None:
+        assert gather_blocks == nblk
+    fp4, sc = _mxfp4_pool(rng, nblk, 64, "cache")
+    return Workload("fp8_chunked", 1, T_rows, lens, True, topk, "e4m3", q, q_scale, w, k,
+                    k_scale, None, 64, fp4, sc, gtab, 0.0, seed)
+
+
+def pad_sel_pos(sel_pos: np.ndarray, frac: float, seed: int, stream: str = "pad") -> np.ndarray:
+    """Overwrite a seeded fraction of the selected positions with -1 (padded slots)."""
+    out = np.array(sel_pos, dtype=np.int32, copy=True)
+    if frac > 0:
+        m = Rng(seed).uniform(out.size, stream) < frac
+        out.reshape(-1)[m] = -1
+    return out
+
+
+def random_sel_pos(wl: Workload, seed: int, stream: str = "sel") -> np.ndarray:
+    """Distinct random visible positions per query row (a stand-in selection),
+    padded with -1 where a row sees fewer than topk keys."""
+    rng = Rng(seed)
+    vis = wl.visible_len()
+    out = np.full((wl.T, wl.topk), -1, dtype=np.int32)
+    for t in range(wl.T):
+        n = int(vis[t])
+        keys = rng.u64(n, f"{stream}/{t}")
+        pick = np.argsort(keys, kind="stable")[: min(n, wl.topk)]
+        out[t, : pick.size] = pick
+    return out
+
+
+CONFIGS = {
+    "tiny": make_tiny,
+    "flash_decode": make_flash_decode,
+    "pro_mtp": make_pro_mtp,
+    "prefill": make_prefill,
+    "fp8_chunked": make_fp8_chunked,
+}

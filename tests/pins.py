@@ -1,0 +1,397 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics fix.
+
+Each ``check_*`` takes an oracle module and raises AssertionError when the
+oracle disagrees with a value or property that does not come from the oracle
+itself: hand-worked fixtures under tests/golden/ (each cites its passage),
+library routines (torch's bf16 / float8_e4m3fn conversions), closed forms,
+invariants and brute force on tiny inputs.  The same checks run against
+deliberately broken copies of the oracle in test_oracle_mutants.py, to show
+that a plausible mistake in it would be caught.
+"""
+from __future__ import annotations
+
+import itertools
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------- fixtures
+
+def load_mxfp4_rows():
+    rows = []
+    cur = None
+    with open(os.path.join(GOLDEN, "mxfp4_hand.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            tag, *rest = line.split()
+            if tag == "row":
+                cur = {"name": rest[0], "bytes": np.zeros(64, np.uint8),
+                       "scales": None, "expect": np.zeros(128, np.uint16)}
+                rows.append(cur)
+            elif tag == "scales":
+                cur["scales"] = np.array([int(x, 16) for x in rest], dtype=np.uint8)
+            elif tag == "bytes":
+                for item in rest:
+                    i, v = item.split(":")
+                    cur["bytes"][int(i)] = int(v, 16)
+            elif tag == "expect":
+                for item in rest:
+                    e, v = item.split(":")
+                    cur["expect"][int(e)] = int(v, 16)
+    return rows
+
+
+def load_logits_case():
+    vals = {}
+    with open(os.path.join(GOLDEN, "logits_hand.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                tag, *rest = line.split()
+                vals[tag] = rest
+    H, Dm, L, n = (int(vals[k][0]) for k in ("H", "D", "L", "next_n"))
+    q = np.array([float(x) for x in vals["q"]]).reshape(n, H, Dm)
+    w = np.array([float(x) for x in vals["w"]]).reshape(n, H)
+    k = np.array([float(x) for x in vals["k"]]).reshape(L, Dm)
+    expect = np.array([float(x) for x in vals["expect"]]).reshape(n, L)
+    return H, Dm, L, n, q, w, k, expect
+
+
+def load_topk_cases():
+    cases = []
+    row = None
+    with open(os.path.join(GOLDEN, "topk_hand.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            tag, *rest = line.split()
+            if tag == "row":
+                row = np.array([float(x) for x in rest], dtype=np.float64)
+            elif tag == "k":
+                k = int(rest[0])
+                assert rest[1] == "expect"
+                cases.append((row, k, np.array([int(x) for x in rest[2:]], dtype=np.int32)))
+    return cases
+
+
+def f64_to_bf16_exact(x: np.ndarray) -> np.ndarray:
+    """bf16 bits of values that bf16 represents exactly (fixtures are chosen so)."""
+    f = np.asarray(x, dtype=np.float32)
+    assert np.array_equal(f.astype(np.float64), np.asarray(x, dtype=np.float64))
+    u = f.view(np.uint32)
+    assert (u & 0xFFFF == 0).all()
+    return (u >> 16).astype(np.uint16)
+
+
+# --------------------------------------------------------------------------- decoders
+
+def check_bf16_decode(orc):
+    import torch
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    got = orc.bf16_to_f64(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan].astype(np.float64))
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def check_e4m3_decode(orc):
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy()
+    got = orc.e4m3_to_f64(codes)
+    nan = np.isnan(ref)
+    assert nan.sum() == 2                       # S.1111.111 only
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan].astype(np.float64))
+    # hand values from the OCP E4M3 definition
+    hand = {0x38: 1.0, 0x7E: 448.0, 0x01: 2.0**-9, 0x08: 2.0**-6, 0xBC: -1.5, 0x00: 0.0, 0x40: 2.0}
+    for c, v in hand.items():
+        assert orc.e4m3_to_f64(np.array([c], np.uint8))[0] == v, hex(c)
+    assert np.signbit(orc.e4m3_to_f64(np.array([0x80], np.uint8))[0])
+
+
+def check_bf16_rounding(orc):
+    import torch
+    x = np.concatenate([
+        np.random.default_rng(0).standard_normal(20000).astype(np.float32) * 1e3,
+        np.array([1.0 + 2**-8, 1.0 + 3 * 2**-8, 3.4e38, -3.4e38, 1e-40, -1e-40, 2.0**-128,
+                  0.0, -0.0, np.inf, -np.inf], dtype=np.float32),
+    ])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = orc.f64_to_bf16_bits(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+# --------------------------------------------------------------------------- mxfp4
+
+def check_e8m0(orc):
+    b = np.arange(256)
+    s = orc.e8m0_scale(b)
+    assert s[127] == 1.0 and s[128] == 2.0 and s[126] == 0.5
+    assert s[0] == 2.0**-127 and s[254] == 2.0**127
+    assert s[255] == 0.0
+    assert np.all(s[1:255] == 2.0 * s[0:254])   # one binade per step
+
+
+def check_e2m1(orc):
+    # OCP MX E2M1 magnitudes, then the sign bit
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    got = orc.e2m1_value(np.arange(16))
+    assert list(got[:8]) == mags
+    assert list(-got[8:]) == mags
+    assert np.signbit(got[8])
+
+
+def check_mxfp4_hand_rows(orc):
+    for row in load_mxfp4_rows():
+        vals = orc.mxfp4_dequant(row["bytes"][None, :], row["scales"][None, :])[0]
+        got = orc.f64_to_bf16_bits(vals)
+        bad = np.nonzero(got != row["expect"])[0]
+        assert bad.size == 0, (row["name"], bad[:8], got[bad[:8]], row["expect"][bad[:8]])
+
+
+def check_mxfp4_gather_hand(orc):
+    """Padded slot -> 256 zero bytes; a live slot reads its row through the table."""
+    rows = load_mxfp4_rows()
+    bs = 2
+    nblk = 2
+    fp4 = np.zeros((nblk, bs, 64), np.uint8)
+    sc = np.full((nblk, bs, 4), 0x7F, np.uint8)
+    # logical position 1 of sequence 0 -> block_table[0, 0] = 1, offset 1
+    fp4[1, 1] = rows[0]["bytes"]
+    sc[1, 1] = rows[0]["scales"]
+    table = np.array([[1, 0]], np.int32)
+    sel = np.array([[1, -1, 2]], np.int32)        # position 2 -> block 0, offset 0 (zeros)
+    out = orc.mxfp4_paged_gather(fp4, sc, table, sel, 1, 1, bs)
+    assert out.shape == (1, 3, 128) and out.dtype == np.uint16
+    assert np.array_equal(out[0, 0], rows[0]["expect"])
+    assert not out[0, 1].any()
+    assert not out[0, 2].any()
+
+
+def check_gather_invariant(orc, seed=7):
+    """Dequantise the whole cache then index == gather (index then dequantise), bitwise.
+
+    The indexing on the left is an explicit loop over (t, s) written here.
+    """
+    r = np.random.default_rng(seed)
+    B, n, K, bs, nblk = 3, 2, 9, 4, 7
+    fp4 = r.integers(0, 256, (nblk, bs, 64), dtype=np.uint8)
+    sc = r.integers(118, 137, (nblk, bs, 4)).astype(np.uint8)
+    sc[r.random(sc.shape) < 0.1] = 0xFF
+    table = np.stack([r.permutation(nblk)[:3] for _ in range(B)]).astype(np.int32)
+    sel = r.integers(-1, 3 * bs, (B * n, K)).astype(np.int32)
+    flat_vals = orc.mxfp4_dequant(fp4.reshape(-1, 64), sc.reshape(-1, 4))
+    flat_bits = orc.f64_to_bf16_bits(flat_vals)
+    expect = np.zeros((B * n, K, 128), np.uint16)
+    for t in range(B * n):
+        for s in range(K):
+            pos = int(sel[t, s])
+            if pos < 0:
+                continue
+            blk = int(table[t // n, pos // bs])
+            expect[t, s] = flat_bits[blk * bs + pos % bs]
+    got = orc.mxfp4_paged_gather(fp4, sc, table, sel, B, n, bs)
+    assert np.array_equal(got, expect)
+
+
+# --------------------------------------------------------------------------- logits
+
+def _logits(orc, q, w, k, B, n, lens, causal=True, table=None, bs=1, q_scale=None,
+            k_scale=None, dtype="bf16"):
+    return orc.indexer_logits(q, q_scale, dtype, w, k, k_scale, table, bs, B, n, lens, causal)
+
+
+def _as_bf16(x):
+    return f64_to_bf16_exact(np.asarray(x, dtype=np.float64))
+
+
+def check_logits_hand(orc):
+    H, Dm, L, n, q, w, k, expect = load_logits_case()
+    lens = np.array([L])
+    got = _logits(orc, _as_bf16(q), w, _as_bf16(k), 1, n, lens)
+    assert np.array_equal(got, expect), got
+    # the same keys through a permuted page table (block size 2)
+    pool = np.concatenate([k[2:4], k[0:2]])          # physical block 0 = keys 2,3; block 1 = keys 0,1
+    table = np.array([[1, 0]], np.int32)
+    got_p = _logits(orc, _as_bf16(q), w, _as_bf16(pool), 1, n, lens, table=table, bs=2)
+    assert np.array_equal(got_p, expect)
+    # non-causal: query 0 also sees key 3: h0 = 1+2 = 3, h1 = -1+0.5 < 0 -> 2*3 = 6
+    got_nc = _logits(orc, _as_bf16(q), w, _as_bf16(k), 1, n, lens, causal=False)
+    assert got_nc[0, 3] == 6.0 and np.array_equal(got_nc[1], expect[1])
+
+
+def check_logits_plain_matmul(orc, seed=3):
+    """H = 1, w = 1 and positive q, k: the score is the plain product q k^T,
+    checked against a triple loop."""
+    r = np.random.default_rng(seed)
+    T, L, Dm = 5, 7, 6
+    qv = r.integers(1, 9, (T, 1, Dm)).astype(np.float64) / 4
+    kv = r.integers(1, 9, (L, Dm)).astype(np.float64) / 8
+    got = _logits(orc, _as_bf16(qv), np.ones((T, 1)), _as_bf16(kv), 1, T, np.array([L]),
+                  causal=False)
+    for t in range(T):
+        for j in range(L):
+            acc = 0.0
+            for d in range(Dm):
+                acc += qv[t, 0, d] * kv[j, d]
+            assert got[t, j] == acc
+
+
+def check_logits_special(orc, seed=4):
+    r = np.random.default_rng(seed)
+    H, Dm, L, T = 4, 8, 6, 3
+    # one-hot q and k: q[t,h] = e_(h), k[j] = c_j * e_(j mod Dm) -> only head (j mod Dm) fires
+    q = np.zeros((T, H, Dm))
+    for h in range(H):
+        q[:, h, h] = 1.0
+    k = np.zeros((L, Dm))
+    for j in range(L):
+        k[j, j % Dm] = j + 1.0
+    w = np.arange(1, T * H + 1, dtype=np.float64).reshape(T, H)
+    got = _logits(orc, _as_bf16(q), w, _as_bf16(k), 1, T, np.array([L]), causal=False)
+    for t in range(T):
+        for j in range(L):
+            want = w[t, j % Dm] * (j + 1.0) if j % Dm < H else 0.0
+            assert got[t, j] == want
+    # all dot products negative -> +0.0
+    qn = -np.abs(r.integers(1, 5, (T, H, Dm))).astype(np.float64)
+    kp = np.abs(r.integers(1, 5, (L, Dm))).astype(np.float64)
+    z = _logits(orc, _as_bf16(qn), np.abs(r.random((T, H))) + 0.1, _as_bf16(kp), 1, T,
+                np.array([L]), causal=False)
+    assert np.all(z == 0.0) and not np.signbit(z).any()
+    # one live head: w = e_h -> relu(q_h . k)
+    qr = r.integers(-4, 5, (T, H, Dm)).astype(np.float64)
+    kr = r.integers(-4, 5, (L, Dm)).astype(np.float64)
+    for h in range(H):
+        wh = np.zeros((T, H))
+        wh[:, h] = 1.0
+        g = _logits(orc, _as_bf16(qr), wh, _as_bf16(kr), 1, T, np.array([L]), causal=False)
+        for t in range(T):
+            for j in range(L):
+                dot = float(np.dot(qr[t, h], kr[j]))
+                assert g[t, j] == max(dot, 0.0)
+
+
+def check_logits_invariances(orc, seed=5):
+    r = np.random.default_rng(seed)
+    H, Dm, L, n, B = 8, 16, 20, 3, 2
+    lens = np.array([L, L - 5])
+    q = _as_bf16(r.integers(-8, 9, (B * n, H, Dm)) / 8.0)
+    k = _as_bf16(r.integers(-8, 9, (L, Dm)) / 8.0)
+    w = r.random((B * n, H))
+    # keys of both sequences from one pool through two tables (block size 5)
+    pool = np.concatenate([k, k])
+    table = np.array([[0, 1, 2, 3], [4, 5, 6, 7]], np.int32)
+    base = _logits(orc, q, w, pool, B, n, lens, table=table, bs=5)
+    # weights x2 -> logits x2 exactly
+    assert np.array_equal(_logits(orc, q, 2 * w, pool, B, n, lens, table=table, bs=5),
+                          2 * base)
+    # jointly permuting heads in q and w, or dims in q and k, changes nothing
+    ph = r.permutation(H)
+    got = _logits(orc, q[:, ph], w[:, ph], pool, B, n, lens, table=table, bs=5)
+    assert np.allclose(got, base, rtol=1e-12, atol=0) and np.array_equal(got == -np.inf,
+                                                                         base == -np.inf)
+    pd = r.permutation(Dm)
+    got = _logits(orc, q[:, :, pd], w, pool[:, pd], B, n, lens, table=table, bs=5)
+    assert np.allclose(got, base, rtol=1e-12, atol=0)
+    # causal visibility, brute force: row t = b*n + i sees j <= L_b - n + i, and j < L_b
+    for t in range(B * n):
+        b, i = divmod(t, n)
+        for j in range(L):
+            vis = j <= lens[b] - n + i and j < lens[b]
+            assert (base[t, j] != -np.inf) == vis, (t, j)
+    # sequence 1 scores depend on its own keys only (pool rows 20..34 through table row 1)
+    pool2 = pool.copy()
+    pool2[:L] = _as_bf16(np.zeros((L, Dm)))
+    got = _logits(orc, q, w, pool2, B, n, lens, table=table, bs=5)
+    assert np.array_equal(got[n:], base[n:])
+
+
+def check_logits_e4m3(orc, seed=6):
+    """E4M3 inputs with per-row scales score like their dequantised float values."""
+    r = np.random.default_rng(seed)
+    H, Dm, L, T = 4, 8, 9, 3
+    qc = r.integers(0, 256, (T, H, Dm)).astype(np.uint8)
+    qc[(qc & 0x7F) == 0x7F] = 0x30                    # no NaN codes
+    kc = r.integers(0, 256, (L, Dm)).astype(np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x31
+    qs = (r.random((T, H)) + 0.5).astype(np.float32)
+    ks = (r.random(L) + 0.5).astype(np.float32)
+    w = r.random((T, H))
+    got = _logits(orc, qc, w, kc, 1, T, np.array([L]), causal=False, q_scale=qs, k_scale=ks,
+                  dtype="e4m3")
+    # rebuild the float inputs from the torch decode of the codes and compare scores
+    import torch
+    qf = torch.from_numpy(qc).view(torch.float8_e4m3fn).double().numpy() * qs[..., None]
+    kf = torch.from_numpy(kc).view(torch.float8_e4m3fn).double().numpy() * ks[:, None]
+    for t in range(T):
+        for j in range(L):
+            want = sum(w[t, h] * max(float(np.dot(qf[t, h], kf[j])), 0.0) for h in range(H))
+            assert abs(got[t, j] - want) <= 1e-12 * (1 + abs(want))
+    # the same keys and row scales through a reversed page table (block size 3)
+    perm = np.array([2, 0, 1])
+    pool = np.concatenate([kc[3 * p:3 * p + 3] for p in np.argsort(perm)])
+    pool_s = np.concatenate([ks[3 * p:3 * p + 3] for p in np.argsort(perm)])
+    table = perm[None, :].astype(np.int32)
+    got_p = _logits(orc, qc, w, pool, 1, T, np.array([L]), causal=False, q_scale=qs,
+                    k_scale=pool_s, dtype="e4m3", table=table, bs=3)
+    assert np.array_equal(got_p, got)
+
+
+# --------------------------------------------------------------------------- top-k
+
+def check_topk_hand(orc):
+    for row, k, expect in load_topk_cases():
+        idx, val = orc.topk_select(row[None, :], k)
+        assert np.array_equal(idx[0], expect), (row, k, idx[0], expect)
+
+
+def _brute_topk(row, k):
+    """Selection by pairwise dominance: i ranks before j iff v_i > v_j or
+    (v_i == v_j and i < j); rank = number of candidates ranking before."""
+    cand = [j for j in range(len(row)) if row[j] != -np.inf]
+    rank = {}
+    for a in cand:
+        rank[a] = sum(1 for b in cand if row[b] > row[a] or (row[b] == row[a] and b < a))
+    out = [-1] * k
+    for a, rk in rank.items():
+        if rk < k:
+            out[rk] = a
+    return out
+
+
+def check_topk_bruteforce(orc, seed=8):
+    r = np.random.default_rng(seed)
+    # every ordering of a small multiset with ties, -0/+0 and -inf
+    base = [2.0, 2.0, -0.0, 0.0, -np.inf, 1.5]
+    for perm in set(itertools.permutations(range(len(base)))):
+        row = np.array([base[p] for p in perm])
+        for k in (1, 3, 6, 7):
+            idx, _ = orc.topk_select(row[None, :], k)
+            assert list(idx[0]) == _brute_topk(row, k)
+    for trial in range(200):
+        K = int(r.integers(1, 65))
+        k = int(r.integers(1, 17))
+        row = r.integers(-3, 4, K).astype(np.float64)
+        row[r.random(K) < 0.2] = -np.inf
+        idx, val = orc.topk_select(row[None, :], k)
+        assert list(idx[0]) == _brute_topk(row, k)
+        live = idx[0] >= 0
+        assert np.array_equal(val[0][live], row[idx[0][live]])
+
+
+ALL_CHECKS = [
+    check_bf16_decode, check_e4m3_decode, check_bf16_rounding, check_e8m0, check_e2m1,
+    check_mxfp4_hand_rows, check_mxfp4_gather_hand, check_gather_invariant,
+    check_logits_hand, check_logits_plain_matmul, check_logits_special,
+    check_logits_invariances, check_logits_e4m3, check_topk_hand, check_topk_bruteforce,
+]
