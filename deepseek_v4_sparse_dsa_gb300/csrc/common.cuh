@@ -1,0 +1,353 @@
+// Device-side building blocks shared by the kernels of this library (sm_103a).
+//
+//  * per-translation-unit error word and wait limit (see dsa.h, dsa_device_error);
+//  * bounded mbarrier waits (time limit read from %globaltimer, never a hang);
+//  * TMA (cp.async.bulk.tensor) and tcgen05 (MMA into tensor memory) wrappers;
+//  * the ranking key of the top-k tie rule and a shared-memory top-k engine
+//    (candidate buffer + radix select + bitonic sort) used by the fused indexer,
+//    the standalone top-k and the merge of partial top-k lists.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// ---------------------------------------------------------------------------------
+// Error word and wait limit.  Each translation unit has its own copy (no relocatable
+// device code); the host reads and clears all of them in dsa_device_error.
+// ---------------------------------------------------------------------------------
+static __device__ unsigned int g_error_word;
+static __device__ unsigned long long g_wait_limit_ns;
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
+constexpr unsigned long long kCleanupWaitNs = 2000000000ull;   // waits for own copies on abort
+
+__device__ __forceinline__ void raise_error(unsigned int bits) { atomicOr(&g_error_word, bits); }
+
+__device__ __forceinline__ unsigned long long wait_limit_ns() {
+  unsigned long long v = *(volatile unsigned long long*)&g_wait_limit_ns;
+  return v == 0 ? kDefaultWaitNs : v;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------------
+// Shared-memory addresses and mbarriers
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits until the phase with the given parity has completed.  Gives up after
+// `limit_ns` (or as soon as *abort becomes non-zero) and returns false; the caller
+// then abandons its work.  Never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns,
+                                          const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// TMA
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// 2-D tiled load of the box at (x = inner element, y = row) into shared memory,
+// completing `bytes` of transaction count on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int32_t x,
+                                            int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored with the 128-byte
+// swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms packed back to back.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+  d |= (uint64_t)(16u >> 4) << 16;                 // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024u >> 4) << 32;               // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                          // descriptor version
+  d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptors: fp32 accumulate, both operands K-major, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_e4m3(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on an mbarrier once every tcgen05 operation issued so far by this thread is done.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Each thread of the warp reads 64 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]),
+        "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+        "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+        "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------------------------
+// Ranking key of the tie rule: larger value first, then smaller index.
+// High 32 bits: order-preserving image of the fp32 value (-0.0 folded onto +0.0);
+// low 32 bits: ~index.  Distinct indices give distinct keys; every real candidate
+// has a key > 0, so 0 marks an empty slot.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ float canon_zero(float v) {
+  return __float_as_uint(v) == 0x80000000u ? 0.0f : v;
+}
+
+__device__ __forceinline__ uint32_t ord_f32(float v) {
+  uint32_t u = __float_as_uint(canon_zero(v));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float f32_of_ord(uint32_t o) {
+  uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ uint64_t rank_key(float v, uint32_t j) {
+  return ((uint64_t)ord_f32(v) << 32) | (uint64_t)(~j);
+}
+
+__device__ __forceinline__ int32_t index_of_key(uint64_t key) { return (int32_t)(~(uint32_t)key); }
+__device__ __forceinline__ float value_of_key(uint64_t key) { return f32_of_ord((uint32_t)(key >> 32)); }
+
+// -inf and NaN are never candidates.
+__device__ __forceinline__ bool is_candidate(float v) { return v > -INFINITY; }
+
+// ---------------------------------------------------------------------------------
+// Shared-memory top-k engine.  Run by a group of 256 threads that synchronise on
+// named barrier 1 (`tid` = 0..255 within the group).
+// ---------------------------------------------------------------------------------
+constexpr int kEngineThreads = 256;
+
+__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+struct EngineScratch {
+  uint32_t hist[256];
+  uint32_t pick[4];
+};
+
+// Appends `key` to buf[*cnt] when `take` is set; warp-aggregated atomics.  All 32
+// lanes of the warp must call it together.
+__device__ __forceinline__ void engine_append(uint64_t* buf, uint32_t* cnt, uint64_t key, bool take) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
+  if (m == 0) return;
+  uint32_t base = 0;
+  const uint32_t leader = __ffs(m) - 1;
+  if (lane == leader) base = atomicAdd(cnt, (uint32_t)__popc(m));
+  base = __shfl_sync(0xFFFFFFFFu, base, leader);
+  if (take) buf[base + __popc(m & ((1u << lane) - 1u))] = key;
+}
+
+// Smallest key T such that exactly k of the n (> k) distinct keys in buf are >= T
+// (the k-th largest key, or a lower bound of it sharing all bits that decide the
+// set).  Most-significant-digit-first radix select over 8-bit digits.
+static __device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScratch* sc, int tid) {
+  uint64_t prefix = 0, mask = 0;
+  uint32_t need = (uint32_t)k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    sc->hist[tid] = 0;
+    group_sync();
+    for (int e = tid; e < n; e += kEngineThreads) {
+      const uint64_t key = buf[e];
+      if ((key & mask) == prefix) atomicAdd(&sc->hist[(uint32_t)(key >> shift) & 255u], 1u);
+    }
+    group_sync();
+    if (tid < 32) {
+      // lane l covers digits 255-8l .. 248-8l, scanned from the top
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = sc->hist[255 - 8 * tid - i];
+        sum += c[i];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (tid >= o) incl += y;
+      }
+      const uint32_t excl = incl - sum;
+      if (excl < need && need <= incl) {
+        uint32_t above = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (above < need && need <= above + c[i]) {
+            sc->pick[0] = 255u - 8u * tid - i;
+            sc->pick[1] = above;
+            sc->pick[2] = c[i];
+          }
+          above += c[i];
+        }
+      }
+    }
+    group_sync();
+    const uint32_t d = sc->pick[0], above = sc->pick[1], inbin = sc->pick[2];
+    need -= above;
+    prefix |= (uint64_t)d << shift;
+    mask |= (uint64_t)0xFF << shift;
+    if (inbin == need) break;      // every key with this prefix belongs to the set
+  }
+  group_sync();                    // everyone has read pick[] before it is reused
+  return prefix;
+}
+
+// Keeps the keys >= thr of buf[0, n), packed to the front; *cnt becomes their
+// number.  MAXPER >= ceil(n / 256).
+template <int MAXPER>
+__device__ void engine_compact(uint64_t* buf, uint32_t* cnt, int n, uint64_t thr, int tid) {
+  uint64_t keep[MAXPER];
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i) {
+    const int e = tid + i * kEngineThreads;
+    keep[i] = (e < n) ? buf[e] : 0ull;
+  }
+  group_sync();
+  if (tid == 0) *cnt = 0;
+  group_sync();
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i) engine_append(buf, cnt, keep[i], keep[i] != 0ull && keep[i] >= thr);
+  group_sync();
+}
+
+// Sorts nlist lists in place, each of P (power of two) keys at buf + l * stride,
+// in descending key order (rank order).  Slots past a list's count must hold 0.
+static __device__ void engine_sort(uint64_t* buf, int stride, int nlist, int P, int tid) {
+  const int pairs = P >> 1;
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int half = size >> 1; half > 0; half >>= 1) {
+      for (int t = tid; t < pairs * nlist; t += kEngineThreads) {
+        const int l = t / pairs, u = t - l * pairs;
+        const int i = 2 * u - (u & (half - 1));
+        const int j = i + half;
+        uint64_t* b = buf + (size_t)l * stride;
+        const uint64_t x = b[i], y = b[j];
+        const bool desc = (i & size) == 0;
+        if ((x < y) == desc) {
+          b[i] = y;
+          b[j] = x;
+        }
+      }
+      group_sync();
+    }
+  }
+}
+
+__host__ __device__ constexpr int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace dsa

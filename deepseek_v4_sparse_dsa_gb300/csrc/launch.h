@@ -1,0 +1,98 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernel translation
+// units.  Not installed; callers use include/dsa.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+void note_launch();      // counts one kernel launch (dsa_launch_count)
+int device_sm_count();   // SMs of the current device (cached per device)
+
+// ------------------------------------------------------------------ indexer (indexer.cu)
+struct IndexerPlan {
+  int nq;            // query rows per work item (1, 2 or 4)
+  int stages;        // key-tile pipeline depth
+  int chunk;         // keys per work item (multiple of 128)
+  int nchunks;       // ceil(max_context_len / chunk)
+  int ngroups;       // ceil(next_n / nq)
+  int cap;           // candidate-buffer capacity per query row (top-k mode)
+  int pow2;          // next power of two >= topk
+  size_t smem;       // dynamic shared memory per CTA
+  int64_t items;     // grid size
+  size_t ws_bytes;   // workspace for partial lists (0 when nchunks == 1)
+  bool ok;           // false: shape does not fit this build
+};
+
+// topk == 0 plans the logits-only kernel.
+IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk);
+
+struct IndexerArgs {
+  const void* q;
+  const float* q_scale;
+  bool fp8;
+  const float* weights;
+  dsa_keys keys;
+  dsa_queries qs;
+  // logits mode
+  float* logits;
+  int64_t ld;
+  // top-k mode
+  int topk;
+  int32_t* out_idx;
+  float* out_val;
+  void* ws;
+};
+
+cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& plan, cudaStream_t stream);
+
+// ------------------------------------------------------------------ top-k (topk.cu)
+struct TopkPlan {
+  int chunk;         // logits per CTA
+  int nchunks;
+  int cap;
+  int pow2;
+  size_t smem;
+  size_t ws_bytes;
+};
+
+TopkPlan plan_topk(const dsa_queries& qs, int topk);
+
+cudaError_t launch_topk(const float* logits, int64_t ld, const dsa_queries& qs, int topk, int32_t* out_idx,
+                        float* out_val, void* ws, const TopkPlan& plan, cudaStream_t stream);
+
+// Merges nchunks partial lists per row (ws layout [T][nchunks][topk] of ranking keys,
+// 0 = empty) into the final top-k.  Row t reads its first ceil(vis_t / chunk) lists.
+cudaError_t launch_merge(const uint64_t* partial, int nchunks, int chunk, const dsa_queries& qs, int topk,
+                         int32_t* out_idx, float* out_val, cudaStream_t stream);
+
+// ------------------------------------------------------------------ gather (gather.cu)
+cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_t num_blocks, int bs,
+                                const int32_t* table, int64_t bt_stride, const int32_t* sel, int next_n,
+                                int topk, int64_t rows, uint16_t* out, int num_sms, cudaStream_t stream);
+
+// ------------------------------------------------------------------ per-TU device words
+#define DSA_DECLARE_TU_ERROR_ACCESSORS(name)                                        \
+  cudaError_t tu_##name##_read_clear_error(unsigned int* out);                      \
+  cudaError_t tu_##name##_set_wait_limit(unsigned long long ns);
+
+#define DSA_DEFINE_TU_ERROR_ACCESSORS(name)                                         \
+  cudaError_t tu_##name##_read_clear_error(unsigned int* out) {                     \
+    unsigned int zero = 0;                                                          \
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_error_word, sizeof(unsigned int));  \
+    if (e != cudaSuccess) return e;                                                 \
+    return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned int));           \
+  }                                                                                 \
+  cudaError_t tu_##name##_set_wait_limit(unsigned long long ns) {                   \
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns));                    \
+  }
+
+DSA_DECLARE_TU_ERROR_ACCESSORS(gather)
+DSA_DECLARE_TU_ERROR_ACCESSORS(indexer)
+DSA_DECLARE_TU_ERROR_ACCESSORS(topk)
+
+}  // namespace dsa

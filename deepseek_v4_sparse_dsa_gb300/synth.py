@@ -124,7 +124,7 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 def normal_bf16(rng: Rng, shape, stream: str) -> np.ndarray:
     out = np.empty(shape, dtype=np.uint16)
     flat = out.reshape(-1)
-    tmp = np.empty(min(flat.size, 2 * _CHUNK), dtype=np.float32)
+    tmp = np.empty(max(1, min(flat.size, 2 * _CHUNK)), dtype=np.float32)
     # Draw in slices so multi-GB key pools never hold a float64 copy.
     step = tmp.size
     for s0 in range(0, flat.size, step):
@@ -256,26 +256,29 @@ def make_tiny(seed: int = 1, T: int = 64, L: int = 2048, topk: int = 512) -> Wor
 
 
 def make_decode(seed: int, B: int, next_n: int, lmin: int, lmax: int, topk: int,
-                name: str, pad_frac: float, block_size: int = 64) -> Workload:
-    """Paged bf16 decode batch: B sequences, next_n causal query tokens each."""
+                name: str, pad_frac: float, block_size: int = 64, with_keys: bool = True) -> Workload:
+    """Paged bf16 decode batch: B sequences, next_n causal query tokens each.
+    with_keys=False leaves the bf16 key pool empty (for gather-only use)."""
     rng = Rng(seed)
     lens = rng.integers(lmin, lmax, B, "context_lens").astype(np.int32)
     table, nblk = _page_pool(rng, lens, block_size, "block_table")
     T = B * next_n
     q = normal_bf16(rng, (T, H, D), "q")
-    k = normal_bf16(rng, (nblk * block_size, D), "k_pool")
+    k = normal_bf16(rng, (nblk * block_size if with_keys else 0, D), "k_pool")
     w = _weights(rng, T, "w")
     fp4, sc = _mxfp4_pool(rng, nblk, block_size, "cache")
     return Workload(name, B, next_n, lens, True, topk, "bf16", q, None, w, k, None, table,
                     block_size, fp4, sc, table, pad_frac, seed)
 
 
-def make_flash_decode(seed: int = 2, B: int = 64, lmin: int = 4096, lmax: int = 65536) -> Workload:
-    return make_decode(seed, B, 1, lmin, lmax, 512, "flash_decode", 0.0)
+def make_flash_decode(seed: int = 2, B: int = 64, lmin: int = 4096, lmax: int = 65536,
+                      with_keys: bool = True) -> Workload:
+    return make_decode(seed, B, 1, lmin, lmax, 512, "flash_decode", 0.0, with_keys=with_keys)
 
 
-def make_pro_mtp(seed: int = 3, B: int = 32, lmin: int = 32768, lmax: int = 131072) -> Workload:
-    return make_decode(seed, B, 2, lmin, lmax, 1024, "pro_mtp", 0.02)
+def make_pro_mtp(seed: int = 3, B: int = 32, lmin: int = 32768, lmax: int = 131072,
+                 with_keys: bool = True) -> Workload:
+    return make_decode(seed, B, 2, lmin, lmax, 1024, "pro_mtp", 0.02, with_keys=with_keys)
 
 
 def make_prefill(seed: int = 4, T: int = 16384, topk: int = 512) -> Workload:

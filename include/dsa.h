@@ -1,0 +1,200 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DeepSeek-V4 DSA indexer hot path.
+ *
+ * The library computes, on one GPU, the three stages of the DeepSeek-V4
+ * sparse-attention indexer:
+ *
+ *   1. the indexer score  logits[t, j] = sum_h w[t, h] * relu(q[t, h, :] . k[j, :])
+ *      (xkernels issue #27 "DSA indexer + attention: validate/provide gfx942
+ *      forward path", comment 2 "What shipped"; H = index_n_heads = 64,
+ *      D = index_head_dim = 128 per the same issue's "Context");
+ *   2. a per-query top-k under a fixed tie rule (larger value first, then the
+ *      smaller key index), the deterministic "canonical" top-k sort of README
+ *      "DeepSeek V4 Flash on a single AMD MI300X" (overlay table);
+ *   3. the paged mxfp4 gather of the selected positions to bf16 (xkernels
+ *      issue #28 "DeepSeek-V4 serving support -- tracking", comment 2 "What it
+ *      does").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is caller-owned DEVICE memory unless stated
+ *   otherwise.  No call allocates or frees memory, synchronises, or keeps a
+ *   pointer after it returns.  Calls are asynchronous on `stream` (a
+ *   cudaStream_t passed as void*; NULL = the legacy default stream) and run on
+ *   the device current to the calling thread.
+ * - Query rows: T = B * next_n.  Row t belongs to sequence b = t / next_n and is
+ *   query i = t % next_n of it, at absolute position p = L_b - next_n + i, where
+ *   L_b = context_lens[b].  With causal != 0 the row sees keys j <= p (and
+ *   j < L_b); otherwise every j < L_b.  This is this library's reading of the
+ *   "optional per-query causal window" of xkernels issue #27, comment 2.
+ * - Host-detectable argument errors return DSA_ERR_INVALID_ARG (or
+ *   DSA_ERR_UNSUPPORTED for valid but unimplemented shapes) BEFORE anything is
+ *   launched; outputs are then untouched.  A failed launch returns DSA_ERR_CUDA.
+ * - Bad indices found on the device (a block id outside [0, num_blocks), a
+ *   block-table column outside [0, bt_stride)) never cause an out-of-range
+ *   access: the affected key is treated as masked (not selected, logit -inf) or
+ *   the gathered row is written as zeros, and a bit is set in the per-device
+ *   error word read by dsa_device_error().  A device-side wait that exceeds its
+ *   time limit abandons the call's work, sets DSA_DEVERR_TIMEOUT in the same
+ *   word and returns without hanging; outputs of that call are then undefined.
+ * - v1 supports H = 64 and D = 128 (DSA_ERR_UNSUPPORTED otherwise); they stay
+ *   parameters so the ABI does not change when other shapes are added.
+ */
+#ifndef DSA_GB300_H_
+#define DSA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,   /* bad pointer / size / stride / alignment      */
+  DSA_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement  */
+  DSA_ERR_CUDA = 3,          /* a CUDA runtime or launch error               */
+  DSA_ERR_WORKSPACE = 4      /* ws is NULL or smaller than dsa_workspace_bytes */
+} dsa_status;
+
+typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1 } dsa_dtype;
+
+typedef enum { DSA_OP_TOPK = 1, DSA_OP_LOGITS_TOPK = 2 } dsa_op;
+
+/* Bits of the per-device error word (see dsa_device_error). */
+#define DSA_DEVERR_INDEX   1u   /* a block id / block-table column was out of range */
+#define DSA_DEVERR_TIMEOUT 2u   /* a bounded device-side wait expired               */
+
+/*
+ * Key source of the indexer (the shared MQA key of xkernels issue #27,
+ * comment 2).  Keys are rows of D elements, row-major, d fastest; each row
+ * starts 16-byte aligned (D * element size is a multiple of 16).
+ *  - Paged (block_table != NULL): `data` is a pool of num_rows rows (num_rows =
+ *    number of physical blocks * block_size).  Logical key j of sequence b is
+ *    pool row block_table[b * bt_stride + j / block_size] * block_size +
+ *    j % block_size.  block_size must be a multiple of 8 that divides 128 or is
+ *    a multiple of 128; bt_stride >= ceil(L_b / block_size) for every b.
+ *  - Contiguous (block_table == NULL): only B == 1; key j is row j, num_rows >= L_0.
+ * `scale` is the per-row fp32 scale of E4M3 keys (same row indexing as `data`,
+ * non-negative), NULL for bf16.
+ */
+typedef struct {
+  const void* data;
+  const float* scale;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int32_t block_size;
+  int64_t num_rows;
+} dsa_keys;
+
+/*
+ * Query batch layout.  context_lens is DEVICE memory [B] (int32, 0 <= L_b <=
+ * max_context_len); max_context_len is a host-side upper bound used to size
+ * launches and the logits width.
+ */
+typedef struct {
+  int32_t B;
+  int32_t next_n;
+  const int32_t* context_lens;
+  int32_t max_context_len;
+  int32_t causal;
+} dsa_queries;
+
+/*
+ * dsa_indexer_logits -- indexer score (xkernels issue #27, comment 2 "What
+ * shipped"): logits[t * ld_logits + j] = sum_h weights[t*H + h] *
+ * relu(qv[t,h,:] . kv[j,:]) for every visible key j, -inf for every other j in
+ * [0, max_context_len).  Columns >= max_context_len are not written.
+ *  q        [T, H, D] bf16 (dtype DSA_BF16) or E4M3 codes (DSA_E4M3), row-major.
+ *  q_scale  [T, H] fp32, non-negative (E4M3 only, else NULL): qv = q * q_scale[t,h].
+ *  weights  [T, H] fp32.
+ *  keys     see dsa_keys; kv = k (bf16) or k * scale[row] (E4M3).
+ *  logits   [T, ld_logits] fp32, ld_logits >= max_context_len.
+ * Arithmetic: bf16 or E4M3 products summed in fp32 by the tensor cores, then
+ * ReLU, weight and head sum in fp32 in a fixed order (heads 0..63 in four
+ * interleaved partial sums), then -0.0 is written as +0.0.  Given the same
+ * inputs the scores are bit-identical to those dsa_indexer_logits_topk ranks.
+ */
+dsa_status dsa_indexer_logits(const void* q, const float* q_scale, dsa_dtype dtype,
+                              const float* weights, int H, int D, dsa_keys keys,
+                              dsa_queries qs, float* logits, int64_t ld_logits,
+                              void* stream);
+
+/*
+ * dsa_indexer_topk -- per-row top-k of a logits matrix laid out as
+ * dsa_indexer_logits writes it.  Only the visible keys of row t (per `qs`) are
+ * candidates; -inf and NaN values are never selected.  out_idx[t * topk + s]
+ * (int32) lists the selected key indices in rank order: larger value first,
+ * ties to the smaller index, -0.0 equal to +0.0; rows with fewer than topk
+ * candidates are padded with -1.  out_val (nullable) receives the matching
+ * values (-inf in padded slots).  1 <= topk <= 2048.
+ *  ws / ws_bytes: device scratch of at least dsa_workspace_bytes(DSA_OP_TOPK,
+ *  DSA_BF16, qs, topk) bytes (may be 0, then ws may be NULL); its contents on
+ *  entry do not matter.
+ */
+dsa_status dsa_indexer_topk(const float* logits, int64_t ld_logits, dsa_queries qs, int topk,
+                            int32_t* out_idx, float* out_val, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/*
+ * dsa_indexer_logits_topk -- dsa_indexer_topk(dsa_indexer_logits(...)) in one
+ * pass that never writes the T x max_context_len logits to memory: the scores
+ * are ranked on chip as the tensor cores produce them.  Arguments as for the
+ * two calls above; the result is bit-identical to running them in sequence.
+ * ws: at least dsa_workspace_bytes(DSA_OP_LOGITS_TOPK, dtype, qs, topk) bytes
+ * (partial top-k lists of key ranges; contents on entry do not matter).
+ */
+dsa_status dsa_indexer_logits_topk(const void* q, const float* q_scale, dsa_dtype dtype,
+                                   const float* weights, int H, int D, dsa_keys keys,
+                                   dsa_queries qs, int topk, int32_t* out_idx, float* out_val,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * mxfp4_paged_gather -- xkernels issue #28, comment 2 "What it does": for every
+ * query row t and slot s, pos = sel_pos[t * topk + s];
+ *   pos < 0  -> out row is 128 x bf16 +0.0 (a padded slot);
+ *   else     -> cache row (blk, off) = (block_table[b * bt_stride + pos / block_size],
+ *               pos % block_size) with b = t / next_n, dequantised to bf16:
+ *               element e = E2M1(nibble e) * 2^(kv_scale[row][e / 32] - 127),
+ *               scale byte 0xFF -> 0 (the sign of the zero follows the nibble),
+ *               rounded to nearest-even bf16 (exact except overflow -> inf).
+ *  kv_fp4   [num_blocks, block_size, D/2] bytes; byte i of a row holds element
+ *           2i in its low nibble and 2i+1 in its high nibble (E2M1: sign bit 3,
+ *           two exponent bits, one mantissa bit).
+ *  kv_scale [num_blocks, block_size, D/32] E8M0 bytes.
+ *  out      [T, topk, D] bf16 bit patterns, row-major.
+ * A block id outside [0, num_blocks) or pos / block_size >= bt_stride gives a
+ * zero row and sets DSA_DEVERR_INDEX.  D must be 128 (DSA_ERR_UNSUPPORTED
+ * otherwise); block_size >= 1.
+ */
+dsa_status mxfp4_paged_gather(const uint8_t* kv_fp4, const uint8_t* kv_scale, int64_t num_blocks,
+                              int block_size, int D, const int32_t* block_table, int64_t bt_stride,
+                              const int32_t* sel_pos, int B, int next_n, int topk,
+                              uint16_t* out, void* stream);
+
+/* Workspace bytes the op needs for this batch shape (host only, no device work). */
+size_t dsa_workspace_bytes(dsa_op op, dsa_dtype dtype, dsa_queries qs, int topk);
+
+/* Static text for a status code. */
+const char* dsa_status_string(dsa_status status);
+
+/* Synchronises `stream`, then returns and clears the current device's error
+ * word (DSA_DEVERR_* bits; 0 = no device-side error since the last read).
+ * Returns -1 if the synchronisation or the read fails. */
+int dsa_device_error(void* stream);
+
+/* Number of kernels this library has launched in this process (all threads,
+ * all devices); lets a caller count the launches inside a timed region. */
+uint64_t dsa_launch_count(void);
+
+/* Sets the limit, in nanoseconds, of every bounded device-side wait launched
+ * after this call on the current device (default 2 s; 0 restores the
+ * default).  Returns DSA_ERR_CUDA if the device symbol cannot be written. */
+dsa_status dsa_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H_ */

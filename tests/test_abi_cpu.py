@@ -1,0 +1,125 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every entry point the
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import os
+import re
+
+import pytest
+
+from deepseek_v4_sparse_dsa_gb300 import dsa
+from deepseek_v4_sparse_dsa_gb300 import build as dsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    srcs = [os.path.join(dsa_build.CSRC, s) for s in os.listdir(dsa_build.CSRC)]
+    newest = max(os.path.getmtime(p) for p in srcs + [HEADER])
+    if not os.path.exists(dsa.LIB_PATH) or os.path.getmtime(dsa.LIB_PATH) < newest:
+        dsa_build.build()
+    return dsa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \t\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["dsa_indexer_logits", "dsa_indexer_topk", "dsa_indexer_logits_topk", "mxfp4_paged_gather",
+              "dsa_workspace_bytes", "dsa_status_string", "dsa_device_error"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert dsa.status_string(s) not in ("", "unknown status")
+    assert dsa.status_string(99) == "unknown status"
+
+
+def _qs(B=1, n=1, L=4096, causal=True):
+    return dsa.make_queries(B, n, 0x1000, L, causal)
+
+
+def test_workspace_plans_are_host_only(lib):
+    # decode-shaped batches split each row's keys and need partial lists
+    flash = dsa.make_queries(64, 1, 0x1000, 65536, True)
+    n = dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, flash, 512)
+    assert n > 0 and n % (64 * 512 * 8) == 0
+    # a prefill-sized batch of query groups needs none
+    prefill = dsa.make_queries(1, 16384, 0x1000, 16384, True)
+    assert dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, prefill, 512) == 0
+    assert dsa.dsa_workspace_bytes(dsa.DSA_OP_TOPK, dsa.DSA_BF16, prefill, 512) == 0
+    assert dsa.dsa_workspace_bytes(dsa.DSA_OP_TOPK, dsa.DSA_BF16, flash, 512) > 0
+    assert dsa.dsa_workspace_bytes(dsa.DSA_OP_TOPK, dsa.DSA_BF16, flash, 0) == 0
+    assert dsa.dsa_workspace_bytes(dsa.DSA_OP_TOPK, dsa.DSA_BF16, flash, 4096) == 0
+
+
+FAKE = 0x100000  # 1 MiB-aligned address: passes alignment checks, never dereferenced
+
+
+def _status(fn, *args):
+    try:
+        fn(*args)
+    except dsa.DsaError as e:
+        return e.status
+    return dsa.DSA_OK
+
+
+def test_host_side_rejections_launch_nothing(lib):
+    before = dsa.dsa_launch_count()
+    keys = dsa.dsa_keys(FAKE, None, None, 0, 0, 4096)
+    qs = _qs()
+    s = 0  # stream handle, never used on a rejected call
+    # unsupported head count / head dim
+    assert _status(dsa.dsa_indexer_logits, FAKE, None, dsa.DSA_BF16, FAKE, 32, 128, keys, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_UNSUPPORTED
+    assert _status(dsa.dsa_indexer_logits, FAKE, None, dsa.DSA_BF16, FAKE, 64, 64, keys, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_UNSUPPORTED
+    # null q, misaligned q, ld too small
+    assert _status(dsa.dsa_indexer_logits, None, None, dsa.DSA_BF16, FAKE, 64, 128, keys, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    assert _status(dsa.dsa_indexer_logits, FAKE + 2, None, dsa.DSA_BF16, FAKE, 64, 128, keys, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    assert _status(dsa.dsa_indexer_logits, FAKE, None, dsa.DSA_BF16, FAKE, 64, 128, keys, qs, FAKE, 100, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    # E4M3 without scales
+    assert _status(dsa.dsa_indexer_logits, FAKE, None, dsa.DSA_E4M3, FAKE, 64, 128, keys, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    # contiguous keys with more than one sequence
+    assert _status(dsa.dsa_indexer_logits, FAKE, None, dsa.DSA_BF16, FAKE, 64, 128, keys, _qs(B=2), FAKE,
+                   4096, s) == dsa.DSA_ERR_INVALID_ARG
+    # paged keys with an unsupported block size
+    bad = dsa.dsa_keys(FAKE, None, FAKE, 64, 12, 4096 * 12)
+    assert _status(dsa.dsa_indexer_logits, FAKE, None, dsa.DSA_BF16, FAKE, 64, 128, bad, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_UNSUPPORTED
+    # top-k bounds
+    for k in (0, 2049):
+        assert _status(dsa.dsa_indexer_topk, FAKE, 4096, qs, k, FAKE, None, None, 0, s) == dsa.DSA_ERR_INVALID_ARG
+        assert _status(dsa.dsa_indexer_logits_topk, FAKE, None, dsa.DSA_BF16, FAKE, 64, 128, keys, qs, k, FAKE,
+                       None, None, 0, s) == dsa.DSA_ERR_INVALID_ARG
+    # split top-k without a workspace
+    flash = dsa.make_queries(64, 1, FAKE, 65536, True)
+    assert _status(dsa.dsa_indexer_topk, FAKE, 65536, flash, 512, FAKE, None, None, 0, s) == dsa.DSA_ERR_WORKSPACE
+    pkeys = dsa.dsa_keys(FAKE, None, FAKE, 1024, 64, 1 << 20)
+    assert _status(dsa.dsa_indexer_logits_topk, FAKE, None, dsa.DSA_BF16, FAKE, 64, 128, pkeys, flash, 512, FAKE,
+                   None, FAKE, 16, s) == dsa.DSA_ERR_WORKSPACE
+    # gather: head dim, misaligned output, bad sizes
+    assert _status(dsa.mxfp4_paged_gather, FAKE, FAKE, 8, 64, 64, FAKE, 8, FAKE, 1, 1, 4, FAKE, s) \
+        == dsa.DSA_ERR_UNSUPPORTED
+    assert _status(dsa.mxfp4_paged_gather, FAKE, FAKE, 8, 64, 128, FAKE, 8, FAKE, 1, 1, 4, FAKE + 8, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    assert _status(dsa.mxfp4_paged_gather, FAKE, FAKE, 8, 0, 128, FAKE, 8, FAKE, 1, 1, 4, FAKE, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    # empty problems are valid no-ops
+    assert _status(dsa.mxfp4_paged_gather, None, None, 0, 64, 128, None, 0, None, 0, 1, 512, None, s) == dsa.DSA_OK
+    assert dsa.dsa_launch_count() == before
