@@ -1,0 +1,401 @@
+"""Benchmark of the DSA indexer hot path on GB300.
+
+One step = the whole path over one batch: the fused indexer score + top-k
+(dsa_indexer_logits_topk) followed by the paged mxfp4 gather of the selected rows
+(mxfp4_paged_gather).  Default workload: the Flash decode batch (64 sequences, one
+query token each, context lengths uniform in [4096, 65536], paged bf16 keys,
+top-512, gather of 512 rows per query).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a bounded
+sample of the same workload.  Under torchrun each rank runs its own batch (weak
+scaling, no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "indexer query-tokens/s (logits+top-k), gather GB/s; % of roofline, 1×GB300"
+UNIT = "query-tokens/s"
+L2_BYTES = 129 * 2**20
+
+WORKLOADS = {
+    "flash_decode": dict(desc="64 seq x 1 query, L~U[4096,65536], paged bf16 keys bs=64, top-512, "
+                              "mxfp4 gather of 512 rows/query", seed=2),
+    "pro_mtp": dict(desc="32 seq x 2 queries (causal), L~U[32768,131072], paged bf16 keys bs=64, "
+                         "top-1024, mxfp4 gather of 1024 rows/query", seed=3),
+    "prefill": dict(desc="1 seq, T=K=16384, causal, contiguous bf16 keys, fused top-512 (no gather)",
+                    seed=4),
+    "fp8_chunked": dict(desc="1 seq, 8192 E4M3 queries at 57344..65535 over 65536 E4M3 keys, causal, "
+                             "top-1024, mxfp4 gather of every selection", seed=5),
+}
+
+
+def make_workload(name: str, seed: int):
+    from deepseek_v4_sparse_dsa_gb300 import synth
+    return {"flash_decode": synth.make_flash_decode, "pro_mtp": synth.make_pro_mtp,
+            "prefill": synth.make_prefill, "fp8_chunked": synth.make_fp8_chunked}[name](seed=seed)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("common.cuh", "indexer.cu", "topk.cu", "gather.cu"):
+        with open(os.path.join(ROOT, "deepseek_v4_sparse_dsa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the fused call from a committed ncu summary, if it was
+    taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("src_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def algorithmic_work(wl):
+    """Bytes / flops one fused call and one gather must move or do (masked work excluded)."""
+    vis = wl.visible_len().astype(np.int64)
+    T, k = wl.T, wl.topk
+    elt = 1 if wl.dtype == "e4m3" else 2
+    L = wl.context_lens.astype(np.int64)
+    key_bytes = int(L.sum()) * 128 * elt + (int(L.sum()) * 4 if wl.dtype == "e4m3" else 0)
+    q_bytes = T * 64 * 128 * elt + T * 64 * 4 + (T * 64 * 4 if wl.dtype == "e4m3" else 0)
+    fused_bytes = key_bytes + q_bytes + T * k * 8 + wl.B * 4
+    flops = 2 * 64 * 128 * int(vis.sum())
+    gather_rows = T * k
+    gather_bytes = gather_rows * (68 + 256) + gather_rows * 4
+    return dict(fused_bytes=fused_bytes, flops=flops, gather_bytes=gather_bytes)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"dsa_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[2]), max=float(parts[3]), power=float(parts[4]),
+                                     hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0}
+        load = [r for r in rows if r["power"] > 300] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["max"] for r in load),
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import torch
+
+    from deepseek_v4_sparse_dsa_gb300 import dsa
+    from deepseek_v4_sparse_dsa_gb300.device import DeviceBatch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dsa.load()
+    info = WORKLOADS[args.workload]
+    wl = make_workload(args.workload, info["seed"] + rank)
+    db = DeviceBatch.from_workload(wl, dev)
+    stream = torch.cuda.current_stream(dev)
+    T, k = wl.T, wl.topk
+    has_gather = wl.kv_fp4 is not None
+    ws = db.workspace(dsa.DSA_OP_LOGITS_TOPK, k)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gout = torch.empty((T, k, 128), dtype=torch.int16, device=dev) if has_gather else None
+    work = algorithmic_work(wl)
+
+    def step():
+        db.logits_topk(k, ws=ws, out_idx=idx, with_values=False, stream=stream)
+        if has_gather:
+            db.gather(idx, out=gout, stream=stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    # keep the GPU busy for ~1 s before the timed region so clocks settle and get sampled
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize(dev)
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches0 = dsa.dsa_launch_count()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        db.logits_topk(k, ws=ws, out_idx=idx, with_values=False, stream=stream)
+        ev[i][1].record(stream)
+        if has_gather:
+            db.gather(idx, out=gout, stream=stream)
+        ev[i][2].record(stream)
+    t1.record(stream)
+    barrier()
+    launches = dsa.dsa_launch_count() - launches0
+    clocks = sampler.stop()
+    assert dsa.dsa_device_error(stream) == 0
+    total_ms = t0.elapsed_time(t1)
+    fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    gather_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) if has_gather else 0.0
+
+    # end to end through the public API: pinned host inputs in, results back to pinned host
+    h_q = db.q.cpu().pin_memory()
+    h_w = db.weights.cpu().pin_memory()
+    h_qs = db.q_scale.cpu().pin_memory() if db.q_scale is not None else None
+    h_lens = db.context_lens.cpu().pin_memory()
+    h_bt = db.block_table.cpu().pin_memory() if db.block_table is not None else None
+    h_idx = torch.empty((T, k), dtype=torch.int32).pin_memory()
+    h_out = torch.empty((T, k, 128), dtype=torch.int16).pin_memory() if has_gather else None
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_w, h_qs, h_lens, h_bt) if x is not None)
+    d2h = h_idx.numel() * 4 + (h_out.numel() * 2 if has_gather else 0)
+
+    def e2e_step():
+        db.q.copy_(h_q, non_blocking=True)
+        db.weights.copy_(h_w, non_blocking=True)
+        if h_qs is not None:
+            db.q_scale.copy_(h_qs, non_blocking=True)
+        db.context_lens.copy_(h_lens, non_blocking=True)
+        if h_bt is not None:
+            db.block_table.copy_(h_bt, non_blocking=True)
+        step()
+        h_idx.copy_(idx, non_blocking=True)
+        if has_gather:
+            h_out.copy_(gout, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    local = torch.tensor([total_ms / args.steps, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(local, op=torch.distributed.ReduceOp.MAX)
+    ms_step, e2e_ms = float(local[0]), float(local[1])
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    bound = "tensor" if args.workload in ("prefill", "fp8_chunked") else "hbm"
+    if bound == "hbm":
+        achieved = work["fused_bytes"] / (fused_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    else:
+        achieved = work["flops"] / (fused_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"] * (2.0 if wl.dtype == "e4m3" else 1.0)
+        unit = "TFLOP/s"
+    out = {
+        "metric": METRIC, "value": T * world / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if wl.dtype == "e4m3" else "bf16",
+        "data": "synthetic (seeded SplitMix64 generator; no dataset or weights)",
+        "config": {"workload": args.workload, "desc": info["desc"], "B": wl.B, "next_n": wl.next_n,
+                   "topk": k, "sum_context": int(wl.context_lens.sum()), "seed": info["seed"],
+                   "l2": "inputs larger than L2" if work["fused_bytes"] > L2_BYTES else "L2 not flushed",
+                   "parallelism": f"replicas x{world}"},
+        "indexer_qtok_s": T / (fused_ms * 1e-3),
+        "fused_ms": fused_ms,
+        "gather_ms": gather_ms,
+        "gather_gbps": (work["gather_bytes"] / (gather_ms * 1e-3) / 1e9) if has_gather else None,
+        "gather_frac_hbm": (work["gather_bytes"] / (gather_ms * 1e-3) / 1e9 / peaks["hbm_gbs"])
+        if has_gather else None,
+        "roofline": {"kernel": "dsa_indexer_logits_topk (indexer_kernel + merge_kernel)", "bound": bound,
+                     "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "peak_source": peaks["source"], "traffic": recorded_traffic(args.workload)},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+    }
+    return out, wl
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_sample(wl, budget_s: float, min_rows: int = 1):
+    """Runs the oracle (score, top-k, gather) on query rows until the time budget is used;
+    returns (rows done, seconds)."""
+    from oracle import dsa_oracle as orc
+    order = np.random.default_rng(0).permutation(wl.T)
+    t0 = time.perf_counter()
+    done = 0
+    for t in order:
+        lg = orc.indexer_logits(wl.q, wl.q_scale, wl.dtype, wl.weights, wl.k_data, wl.k_scale,
+                                wl.block_table, wl.block_size, wl.B, wl.next_n, wl.context_lens,
+                                wl.causal, rows=np.array([t]))
+        idx, _ = orc.topk_select(lg, wl.topk)
+        if wl.kv_fp4 is not None:
+            b = t // wl.next_n
+            orc.mxfp4_paged_gather(wl.kv_fp4, wl.kv_scale, wl.gather_block_table[b:b + 1], idx, 1, 1,
+                                   wl.block_size)
+        done += 1
+        if done >= min_rows and time.perf_counter() - t0 >= budget_s:
+            break
+    return done, time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    info = WORKLOADS[args.workload]
+    wl = make_workload(args.workload, info["seed"])
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.0)
+    rows = 0
+    secs = 0.0
+    per_step = []
+    for _ in range(args.steps):
+        r, s = oracle_sample(wl, 2.0)
+        rows += r
+        secs += s
+        per_step.append(s / r)
+    value = rows / secs
+    sample = f"{rows} query rows over {args.steps} steps (score, top-k and gather per row)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.T * statistics.mean(per_step),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded SplitMix64 generator; no dataset or weights)",
+        "config": {"workload": args.workload, "desc": info["desc"], "B": wl.B, "next_n": wl.next_n,
+                   "topk": wl.topk},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="flash_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if res is not None:
+        out, wl = res
+        if world == 1 or rank == 0:
+            rows, secs = oracle_sample(wl, args.cpu_baseline_seconds)
+            out["cpu_baseline"] = {"value": rows / secs, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                                   "sample": f"{rows} of {wl.T} query rows (score, top-k, gather), "
+                                             f"{secs:.1f} s"}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -225,12 +225,13 @@ __device__ __forceinline__ float value_of_key(uint64_t key) { return f32_of_ord(
 __device__ __forceinline__ bool is_candidate(float v) { return v > -INFINITY; }
 
 // ---------------------------------------------------------------------------------
-// Shared-memory top-k engine.  Run by a group of 256 threads that synchronise on
-// named barrier 1 (`tid` = 0..255 within the group).
+// Shared-memory top-k engine.  Run by a group of NT threads (a multiple of 128) that
+// synchronise on named barrier 1; `tid` = 0..NT-1 within the group.
 // ---------------------------------------------------------------------------------
-constexpr int kEngineThreads = 256;
-
-__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+template <int NT>
+__device__ __forceinline__ void group_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
 
 struct EngineScratch {
   uint32_t hist[256];
@@ -238,8 +239,12 @@ struct EngineScratch {
 };
 
 // Appends `key` to buf[*cnt] when `take` is set; warp-aggregated atomics.  All 32
-// lanes of the warp must call it together.
-__device__ __forceinline__ void engine_append(uint64_t* buf, uint32_t* cnt, uint64_t key, bool take) {
+// lanes of the warp must call it together.  A slot at or past `cap` is never written:
+// the key is dropped and DSA_DEVERR_OVERFLOW raised, with the call site (1..255) in bits
+// 8..15 of the error word (the callers size their buffers so that this cannot happen;
+// the check keeps a broken invariant from touching memory it does not own).
+__device__ __forceinline__ void engine_append(uint64_t* buf, uint32_t* cnt, uint64_t key, bool take,
+                                              uint32_t cap, uint32_t site) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t m = __ballot_sync(0xFFFFFFFFu, take);
   if (m == 0) return;
@@ -247,87 +252,173 @@ __device__ __forceinline__ void engine_append(uint64_t* buf, uint32_t* cnt, uint
   const uint32_t leader = __ffs(m) - 1;
   if (lane == leader) base = atomicAdd(cnt, (uint32_t)__popc(m));
   base = __shfl_sync(0xFFFFFFFFu, base, leader);
-  if (take) buf[base + __popc(m & ((1u << lane) - 1u))] = key;
+  if (take) {
+    const uint32_t slot = base + __popc(m & ((1u << lane) - 1u));
+    if (slot < cap) buf[slot] = key;
+    else raise_error(DSA_DEVERR_OVERFLOW | ((site & 0xFFu) << 8));
+  }
 }
 
-// Smallest key T such that exactly k of the n (> k) distinct keys in buf are >= T
-// (the k-th largest key, or a lower bound of it sharing all bits that decide the
-// set).  Most-significant-digit-first radix select over 8-bit digits.
-static __device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScratch* sc, int tid) {
+// hist[bin] += 1 for every lane with `take`; one shared atomic per distinct bin per warp
+// (keys of a candidate set share their leading digits, so bins are heavily contended).
+// All 32 lanes must call it together.
+__device__ __forceinline__ void hist_add(uint32_t* hist, bool take, uint32_t bin) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t active = __ballot_sync(0xFFFFFFFFu, take);
+  if (!take) return;
+  const uint32_t peers = __match_any_sync(active, bin);
+  if (lane == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
+
+// Picks the digit of the current radix pass: the bin holding the `need`-th largest key,
+// scanning hist from the top.  Run by warp 0 of the group; results in sc->pick.
+__device__ __forceinline__ void pick_digit(uint32_t* hist, uint32_t* pick, uint32_t need, int tid) {
+  uint32_t c[8], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    c[i] = hist[255 - 8 * tid - i];
+    sum += c[i];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (tid >= o) incl += y;
+  }
+  const uint32_t excl = incl - sum;
+  if (tid == 31) pick[3] = incl;    // total count of this pass
+  if (tid == 31 && need > incl) pick[0] = 0xFFFFFFFFu;   // no such bin: inconsistent input
+  if (excl < need && need <= incl) {
+    uint32_t above = excl;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (above < need && need <= above + c[i]) {
+        pick[0] = 255u - 8u * tid - i;
+        pick[1] = above;
+        pick[2] = c[i];
+      }
+      above += c[i];
+    }
+  }
+}
+
+// Smallest key T such that exactly k of the distinct nonzero keys in buf[0, n) are >= T
+// (the k-th largest key, or a lower bound of it sharing all bits that decide the set);
+// 1 when there are at most k of them.  Most-significant-digit-first radix select over
+// 8-bit digits; zero slots are ignored.
+template <int NT>
+__device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScratch* sc, int tid) {
   uint64_t prefix = 0, mask = 0;
   uint32_t need = (uint32_t)k;
   for (int shift = 56; shift >= 0; shift -= 8) {
-    sc->hist[tid] = 0;
-    group_sync();
-    for (int e = tid; e < n; e += kEngineThreads) {
-      const uint64_t key = buf[e];
-      if ((key & mask) == prefix) atomicAdd(&sc->hist[(uint32_t)(key >> shift) & 255u], 1u);
+    for (int i = tid; i < 256; i += NT) sc->hist[i] = 0;
+    group_sync<NT>();
+    for (int base = 0; base < n; base += NT) {
+      const int e = base + tid;
+      const uint64_t key = e < n ? buf[e] : 0ull;
+      hist_add(sc->hist, key != 0ull && (key & mask) == prefix, (uint32_t)(key >> shift) & 255u);
     }
-    group_sync();
-    if (tid < 32) {
-      // lane l covers digits 255-8l .. 248-8l, scanned from the top
-      uint32_t c[8], sum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = sc->hist[255 - 8 * tid - i];
-        sum += c[i];
-      }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (tid >= o) incl += y;
-      }
-      const uint32_t excl = incl - sum;
-      if (excl < need && need <= incl) {
-        uint32_t above = excl;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (above < need && need <= above + c[i]) {
-            sc->pick[0] = 255u - 8u * tid - i;
-            sc->pick[1] = above;
-            sc->pick[2] = c[i];
-          }
-          above += c[i];
-        }
-      }
+    group_sync<NT>();
+    if (tid < 32) pick_digit(sc->hist, sc->pick, need, tid);   // lane l: digits 255-8l .. 248-8l
+    group_sync<NT>();
+    if (shift == 56 && sc->pick[3] <= (uint32_t)k) {           // at most k keys: take them all
+      group_sync<NT>();
+      return 1ull;
     }
-    group_sync();
     const uint32_t d = sc->pick[0], above = sc->pick[1], inbin = sc->pick[2];
+    if (d > 255u) {                // counts did not add up: keep everything (never drops a key)
+      if (tid == 0) raise_error(DSA_DEVERR_OVERFLOW | (42u << 8));
+      group_sync<NT>();
+      return 1ull;
+    }
     need -= above;
     prefix |= (uint64_t)d << shift;
     mask |= (uint64_t)0xFF << shift;
     if (inbin == need) break;      // every key with this prefix belongs to the set
   }
-  group_sync();                    // everyone has read pick[] before it is reused
+  group_sync<NT>();                // everyone has read pick[] before it is reused
+  return prefix;
+}
+
+// As engine_select, over the nonzero keys of a global-memory array (read through L2).
+// Returns 1 (take every nonzero key) when there are at most k of them.
+template <int NT>
+__device__ uint64_t engine_select_global(const uint64_t* src, int n, int k, EngineScratch* sc, int tid) {
+  uint64_t prefix = 0, mask = 0;
+  uint32_t need = (uint32_t)k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += NT) sc->hist[i] = 0;
+    group_sync<NT>();
+    for (int base = 0; base < n; base += 4 * NT) {
+      uint64_t key[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = base + u * NT + tid;
+        key[u] = e < n ? __ldcg(src + e) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        hist_add(sc->hist, key[u] != 0ull && (key[u] & mask) == prefix, (uint32_t)(key[u] >> shift) & 255u);
+    }
+    group_sync<NT>();
+    if (tid < 32) pick_digit(sc->hist, sc->pick, need, tid);
+    group_sync<NT>();
+    if (shift == 56 && sc->pick[3] <= (uint32_t)k) {
+      group_sync<NT>();
+      return 1ull;
+    }
+    const uint32_t d = sc->pick[0], above = sc->pick[1], inbin = sc->pick[2];
+    need -= above;
+    prefix |= (uint64_t)d << shift;
+    mask |= (uint64_t)0xFF << shift;
+    if (inbin == need) break;
+  }
+  group_sync<NT>();
   return prefix;
 }
 
 // Keeps the keys >= thr of buf[0, n), packed to the front; *cnt becomes their
-// number.  MAXPER >= ceil(n / 256).
-template <int MAXPER>
+// number.  Holds the keys in registers meanwhile: needs n <= NT * MAXPER.
+template <int NT, int MAXPER>
 __device__ void engine_compact(uint64_t* buf, uint32_t* cnt, int n, uint64_t thr, int tid) {
   uint64_t keep[MAXPER];
 #pragma unroll
   for (int i = 0; i < MAXPER; ++i) {
-    const int e = tid + i * kEngineThreads;
+    const int e = tid + i * NT;
     keep[i] = (e < n) ? buf[e] : 0ull;
   }
-  group_sync();
+  group_sync<NT>();
   if (tid == 0) *cnt = 0;
-  group_sync();
+  group_sync<NT>();
 #pragma unroll
-  for (int i = 0; i < MAXPER; ++i) engine_append(buf, cnt, keep[i], keep[i] != 0ull && keep[i] >= thr);
-  group_sync();
+  for (int i = 0; i < MAXPER; ++i)
+    engine_append(buf, cnt, keep[i], keep[i] != 0ull && keep[i] >= thr, (uint32_t)(NT * MAXPER), 1u);
+  group_sync<NT>();
+}
+
+// Copies the keys >= thr of src[0, n) to the front of dst (capacity dcap); *cnt becomes
+// their number.
+template <int NT>
+__device__ void engine_compact_to(const uint64_t* src, uint64_t* dst, uint32_t* cnt, int n, uint64_t thr,
+                                  int tid, uint32_t dcap) {
+  if (tid == 0) *cnt = 0;
+  group_sync<NT>();
+  for (int base = 0; base < n; base += NT) {
+    const int e = base + tid;
+    const uint64_t key = e < n ? src[e] : 0ull;
+    engine_append(dst, cnt, key, key != 0ull && key >= thr, dcap, 2u);
+  }
+  group_sync<NT>();
 }
 
 // Sorts nlist lists in place, each of P (power of two) keys at buf + l * stride,
 // in descending key order (rank order).  Slots past a list's count must hold 0.
-static __device__ void engine_sort(uint64_t* buf, int stride, int nlist, int P, int tid) {
+template <int NT>
+__device__ void engine_sort(uint64_t* buf, int stride, int nlist, int P, int tid) {
   const int pairs = P >> 1;
   for (int size = 2; size <= P; size <<= 1) {
     for (int half = size >> 1; half > 0; half >>= 1) {
-      for (int t = tid; t < pairs * nlist; t += kEngineThreads) {
+      for (int t = tid; t < pairs * nlist; t += NT) {
         const int l = t / pairs, u = t - l * pairs;
         const int i = 2 * u - (u & (half - 1));
         const int j = i + half;
@@ -339,7 +430,7 @@ static __device__ void engine_sort(uint64_t* buf, int stride, int nlist, int P, 
           b[j] = x;
         }
       }
-      group_sync();
+      group_sync<NT>();
     }
   }
 }

@@ -3,24 +3,29 @@
 // Score (xkernels issue #27 "DSA indexer + attention: validate/provide gfx942 forward
 // path", comment 2 "What shipped"):  logits[t, j] = sum_h w[t, h] * relu(q[t, h, :] . k[j, :]).
 //
-// One CTA owns a work item = (sequence b, a group of NQ query rows, a key range).  The
-// contraction runs key-major: A = a tile of 128 keys x D (K-major, from shared memory),
-// B = the NQ*64 (query, head) rows of q x D, so the accumulator D[key, (query, head)]
-// sits in tensor memory with one key per TMEM lane.  An epilogue thread therefore owns
-// one key and reduces its 64 head columns in registers: ReLU, weight and head sum need
-// no cross-thread traffic.
+// Work item = (sequence b, a group of NQ query rows, a chunk of keys).  The contraction
+// runs key-major: A = a tile of 128 keys x D (K-major, shared memory), B = the NQ*64
+// (query, head) rows of q x D, so the accumulator D[key, (query, head)] sits in tensor
+// memory with one key per TMEM lane.  An epilogue thread owns one key and reduces its
+// 64 head columns in registers: ReLU, weight and head sum need no cross-thread traffic.
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: the Q tile once, then key tiles into an S-stage ring
-//               (paged keys: one box per page through the block table)
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 2-5   epilogue group 0: even key tiles (TMEM accumulator buffer 0)
-//   warps 6-9   epilogue group 1: odd key tiles  (TMEM accumulator buffer 1)
+// The kernel is persistent.  In top-k mode a one-CTA plan kernel first reads the actual
+// context lengths, picks the key chunk (about two items per CTA, at most 16 chunks per
+// query group) and writes a longest-first work list; CTAs take items from it through an
+// atomic counter.  (Logits mode, which has no workspace, walks fixed chunks with a
+// static stride.)  Warp roles (64 + 128 * EG threads):
+//   warp 0     producer: fetches items, publishes their descriptors, loads each item's
+//              Q tile and streams key tiles into an S-stage ring with TMA (paged keys:
+//              one box per page, block ids read from a shared-memory window the whole
+//              warp refills); it runs ahead of the other roles across item boundaries
+//   warp 1     TMEM allocator + single-thread tcgen05.mma issuer
+//   warps 2..  EG epilogue groups of 4 warps; global tile T uses TMEM buffer T & 1 and
+//              epilogue group T % EG
 // Epilogue: tcgen05.ld of each query's 64 head sums, fp32 ReLU * weight head sum in a
-// fixed order, then either a store of the score row (logits mode) or an insert into a
-// per-query candidate buffer in shared memory (top-k mode) that is cut back to the
-// top-k with a radix select whenever it fills, and sorted at the end.  The candidate
-// test is "ranking key >= threshold", which is exact for any arrival order.
+// fixed order, then a store of the score row (logits mode) or an insert into a per-query
+// candidate buffer in shared memory (top-k mode) that a radix select cuts back to the
+// top-k whenever it fills.  A group whose keys fit one chunk gets its sorted rows here;
+// split groups write unsorted per-chunk lists that the merge kernel (topk.cu) ranks.
 //
 // Every wait is bounded (see common.cuh); a timeout abandons the work, flags
 // DSA_DEVERR_TIMEOUT, waits for this CTA's own copies and MMAs, frees TMEM and returns.
@@ -46,20 +51,38 @@ struct IndexerParams {
   int64_t ld;
   int32_t* out_idx;
   float* out_val;
-  uint64_t* partial;
+  uint64_t* partial;        // [T][nl_max][topk] ranking keys of split rows
+  const int32_t* plan;      // device work list (top-k mode): chunk, item count, items
+  uint32_t* work;           // item counter of the work list
   int32_t block_size;
   int32_t B, next_n, causal, max_len;
-  int32_t ngroups, nchunks, chunk;
+  int32_t ngroups, nchunks, chunk;  // static schedule (logits mode)
+  int32_t nl_max;           // list slots per row in `partial`
   int32_t topk, cap, pow2, stages;
 };
 
+// Layout of the device work list written by plan_kernel.
+constexpr int kPlanHeader = 4;      // int32: chunk (keys), item count, reserved x2
+constexpr int kMaxLists = 16;       // key chunks per query group at most (split rows)
+
 constexpr int kMaxPer = 10;        // candidate capacity per query <= 256 * kMaxPer
+
+struct ItemInfo {
+  int32_t valid, b, g, c, L, nreal, vis_max, ks, ntiles, t0, chunk, nl;
+  int32_t vis[4];
+};
+
+constexpr int kPageWindow = 256;    // block-table entries the producer keeps in shared memory
 
 template <int NQ>
 struct EpiSmem {
-  float w[NQ][64];
+  int32_t pages[kPageWindow];
+  float w[2][NQ][64];
+  ItemInfo info[2];
   uint32_t tmem_base;
   int abort;
+  int stop;
+  int last;
   uint32_t cnt[4];
   uint64_t thr[4];
   EngineScratch esc;
@@ -78,10 +101,203 @@ __device__ __forceinline__ float head_sum(const float (&s)[64], const float* w) 
   return (a0 + a1) + (a2 + a3);
 }
 
-template <bool kFP8, int NQ, bool kTopk>
-__global__ void __launch_bounds__(320, 1)
+// Descriptor of work item (query group u = b * ngroups + gi, key chunk c).
+template <int NQ>
+__device__ void decode_item(const IndexerParams& p, int u, int c, int chunk, ItemInfo& it) {
+  const int b = u / p.ngroups;
+  const int gi = u - b * p.ngroups;
+  int L = __ldg(p.context_lens + b);
+  if (L < 0 || L > p.max_len) {
+    if (c == 0 && gi == 0) raise_error(DSA_DEVERR_INDEX);
+    L = L < 0 ? 0 : p.max_len;
+  }
+  const int i0 = gi * NQ;
+  const int nreal = min(NQ, p.next_n - i0);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    int v = 0;
+    if (q < nreal) v = p.causal ? min(max(L - p.next_n + i0 + q + 1, 0), L) : L;
+    it.vis[q] = v;
+  }
+  const int vis_max = p.causal ? min(max(L - p.next_n + i0 + nreal, 0), L) : L;
+  const int ks = c * chunk;
+  const int ke = min(ks + chunk, vis_max);
+  it.valid = 1;
+  it.b = b;
+  it.g = gi;
+  it.c = c;
+  it.L = L;
+  it.nreal = nreal;
+  it.vis_max = vis_max;
+  it.ks = ks;
+  it.ntiles = ke > ks ? (ke - ks + 127) / 128 : 0;
+  it.t0 = b * p.next_n + i0;
+  it.chunk = chunk;
+  it.nl = max((vis_max + chunk - 1) / chunk, 1);
+}
+
+// Visible key tiles of query group u (its last real query sees the most keys).
+__device__ __forceinline__ int group_tiles(const int32_t* context_lens, int u, int ngroups, int nq, int next_n,
+                                           int causal, int max_len) {
+  const int b = u / ngroups;
+  const int gi = u - b * ngroups;
+  int L = __ldg(context_lens + b);
+  L = L < 0 ? 0 : (L > max_len ? max_len : L);
+  const int nreal = min(nq, next_n - gi * nq);
+  const int vis = causal ? min(max(L - next_n + gi * nq + nreal, 0), L) : L;
+  return (vis + 127) / 128;
+}
+
+// Builds the work list of the fused call from the actual context lengths: picks the key
+// chunk (a multiple of 128) so that there are about `target` items and at most nl_max
+// chunks per query group, then orders the items longest first: whole chunks, then the
+// groups' remainders by decreasing length, then groups without visible keys (they only
+// report empty rows).  Items are (u << 8) | c.  One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ context_lens, int B, int next_n,
+                                                    int causal, int max_len, int nq, int ngroups, int target,
+                                                    int nl_max, int32_t* __restrict__ plan, uint32_t* work) {
+  constexpr int kBuckets = 4096;
+  __shared__ unsigned long long s_sum[32];
+  __shared__ int s_max[32];
+  __shared__ int s_hist[kBuckets];
+  __shared__ int s_scan[32];
+  __shared__ int s_misc[4];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int units = B * ngroups;
+  // 1. total and longest group, in tiles
+  unsigned long long lsum = 0;
+  int lmax = 0;
+  for (int u = tid; u < units; u += 1024) {
+    const int t = group_tiles(context_lens, u, ngroups, nq, next_n, causal, max_len);
+    lsum += (unsigned long long)t;
+    lmax = max(lmax, t);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+    lmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+  }
+  if (lane == 0) {
+    s_sum[wid] = lsum;
+    s_max[wid] = lmax;
+  }
+  for (int i = tid; i < kBuckets; i += 1024) s_hist[i] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long sum = 0;
+    int mx = 0;
+    for (int w = 0; w < 32; ++w) {
+      sum += s_sum[w];
+      mx = max(mx, s_max[w]);
+    }
+    long long ct = (long long)((sum + (unsigned long long)target - 1) / (unsigned long long)target);
+    if (ct < 16) ct = 16;                                   // at least 2048 keys per chunk
+    const long long need = ((long long)mx + nl_max - 1) / nl_max;
+    if (ct < need) ct = need;
+    if (ct >= mx) ct = mx > 0 ? mx : 1;                     // no group needs splitting
+    s_misc[0] = (int)ct;
+    s_misc[1] = (int)((ct + kBuckets - 1) / kBuckets);      // tiles per ordering bucket
+    *work = 0u;
+  }
+  __syncthreads();
+  const int ct = s_misc[0];
+  const int per = s_misc[1];
+  // 2. whole chunks in group order; remainders counted per length bucket
+  int base = 0;
+  for (int u0 = 0; u0 < units; u0 += 1024) {
+    const int u = u0 + tid;
+    int nfull = 0;
+    if (u < units) {
+      const int t = group_tiles(context_lens, u, ngroups, nq, next_n, causal, max_len);
+      nfull = t / ct;
+      const int rem = t - nfull * ct;
+      if (rem > 0) atomicAdd(&s_hist[kBuckets - 1 - (rem - 1) / per], 1);     // longest first
+    }
+    int incl = nfull;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_scan[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int v = s_scan[lane], x = v;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      s_scan[lane] = x - v;                                 // exclusive
+      if (lane == 31) s_misc[2] = x;
+    }
+    __syncthreads();
+    const int start = base + s_scan[wid] + incl - nfull;
+    for (int c = 0; c < nfull; ++c) plan[kPlanHeader + start + c] = (u << 8) | c;
+    base += s_misc[2];
+    __syncthreads();
+  }
+  // 3. bucket offsets (exclusive scan over buckets, longest first), then remainders
+  {
+    int v[kBuckets / 1024], sum = 0;
+#pragma unroll
+    for (int i = 0; i < kBuckets / 1024; ++i) {
+      v[i] = s_hist[tid * (kBuckets / 1024) + i];
+      sum += v[i];
+    }
+    int incl = sum;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_scan[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int w = s_scan[lane], x = w;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      s_scan[lane] = x - w;
+      if (lane == 31) s_misc[3] = base + x;
+    }
+    __syncthreads();
+    int acc = base + s_scan[wid] + incl - sum;
+#pragma unroll
+    for (int i = 0; i < kBuckets / 1024; ++i) {
+      s_hist[tid * (kBuckets / 1024) + i] = acc;
+      acc += v[i];
+    }
+  }
+  __syncthreads();
+  for (int u = tid; u < units; u += 1024) {
+    const int t = group_tiles(context_lens, u, ngroups, nq, next_n, causal, max_len);
+    const int nfull = t / ct;
+    const int rem = t - nfull * ct;
+    if (rem > 0) {
+      const int pos = atomicAdd(&s_hist[kBuckets - 1 - (rem - 1) / per], 1);
+      plan[kPlanHeader + pos] = (u << 8) | nfull;
+    }
+  }
+  __syncthreads();
+  // 4. groups without visible keys
+  if (tid == 0) s_misc[2] = s_misc[3];
+  __syncthreads();
+  for (int u = tid; u < units; u += 1024) {
+    if (group_tiles(context_lens, u, ngroups, nq, next_n, causal, max_len) == 0) {
+      const int pos = atomicAdd(&s_misc[2], 1);
+      plan[kPlanHeader + pos] = (u << 8);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    plan[0] = ct * 128;
+    plan[1] = s_misc[2];
+  }
+}
+
+template <bool kFP8, int NQ, bool kTopk, int EG>
+__global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const IndexerParams p) {
+  constexpr int NT = 128 * EG;                     // epilogue threads
   constexpr int N = NQ * 64;                       // MMA N: (query, head) rows
   constexpr int ELT = kFP8 ? 1 : 2;                // bytes per element
   constexpr int KCH = kFP8 ? 1 : 2;                // 128-byte K chunks per row (D = 128)
@@ -97,47 +313,23 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
   uint8_t* q_s = smem;
-  uint8_t* k_s = smem + Q_BYTES;
+  uint8_t* k_s = smem + Q_BYTES;                         // S stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(k_s + (size_t)S * K_BYTES);
-  // bars: full[S] | empty[S] | tfull[2] | tempty[2] | qfull | mmadone
-  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 6);
+  // full[S] | empty[S] | tfull[2] | tempty[2] | qfull | qempty | ifull[2] | iempty[2] | mmadone | pad
+  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 12);
   uint64_t* ebuf = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(es) + sizeof(EpiSmem<NQ>) + 15) & ~uintptr_t(15));
 
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
   const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
-  const uint32_t qfull = smem_u32(bars + 2 * S + 4), mmadone = smem_u32(bars + 2 * S + 5);
+  const uint32_t qfull = smem_u32(bars + 2 * S + 4), qempty = smem_u32(bars + 2 * S + 5);
+  const uint32_t ifull0 = smem_u32(bars + 2 * S + 6), iempty0 = smem_u32(bars + 2 * S + 8);
+  const uint32_t mmadone = smem_u32(bars + 2 * S + 10);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const unsigned long long limit = wait_limit_ns();
   volatile int* abort_flag = &es->abort;
-
-  // ---- work item: heavy groups first (later queries see more keys when causal)
-  const int item = blockIdx.x;
-  const int c = item % p.nchunks;
-  const int rest = item / p.nchunks;
-  const int g = p.ngroups - 1 - (rest % p.ngroups);
-  const int b = rest / p.ngroups;
-  int L = __ldg(p.context_lens + b);
-  if (L < 0 || L > p.max_len) {
-    if (threadIdx.x == 0) raise_error(DSA_DEVERR_INDEX);
-    L = L < 0 ? 0 : p.max_len;
-  }
-  const int i0 = g * NQ;
-  const int nreal = min(NQ, p.next_n - i0);
-  const int t0 = b * p.next_n + i0;
-  int vis[NQ];
-#pragma unroll
-  for (int q = 0; q < NQ; ++q) {
-    int v = 0;
-    if (q < nreal) v = p.causal ? min(max(L - p.next_n + i0 + q + 1, 0), L) : L;
-    vis[q] = v;
-  }
-  const int vis_max = p.causal ? min(max(L - p.next_n + i0 + nreal, 0), L) : L;
-  const int ks = c * p.chunk;
-  const int ke = min(ks + p.chunk, vis_max);
-  const int ntiles = ke > ks ? (ke - ks + 127) / 128 : 0;
   const bool paged = p.block_table != nullptr;
   const int bs = p.block_size;
 
@@ -150,127 +342,203 @@ __global__ void __launch_bounds__(320, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
       mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(ifull0 + 8 * a, 1);
+      mbar_init(iempty0 + 8 * a, 1 + 4 * EG);
     }
     mbar_init(qfull, 1);
+    mbar_init(qempty, 1);
     mbar_init(mmadone, 1);
     es->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(&es->tmem_base), TMEM_COLS);
-  if (warp >= 2) {
-    const int et = threadIdx.x - 64;
-    for (int e = et; e < NQ * 64; e += 256) {
-      const int q = e >> 6, h = e & 63;
-      float w = 0.f;
-      if (q < nreal) {
-        const int64_t o = (int64_t)(t0 + q) * 64 + h;
-        w = __ldg(p.weights + o);
-        if (kFP8) w *= __ldg(p.q_scale + o);
-      }
-      es->w[q][h] = w;
-    }
-    if (kTopk && et < 4) {
-      es->cnt[et] = 0;
-      es->thr[et] = 0;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = es->tmem_base;
 
   if (warp == 0) {
-    // ============================ TMA producer ============================
-    if (lane == 0 && ntiles > 0) {
+    // ============================ producer (whole warp) ============================
+    // Lane 0 owns the barriers and issues every copy; the other lanes help load the
+    // block table into a shared window so no copy waits on a dependent global load.
+    int plan_chunk = p.chunk, plan_items = p.B * p.ngroups * p.nchunks;
+    if (p.plan) {
+      plan_chunk = __ldg(p.plan);
+      plan_items = __ldg(p.plan + 1);
+    }
+    int next = 0;
+    if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      mbar_arrive_expect_tx(qfull, Q_BYTES);
-      for (int kc = 0; kc < KCH; ++kc)
-        tma_load_2d(smem_u32(q_s + kc * Q_CHUNK), &tm_q, qfull, kc * (128 / ELT), t0 * 64);
-      int last_issue[8];
-      for (int s = 0; s < 8; ++s) last_issue[s] = -1;
-      for (int i = 0; i < ntiles; ++i) {
-        const int s = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, limit, abort_flag)) {
-          raise_error(DSA_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-          break;
-        }
-        const int j0 = ks + i * 128;
-        const int jend = min(j0 + 128, ke);
-        const uint32_t stage = smem_u32(k_s + (size_t)s * K_BYTES);
-        const uint32_t fb = full0 + 8 * s;
-        if (!paged) {
-          mbar_arrive_expect_tx(fb, K_BYTES);
-          for (int kc = 0; kc < KCH; ++kc) tma_load_2d(stage + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), j0);
-        } else if (bs >= 128) {
-          const int64_t pg = j0 / bs;
-          int64_t blk = -1;
-          if (pg < p.bt_stride) blk = __ldg(p.block_table + (int64_t)b * p.bt_stride + pg);
-          if (blk >= 0 && blk < p.num_blocks) {
-            mbar_arrive_expect_tx(fb, K_BYTES);
-            const int32_t row = (int32_t)(blk * bs + (j0 % bs));
-            for (int kc = 0; kc < KCH; ++kc) tma_load_2d(stage + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), row);
+      next = p.plan ? (int)atomicAdd(p.work, 1u) : (int)blockIdx.x;
+    }
+    int tiles_issued = 0, items_issued = 0;
+    int last_issue[8];
+    for (int s = 0; s < 8; ++s) last_issue[s] = -1;
+    bool ok = true;
+    for (int n = 0;; ++n) {
+      const int slot = n & 1;
+      int have = 0;
+      if (lane == 0) {
+        ok = mbar_wait(iempty0 + 8 * slot, ((uint32_t)(n >> 1) & 1u) ^ 1u, limit, abort_flag);
+        ItemInfo it;
+        it.valid = 0;
+        if (ok && next < plan_items) {
+          const int cur = next;
+          next = p.plan ? (int)atomicAdd(p.work, 1u) : next + (int)gridDim.x;
+          int u, c;
+          if (p.plan) {
+            const int code = __ldg(p.plan + kPlanHeader + cur);
+            u = code >> 8;
+            c = code & 255;
           } else {
-            raise_error(DSA_DEVERR_INDEX);
-            mbar_arrive_expect_tx(fb, 0);
+            u = cur / p.nchunks;
+            c = cur - u * p.nchunks;
           }
-        } else {
+          decode_item<NQ>(p, u, c, plan_chunk, it);
+          have = 1;
+        }
+        es->info[slot] = it;
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      have = __shfl_sync(0xFFFFFFFFu, have, 0);
+      if (!ok) break;
+      if (!have) {
+        if (lane == 0) mbar_arrive(ifull0 + 8 * slot);      // end-of-work descriptor
+        break;
+      }
+      __syncwarp();
+      const ItemInfo it = es->info[slot];
+      // this item's Q tile, once the previous item's MMAs are done with the last one
+      if (lane == 0) {
+        ok = mbar_wait(qempty, ((uint32_t)n & 1u) ^ 1u, limit, abort_flag);
+        if (ok) {
+          mbar_arrive_expect_tx(qfull, Q_BYTES);
+          for (int kc = 0; kc < KCH; ++kc)
+            tma_load_2d(smem_u32(q_s + kc * Q_CHUNK), &tm_q, qfull, kc * (128 / ELT), it.t0 * 64);
+          ++items_issued;
+          mbar_arrive(ifull0 + 8 * slot);
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      // its key tiles
+      const int ke = min(it.ks + it.chunk, it.vis_max);
+      int win0 = -1;                                        // first page held in the window
+      for (int i = 0; i < it.ntiles; ++i) {
+        const int T = tiles_issued + i;
+        const int s = T % S;
+        const int j0 = it.ks + i * 128;
+        const int jend = min(j0 + 128, ke);
+        if (paged) {
           const int pg0 = j0 / bs, pg1 = (jend - 1) / bs;
-          int32_t blks[16];
-          uint32_t bytes = 0;
-          for (int pg = pg0; pg <= pg1; ++pg) {
-            int64_t blk = -1;
-            if (pg < p.bt_stride) blk = __ldg(p.block_table + (int64_t)b * p.bt_stride + pg);
-            const bool ok = blk >= 0 && blk < p.num_blocks;
-            if (!ok) raise_error(DSA_DEVERR_INDEX);
-            blks[pg - pg0] = ok ? (int32_t)blk : -1;
-            if (ok) bytes += (uint32_t)bs * 128u * KCH;
-          }
-          mbar_arrive_expect_tx(fb, bytes);
-          for (int pg = pg0; pg <= pg1; ++pg) {
-            const int32_t blk = blks[pg - pg0];
-            if (blk < 0) continue;
-            const uint32_t dst = stage + (uint32_t)(pg - pg0) * (uint32_t)bs * 128u;
-            for (int kc = 0; kc < KCH; ++kc)
-              tma_load_2d(dst + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), blk * bs);
+          if (win0 < 0 || pg1 >= win0 + kPageWindow) {
+            __syncwarp();
+            win0 = pg0;
+            const int pend = (ke - 1) / bs;
+            for (int e = lane; e < kPageWindow; e += 32) {
+              const int pg = win0 + e;
+              int32_t blk = -1;
+              if (pg <= pend && pg < p.bt_stride) blk = __ldg(p.block_table + (int64_t)it.b * p.bt_stride + pg);
+              es->pages[e] = blk;
+            }
+            __syncwarp();
           }
         }
-        last_issue[s] = i;
+        if (lane == 0) {
+          ok = mbar_wait(empty0 + 8 * s, ((uint32_t)(T / S) & 1u) ^ 1u, limit, abort_flag);
+          if (ok) {
+            const uint32_t stage = smem_u32(k_s + (size_t)s * K_BYTES);
+            const uint32_t fb = full0 + 8 * s;
+            if (!paged) {
+              mbar_arrive_expect_tx(fb, K_BYTES);
+              for (int kc = 0; kc < KCH; ++kc)
+                tma_load_2d(stage + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), j0);
+            } else if (bs >= 128) {
+              const int64_t blk = es->pages[j0 / bs - win0];
+              if (blk >= 0 && blk < p.num_blocks) {
+                mbar_arrive_expect_tx(fb, K_BYTES);
+                const int32_t row = (int32_t)(blk * bs + (j0 % bs));
+                for (int kc = 0; kc < KCH; ++kc)
+                  tma_load_2d(stage + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), row);
+              } else {
+                raise_error(DSA_DEVERR_INDEX);
+                mbar_arrive_expect_tx(fb, 0);
+              }
+            } else {
+              const int pg0 = j0 / bs, pg1 = (jend - 1) / bs;
+              uint32_t bytes = 0;
+              for (int pg = pg0; pg <= pg1; ++pg) {
+                const int64_t blk = es->pages[pg - win0];
+                if (blk >= 0 && blk < p.num_blocks) bytes += (uint32_t)bs * 128u * KCH;
+                else raise_error(DSA_DEVERR_INDEX);
+              }
+              mbar_arrive_expect_tx(fb, bytes);
+              for (int pg = pg0; pg <= pg1; ++pg) {
+                const int64_t blk = es->pages[pg - win0];
+                if (blk < 0 || blk >= p.num_blocks) continue;
+                const uint32_t dst = stage + (uint32_t)(pg - pg0) * (uint32_t)bs * 128u;
+                for (int kc = 0; kc < KCH; ++kc)
+                  tma_load_2d(dst + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), (int32_t)(blk * bs));
+              }
+            }
+            last_issue[s] = T;
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      if (!ok) break;
+      tiles_issued += it.ntiles;
+    }
+    if (lane == 0) {
+      if (!ok) {
+        raise_error(DSA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
       }
       // Own copies must land before this CTA can exit (matters only after an abort).
-      mbar_wait(qfull, 0, kCleanupWaitNs, nullptr);
+      if (items_issued > 0) mbar_wait(qfull, (uint32_t)(items_issued - 1) & 1u, kCleanupWaitNs, nullptr);
       for (int s = 0; s < S && s < 8; ++s)
         if (last_issue[s] >= 0) mbar_wait(full0 + 8 * s, (uint32_t)(last_issue[s] / S) & 1u, kCleanupWaitNs, nullptr);
     }
   } else if (warp == 1) {
     // ============================ MMA issuer ============================
-    if (lane == 0 && ntiles > 0) {
-      bool ok = mbar_wait(qfull, 0, limit, abort_flag);
-      const uint32_t qbase = smem_u32(q_s);
-      for (int i = 0; ok && i < ntiles; ++i) {
-        const int s = i % S;
-        const int a = i & 1;
-        ok = mbar_wait(full0 + 8 * s, (uint32_t)(i / S) & 1u, limit, abort_flag) &&
-             mbar_wait(tempty0 + 8 * a, ((uint32_t)(i >> 1) & 1u) ^ 1u, limit, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t stage = smem_u32(k_s + (size_t)s * K_BYTES);
-        const uint32_t d = tmem_base + (uint32_t)(a * N);
+    if (lane == 0) {
+      int T = 0;
+      bool ok = true;
+      for (int n = 0; ok; ++n) {
+        const int slot = n & 1;
+        if (!(ok = mbar_wait(ifull0 + 8 * slot, (uint32_t)(n >> 1) & 1u, limit, abort_flag))) break;
+        const ItemInfo it = es->info[slot];
+        if (!it.valid) break;
+        if (!(ok = mbar_wait(qfull, (uint32_t)n & 1u, limit, abort_flag))) break;
+        const uint32_t qbase = smem_u32(q_s);
+        for (int i = 0; i < it.ntiles; ++i, ++T) {
+          const int s = T % S;
+          const int a = T & 1;
+          ok = mbar_wait(full0 + 8 * s, (uint32_t)(T / S) & 1u, limit, abort_flag) &&
+               mbar_wait(tempty0 + 8 * a, ((uint32_t)(T >> 1) & 1u) ^ 1u, limit, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t stage = smem_u32(k_s + (size_t)s * K_BYTES);
+          const uint32_t d = tmem_base + (uint32_t)(a * N);
 #pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-          const uint32_t off = (uint32_t)(kk & 3) * 32u;   // 16 bf16 / 32 E4M3 along K
-          const uint64_t adesc = smem_desc_sw128(stage + (uint32_t)(kk >> 2) * K_CHUNK + off);
-          const uint64_t bdesc = smem_desc_sw128(qbase + (uint32_t)(kk >> 2) * Q_CHUNK + off);
-          if (kFP8)
-            mma_e4m3(d, adesc, bdesc, IDESC, kk > 0 ? 1u : 0u);
-          else
-            mma_bf16(d, adesc, bdesc, IDESC, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            const uint32_t off = (uint32_t)(kk & 3) * 32u;   // 16 bf16 / 32 E4M3 along K
+            const uint64_t adesc = smem_desc_sw128(stage + (uint32_t)(kk >> 2) * K_CHUNK + off);
+            const uint64_t bdesc = smem_desc_sw128(qbase + (uint32_t)(kk >> 2) * Q_CHUNK + off);
+            if (kFP8)
+              mma_e4m3(d, adesc, bdesc, IDESC, kk > 0 ? 1u : 0u);
+            else
+              mma_bf16(d, adesc, bdesc, IDESC, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(empty0 + 8 * s);
+          mma_commit(tfull0 + 8 * a);
         }
-        mma_commit(empty0 + 8 * s);
-        mma_commit(tfull0 + 8 * a);
+        if (!ok) break;
+        mma_commit(qempty);                 // the Q tile is free once this item's MMAs are done
+        mbar_arrive(iempty0 + 8 * slot);
       }
       if (!ok) {
         raise_error(DSA_DEVERR_TIMEOUT);
@@ -282,125 +550,173 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ============================ epilogue ============================
-    const int et = threadIdx.x - 64;            // 0..255
-    const int grp = (warp - 2) >> 2;            // 0: even tiles, 1: odd tiles
+    const int et = threadIdx.x - 64;            // 0..NT-1
+    const int grp = (warp - 2) >> 2;
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;        // key row within the tile
-    const int npairs = (ntiles + 1) / 2;
-    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(grp * N);
+    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const int cap = p.cap;
-
-    for (int m = 0; m < npairs; ++m) {
-      if (kTopk) {
-        group_sync();
+    int T0 = 0;                                 // global index of the item's first tile
+    for (int n = 0;; ++n) {
+      const int slot = n & 1;
+      bool ok = (lane == 0) ? mbar_wait(ifull0 + 8 * slot, (uint32_t)(n >> 1) & 1u, limit, abort_flag) : true;
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (!ok && lane == 0) {
+        raise_error(DSA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // One thread decides for the whole group between two barriers (the abort flag may
+      // change at any time); an expired wait means the producer is gone: stop as on the
+      // end-of-work descriptor.
+      group_sync<NT>();
+      if (et == 0) es->stop = (*abort_flag != 0) || !es->info[slot].valid;
+      group_sync<NT>();
+      if (es->stop) break;
+      const ItemInfo it = es->info[slot];
+      // per-item head weights (q scale folded in for E4M3)
+      for (int e = et; e < NQ * 64; e += NT) {
+        const int q = e >> 6, h = e & 63;
+        float w = 0.f;
+        if (q < it.nreal) {
+          const int64_t o = (int64_t)(it.t0 + q) * 64 + h;
+          w = __ldg(p.weights + o);
+          if (kFP8) w *= __ldg(p.q_scale + o);
+        }
+        es->w[slot][q][h] = w;
+      }
+      if (kTopk && et < 4) {
+        es->cnt[et] = 0;
+        es->thr[et] = 0;
+      }
+      group_sync<NT>();
+      const float* wq = &es->w[slot][0][0];
+      const int niter = (it.ntiles + EG - 1) / EG;
+      const int first = ((grp - T0) % EG + EG) % EG;   // this group's first local tile
+      for (int m = 0; m < niter; ++m) {
+        if (kTopk) {
+          group_sync<NT>();
 #pragma unroll 1
+          for (int q = 0; q < NQ; ++q) {
+            const uint32_t cn = es->cnt[q];
+            if (cn > (uint32_t)(cap - 128 * EG)) {
+              uint64_t* buf = ebuf + (size_t)q * cap;
+              const uint64_t thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
+              engine_compact<NT, kMaxPer * 2 / EG>(buf, &es->cnt[q], (int)cn, thr, et);
+              if (et == 0) es->thr[q] = thr;
+              group_sync<NT>();
+            }
+          }
+        }
+        const int i = EG * m + first;
+        if (i >= it.ntiles) continue;
+        const int T = T0 + i;
+        const int a = T & 1;
+        const int j = it.ks + i * 128 + row;
+        bool valid = true;
+        float kscale = 1.f;
+        if (paged) {
+          const int64_t pg = j / bs;
+          int64_t blk = -1;
+          if (j < it.L && pg < p.bt_stride) blk = __ldg(p.block_table + (int64_t)it.b * p.bt_stride + pg);
+          valid = blk >= 0 && blk < p.num_blocks;
+          if (kFP8 && valid) kscale = __ldg(p.k_scale + blk * bs + (j % bs));
+        } else {
+          valid = j < p.num_rows;
+          if (kFP8 && valid) kscale = __ldg(p.k_scale + j);
+        }
+        bool okt = (lane == 0) ? mbar_wait(tfull0 + 8 * a, (uint32_t)(T >> 1) & 1u, limit, abort_flag) : true;
+        okt = __shfl_sync(0xFFFFFFFFu, okt ? 1 : 0, 0) != 0;
+        if (!okt) {
+          if (lane == 0) {
+            raise_error(DSA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          continue;
+        }
+        __syncwarp();
+        tc_fence_after();
+        float v[NQ];
+#pragma unroll
         for (int q = 0; q < NQ; ++q) {
-          const uint32_t n = es->cnt[q];
-          if (n > (uint32_t)(cap - 256)) {
-            uint64_t* buf = ebuf + (size_t)q * cap;
-            const uint64_t thr = engine_select(buf, (int)n, p.topk, &es->esc, et);
-            engine_compact<kMaxPer>(buf, &es->cnt[q], (int)n, thr, et);
-            if (et == 0) es->thr[q] = thr;
-            group_sync();
+          float acc[64];
+          tmem_ld64(t_lane + (uint32_t)(a * N + q * 64), acc);
+          float s = head_sum(acc, wq + q * 64);
+          if (kFP8) s = s * kscale;
+          v[q] = canon_zero(s);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * a);
+
+        if (!kTopk) {
+          if (j < p.max_len) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+              if (q < it.nreal)
+                p.logits[(int64_t)(it.t0 + q) * p.ld + j] = (valid && j < it.vis[q]) ? v[q] : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            const uint64_t key = rank_key(v[q], (uint32_t)j);
+            const bool take = valid && j < it.vis[q] && is_candidate(v[q]) && key >= es->thr[q];
+            engine_append(ebuf + (size_t)q * cap, &es->cnt[q], key, take, (uint32_t)cap, 10u);
           }
         }
       }
-      const int i = 2 * m + grp;
-      if (i >= ntiles) continue;
-      const int j = ks + i * 128 + row;
-      // key validity and (E4M3) key scale, fetched before waiting on the MMA
-      bool valid = true;
-      float kscale = 1.f;
-      if (paged) {
-        const int64_t pg = j / bs;
-        int64_t blk = -1;
-        if (j < L && pg < p.bt_stride) blk = __ldg(p.block_table + (int64_t)b * p.bt_stride + pg);
-        valid = blk >= 0 && blk < p.num_blocks;
-        if (kFP8 && valid) kscale = __ldg(p.k_scale + blk * bs + (j % bs));
-      } else {
-        valid = j < p.num_rows;
-        if (kFP8 && valid) kscale = __ldg(p.k_scale + j);
-      }
-      bool ok = (lane == 0) ? mbar_wait(tfull0 + 8 * grp, (uint32_t)m & 1u, limit, abort_flag) : true;
-      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-      if (!ok) {
-        if (lane == 0) {
-          raise_error(DSA_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-        }
-        continue;
-      }
-      __syncwarp();
-      tc_fence_after();
-      float v[NQ];
-#pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        float acc[64];
-        tmem_ld64(t_lane + (uint32_t)(q * 64), acc);
-        float s = head_sum(acc, es->w[q]);
-        if (kFP8) s = s * kscale;
-        v[q] = canon_zero(s);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * grp);
+      T0 += it.ntiles;
 
       if (!kTopk) {
-        if (j < p.max_len) {
-#pragma unroll
-          for (int q = 0; q < NQ; ++q)
-            if (q < nreal)
-              p.logits[(int64_t)(t0 + q) * p.ld + j] = (valid && j < vis[q]) ? v[q] : -INFINITY;
-        }
+        // keys of this chunk past the last processed tile are masked for every row
+        const int f0 = it.ks + it.ntiles * 128;
+        const int f1 = min(it.ks + it.chunk, p.max_len);
+        for (int q = 0; q < it.nreal; ++q)
+          for (int jj = f0 + et; jj < f1; jj += NT) p.logits[(int64_t)(it.t0 + q) * p.ld + jj] = -INFINITY;
       } else {
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-          const uint64_t key = rank_key(v[q], (uint32_t)j);
-          const bool take = valid && j < vis[q] && is_candidate(v[q]) && key >= es->thr[q];
-          engine_append(ebuf + (size_t)q * cap, &es->cnt[q], key, take);
-        }
-      }
-    }
-
-    if (!kTopk) {
-      // keys of this chunk past the last processed tile are masked for every row
-      const int f0 = ks + ntiles * 128;
-      const int f1 = min(ks + p.chunk, p.max_len);
-      for (int q = 0; q < nreal; ++q)
-        for (int jj = f0 + et; jj < f1; jj += 256) p.logits[(int64_t)(t0 + q) * p.ld + jj] = -INFINITY;
-    } else {
-      group_sync();
+        group_sync<NT>();
 #pragma unroll 1
-      for (int q = 0; q < NQ; ++q) {
-        const uint32_t n = es->cnt[q];
-        if (n > (uint32_t)p.topk) {
-          uint64_t* buf = ebuf + (size_t)q * cap;
-          const uint64_t thr = engine_select(buf, (int)n, p.topk, &es->esc, et);
-          engine_compact<kMaxPer>(buf, &es->cnt[q], (int)n, thr, et);
+        for (int q = 0; q < NQ; ++q) {
+          const uint32_t cn = es->cnt[q];
+          if (cn > (uint32_t)p.topk) {
+            uint64_t* buf = ebuf + (size_t)q * cap;
+            const uint64_t thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
+            engine_compact<NT, kMaxPer * 2 / EG>(buf, &es->cnt[q], (int)cn, thr, et);
+          }
         }
-      }
-      group_sync();
-      const int P = p.pow2;
-      for (int q = 0; q < NQ; ++q) {
-        const int n = (int)es->cnt[q];
-        for (int e = n + et; e < P; e += 256) ebuf[(size_t)q * cap + e] = 0ull;
-      }
-      group_sync();
-      engine_sort(ebuf, cap, NQ, P, et);
-      const bool split = p.nchunks > 1;
-      for (int q = 0; q < nreal; ++q) {
-        const int64_t t = t0 + q;
-        const uint64_t* buf = ebuf + (size_t)q * cap;
-        for (int s = et; s < p.topk; s += 256) {
-          const uint64_t key = buf[s];
-          if (split) {
-            p.partial[((size_t)t * p.nchunks + c) * p.topk + s] = key;
-          } else {
-            p.out_idx[t * p.topk + s] = key ? index_of_key(key) : -1;
-            if (p.out_val) p.out_val[t * p.topk + s] = key ? value_of_key(key) : -INFINITY;
+        group_sync<NT>();
+        if (it.nl == 1) {
+          // the whole group in one item: final, sorted rows
+          const int P = p.pow2;
+          for (int q = 0; q < NQ; ++q) {
+            const int cn = (int)es->cnt[q];
+            for (int e = cn + et; e < P; e += NT) ebuf[(size_t)q * cap + e] = 0ull;
+          }
+          group_sync<NT>();
+          engine_sort<NT>(ebuf, cap, NQ, P, et);
+          for (int q = 0; q < it.nreal; ++q) {
+            const int64_t t = it.t0 + q;
+            const uint64_t* buf = ebuf + (size_t)q * cap;
+            for (int s = et; s < p.topk; s += NT) {
+              const uint64_t key = buf[s];
+              p.out_idx[t * p.topk + s] = key ? index_of_key(key) : -1;
+              if (p.out_val) p.out_val[t * p.topk + s] = key ? value_of_key(key) : -INFINITY;
+            }
+          }
+        } else {
+          // this chunk's top-k of every query row, unsorted and zero-padded; the merge
+          // kernel ranks the group's lists
+          for (int q = 0; q < it.nreal; ++q) {
+            const int64_t t = it.t0 + q;
+            const int cn = (int)es->cnt[q];
+            const uint64_t* buf = ebuf + (size_t)q * cap;
+            for (int s = et; s < p.topk; s += NT)
+              p.partial[((size_t)t * p.nl_max + it.c) * p.topk + s] = s < cn ? buf[s] : 0ull;
           }
         }
       }
+      // item slot and its weights free for the producer
+      group_sync<NT>();
+      if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
     }
   }
 
@@ -448,13 +764,15 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, uint64_t rows, uint32_
 }
 
 constexpr size_t kSmemLimit = 232448;   // max dynamic shared memory per CTA (227 KB)
+constexpr size_t kSmemHalf = 115712;    // two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
+constexpr int64_t kSplitUnits = 1216;   // fewer query groups than this: rows may be split
 
 size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap) {
   const size_t elt = fp8 ? 1 : 2;
   size_t s = 1024;                                    // alignment slack
   s += (size_t)nq * 64 * 128 * elt;                  // Q tile
   s += (size_t)stages * 128 * 128 * elt;             // key ring
-  s += (size_t)(2 * stages + 6) * 8;                 // barriers
+  s += (size_t)(2 * stages + 12) * 8;                // barriers
   s += sizeof(EpiSmem<4>) + 16;
   if (topk) s += (size_t)nq * cap * 8;
   return s;
@@ -468,13 +786,17 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
   pl.nq = qs.next_n == 1 ? 1 : (qs.next_n == 2 ? 2 : 4);
   if (tk) {
     pl.pow2 = next_pow2(topk);
-    const int c0 = pl.pow2 > topk + 512 ? pl.pow2 : topk + 512;
+    // room for several tiles of inserts between cut-backs
+    const int c0 = pl.pow2 > 2 * topk ? pl.pow2 : (topk + 1024 > 2 * topk ? topk + 1024 : 2 * topk);
     pl.cap = ((c0 + 255) / 256) * 256;
+    if (pl.cap > 256 * kMaxPer) pl.cap = 256 * kMaxPer;
   }
   pl.ok = true;
-  // deepest key ring that fits, 2..8 stages; fewer query rows if the candidate buffers do not fit
+  // One epilogue group (192 threads) for one or two query rows per item, with two CTAs
+  // per SM where shared memory allows; two groups (320 threads) for four rows.
   for (;;) {
-    int st = 8;
+    pl.eg = pl.nq <= 2 ? 1 : 2;
+    int st = 4;
     while (st >= 2 && smem_bytes(fp8, pl.nq, st, tk, pl.cap) > kSmemLimit) --st;
     if (st >= 2) {
       pl.stages = st;
@@ -486,16 +808,24 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
     }
     pl.nq >>= 1;
   }
-  if (tk && pl.cap > 256 * kMaxPer) pl.ok = false;
-  // decode-sized batches split each row's keys so that enough CTAs stream them
-  pl.stages = pl.stages > 4 ? 4 : pl.stages;
+  pl.ctas_per_sm = 1;
+  if (pl.eg == 1) {
+    int st = 4;
+    while (st >= 2 && smem_bytes(fp8, pl.nq, st, tk, pl.cap) > kSmemHalf) --st;
+    if (st >= 2) {
+      pl.stages = st;
+      pl.ctas_per_sm = 2;
+    }
+  }
+  if (tk && (pl.cap < topk + 128 * pl.eg || pl.cap < pl.pow2)) pl.ok = false;
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
   pl.ngroups = (qs.next_n + pl.nq - 1) / pl.nq;
+  const int64_t units = (int64_t)qs.B * pl.ngroups;
+  // logits mode: static chunks of the longest row, split when groups are few
   const int64_t full = ((int64_t)qs.max_context_len + 127) / 128 * 128;
   int64_t chunk = full;
-  const int64_t units = (int64_t)qs.B * pl.ngroups;
-  if (units < 1216) {
-    const int64_t want = (full * units + 1215) / 1216;
+  if (units < kSplitUnits) {
+    const int64_t want = (full * units + 2431) / 2432;
     chunk = (want + 127) / 128 * 128;
     if (chunk < 2048) chunk = 2048;
     if (chunk > full) chunk = full;
@@ -505,28 +835,38 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
   pl.nchunks = (int)((qs.max_context_len + chunk - 1) / chunk);
   if (pl.nchunks < 1) pl.nchunks = 1;
   pl.items = units * pl.nchunks;
-  pl.ws_bytes = (tk && pl.nchunks > 1) ? (size_t)qs.B * qs.next_n * pl.nchunks * topk * 8 : 0;
+  // top-k mode: the device plans its own chunks; workspace = [plan][work counter][partial lists]
+  pl.nl_max = units < kSplitUnits ? kMaxLists : 1;
+  if (tk) {
+    size_t off = ((size_t)(kPlanHeader + units * pl.nl_max) * 4 + 15) / 16 * 16;
+    pl.work_off = off;
+    off += 16;
+    pl.partial_off = off;
+    if (pl.nl_max > 1) off += (size_t)qs.B * qs.next_n * pl.nl_max * topk * 8;
+    pl.ws_bytes = off;
+    pl.items = units * pl.nl_max;
+  }
   return pl;
 }
 
-template <bool kFP8, int NQ, bool kTopk>
+template <bool kFP8, int NQ, bool kTopk, int EG>
 static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& prm,
-                              const IndexerPlan& pl, cudaStream_t st) {
-  auto kern = indexer_kernel<kFP8, NQ, kTopk>;
+                              const IndexerPlan& pl, int grid, cudaStream_t st) {
+  auto kern = indexer_kernel<kFP8, NQ, kTopk, EG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)pl.items, 320, pl.smem, st>>>(mq, mk, prm);
+  kern<<<(unsigned)grid, 64 + 128 * EG, pl.smem, st>>>(mq, mk, prm);
   note_launch();
   return cudaGetLastError();
 }
 
 template <bool kFP8, bool kTopk>
 static cudaError_t dispatch_nq(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& prm,
-                               const IndexerPlan& pl, cudaStream_t st) {
+                               const IndexerPlan& pl, int grid, cudaStream_t st) {
   switch (pl.nq) {
-    case 1: return launch_one<kFP8, 1, kTopk>(mq, mk, prm, pl, st);
-    case 2: return launch_one<kFP8, 2, kTopk>(mq, mk, prm, pl, st);
-    default: return launch_one<kFP8, 4, kTopk>(mq, mk, prm, pl, st);
+    case 1: return launch_one<kFP8, 1, kTopk, 1>(mq, mk, prm, pl, grid, st);
+    case 2: return launch_one<kFP8, 2, kTopk, 1>(mq, mk, prm, pl, grid, st);
+    default: return launch_one<kFP8, 4, kTopk, 2>(mq, mk, prm, pl, grid, st);
   }
 }
 
@@ -563,17 +903,35 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   prm.pow2 = pl.pow2;
   prm.out_idx = a.out_idx;
   prm.out_val = a.out_val;
-  prm.partial = reinterpret_cast<uint64_t*>(a.ws);
-  cudaError_t e;
+  prm.nl_max = pl.nl_max;
   const bool tk = a.topk > 0;
+  const int slots = device_sm_count() * pl.ctas_per_sm;
+  int64_t grid = slots;
+  cudaError_t e;
+  if (tk) {
+    char* ws = static_cast<char*>(a.ws);
+    int32_t* plan = reinterpret_cast<int32_t*>(ws);
+    prm.plan = plan;
+    prm.work = reinterpret_cast<uint32_t*>(ws + pl.work_off);
+    prm.partial = pl.nl_max > 1 ? reinterpret_cast<uint64_t*>(ws + pl.partial_off) : nullptr;
+    const int target = pl.nl_max > 1 ? 2 * slots : 1;   // about two items per CTA when rows split
+    plan_kernel<<<1, 1024, 0, stream>>>(a.qs.context_lens, a.qs.B, a.qs.next_n, a.qs.causal,
+                                        a.qs.max_context_len, pl.nq, pl.ngroups, target, pl.nl_max, plan,
+                                        prm.work);
+    note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else if (grid > pl.items) {
+    grid = pl.items;
+  }
   if (a.fp8)
-    e = tk ? dispatch_nq<true, true>(mq, mk, prm, pl, stream) : dispatch_nq<true, false>(mq, mk, prm, pl, stream);
+    e = tk ? dispatch_nq<true, true>(mq, mk, prm, pl, (int)grid, stream)
+           : dispatch_nq<true, false>(mq, mk, prm, pl, (int)grid, stream);
   else
-    e = tk ? dispatch_nq<false, true>(mq, mk, prm, pl, stream) : dispatch_nq<false, false>(mq, mk, prm, pl, stream);
-  if (e != cudaSuccess) return e;
-  if (tk && pl.nchunks > 1)
-    e = launch_merge(prm.partial, pl.nchunks, pl.chunk, a.qs, a.topk, a.out_idx, a.out_val, stream);
-  return e;
+    e = tk ? dispatch_nq<false, true>(mq, mk, prm, pl, (int)grid, stream)
+           : dispatch_nq<false, false>(mq, mk, prm, pl, (int)grid, stream);
+  if (e != cudaSuccess || !tk || pl.nl_max == 1) return e;
+  // rows split over several chunks: rank each group's lists
+  return launch_merge(prm.partial, pl.nl_max, prm.plan, 0, pl.nq, a.qs, a.topk, a.out_idx, a.out_val, stream);
 }
 
 DSA_DEFINE_TU_ERROR_ACCESSORS(indexer)

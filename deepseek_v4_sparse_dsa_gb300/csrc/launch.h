@@ -16,15 +16,20 @@ int device_sm_count();   // SMs of the current device (cached per device)
 // ------------------------------------------------------------------ indexer (indexer.cu)
 struct IndexerPlan {
   int nq;            // query rows per work item (1, 2 or 4)
+  int eg;            // epilogue warp groups of 128 threads (1 or 2)
   int stages;        // key-tile pipeline depth
-  int chunk;         // keys per work item (multiple of 128)
-  int nchunks;       // ceil(max_context_len / chunk)
+  int ctas_per_sm;   // resident CTAs per SM the shared memory allows (1 or 2)
+  int chunk;         // logits mode: keys per work item (multiple of 128)
+  int nchunks;       // logits mode: ceil(max_context_len / chunk)
   int ngroups;       // ceil(next_n / nq)
+  int nl_max;        // top-k mode: key chunks per query group at most (1 = rows never split)
   int cap;           // candidate-buffer capacity per query row (top-k mode)
   int pow2;          // next power of two >= topk
   size_t smem;       // dynamic shared memory per CTA
-  int64_t items;     // grid size
-  size_t ws_bytes;   // workspace for partial lists (0 when nchunks == 1)
+  int64_t items;     // work items (upper bound)
+  size_t ws_bytes;   // workspace bytes (top-k mode)
+  size_t work_off;   // byte offset of the work-item counter in ws
+  size_t partial_off;  // byte offset of the partial lists in ws
   bool ok;           // false: shape does not fit this build
 };
 
@@ -52,12 +57,9 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& plan, cudaSt
 
 // ------------------------------------------------------------------ top-k (topk.cu)
 struct TopkPlan {
-  int chunk;         // logits per CTA
-  int nchunks;
-  int cap;
-  int pow2;
-  size_t smem;
-  size_t ws_bytes;
+  int pow2;          // next power of two >= topk (sorted slots per row)
+  size_t smem;       // dynamic shared memory per CTA
+  size_t ws_bytes;   // workspace bytes (none needed: 0)
 };
 
 TopkPlan plan_topk(const dsa_queries& qs, int topk);
@@ -65,10 +67,12 @@ TopkPlan plan_topk(const dsa_queries& qs, int topk);
 cudaError_t launch_topk(const float* logits, int64_t ld, const dsa_queries& qs, int topk, int32_t* out_idx,
                         float* out_val, void* ws, const TopkPlan& plan, cudaStream_t stream);
 
-// Merges nchunks partial lists per row (ws layout [T][nchunks][topk] of ranking keys,
-// 0 = empty) into the final top-k.  Row t reads its first ceil(vis_t / chunk) lists.
-cudaError_t launch_merge(const uint64_t* partial, int nchunks, int chunk, const dsa_queries& qs, int topk,
-                         int32_t* out_idx, float* out_val, cudaStream_t stream);
+// Ranks the partial lists of split rows.  partial: [T][nl_max][topk] ranking keys (0 =
+// empty).  Row t belongs to a group of nq query rows whose longest visible range spans
+// nl = ceil(vis / chunk) chunks (chunk read from dev_chunk when given); rows with nl == 1
+// were finished by the producing kernel and are skipped.
+cudaError_t launch_merge(const uint64_t* partial, int nl_max, const int32_t* dev_chunk, int chunk, int nq,
+                         const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val, cudaStream_t stream);
 
 // ------------------------------------------------------------------ gather (gather.cu)
 cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_t num_blocks, int bs,

@@ -4,18 +4,14 @@
 // canonical top-k sort): larger value first, then the smaller key index; -0.0 == +0.0;
 // -inf / NaN never selected; short rows padded with -1.
 //
-// Both kernels stream candidates through the shared-memory engine of common.cuh: a
-// candidate is appended when its ranking key is >= the current threshold; when the
-// buffer could overflow in the next round it is cut back to the top-k by a radix select
-// (which also raises the threshold); the survivors are sorted at the end.  Long rows are
-// split over several CTAs whose sorted lists are merged by the same engine.
+// Both use the radix select, append and sort of common.cuh.  The standalone top-k reads
+// each row straight from memory (a few select passes, one collect pass); the merge ranks
+// the per-chunk lists the fused indexer kernel wrote for rows it split.
 #include "common.cuh"
 #include "launch.h"
 
 namespace dsa {
 
-constexpr int kTopkMaxPer = 12;   // capacity <= 256 * 12
-constexpr int kRound = 1024;      // candidates per round (4 per thread)
 
 __device__ __forceinline__ int visible_len(const int32_t* context_lens, int t, int next_n, int causal,
                                            int max_len, bool report) {
@@ -34,171 +30,222 @@ struct TopkShared {
   EngineScratch esc;
 };
 
-__device__ void finish_list(uint64_t* buf, TopkShared* sh, int topk, int P, int tid, int64_t t, int nchunks,
-                            int c, int32_t* out_idx, float* out_val, uint64_t* partial) {
-  group_sync();
-  const uint32_t n = sh->cnt;
-  if (n > (uint32_t)topk) {
-    const uint64_t thr = engine_select(buf, (int)n, topk, &sh->esc, tid);
-    engine_compact<kTopkMaxPer>(buf, &sh->cnt, (int)n, thr, tid);
-  }
-  const int m = (int)sh->cnt;
-  for (int e = m + tid; e < P; e += kEngineThreads) buf[e] = 0ull;
-  group_sync();
-  engine_sort(buf, P, 1, P, tid);
-  for (int s = tid; s < topk; s += kEngineThreads) {
-    const uint64_t key = buf[s];
-    if (partial) {
-      partial[((size_t)t * nchunks + c) * topk + s] = key;
-    } else {
-      out_idx[t * topk + s] = key ? index_of_key(key) : -1;
-      if (out_val) out_val[t * topk + s] = key ? value_of_key(key) : -INFINITY;
-    }
-  }
+constexpr int kRowNT = 1024;        // standalone top-k: threads per row
+
+// Ranking key of logits[t, j]: 0 (never selected) past the visible range or for -inf/NaN.
+__device__ __forceinline__ uint64_t row_key(const float* __restrict__ row, int j, int vis) {
+  if (j >= vis) return 0ull;
+  const float v = __ldg(row + j);
+  return is_candidate(v) ? rank_key(v, (uint32_t)j) : 0ull;
 }
 
-__global__ void __launch_bounds__(256) topk_rows_kernel(const float* __restrict__ logits, int64_t ld,
-                                                        const int32_t* __restrict__ context_lens, int next_n,
-                                                        int causal, int max_len, int topk, int chunk,
-                                                        int nchunks, int cap, int P, int32_t* out_idx,
-                                                        float* out_val, uint64_t* partial) {
-  extern __shared__ uint64_t buf[];
-  __shared__ TopkShared sh;
-  const int tid = threadIdx.x;
-  const int64_t t = blockIdx.x / nchunks;
-  const int c = blockIdx.x % nchunks;
-  const int vis = visible_len(context_lens, (int)t, next_n, causal, max_len, tid == 0 && c == 0);
-  const int j0 = c * chunk;
-  const int j1 = min(j0 + chunk, vis);
-  if (tid == 0) {
-    sh.cnt = 0;
-    sh.thr = 0;
-  }
-  const float* row = logits + t * ld;
-  float nxt[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int j = j0 + u * 256 + tid;
-    nxt[u] = j < j1 ? __ldg(row + j) : -INFINITY;
-  }
-  for (int base = j0; base < j1; base += kRound) {
-    float v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      v[u] = nxt[u];
-      const int j = base + kRound + u * 256 + tid;
-      nxt[u] = j < j1 ? __ldg(row + j) : -INFINITY;
-    }
-    group_sync();
-    const uint32_t n = sh.cnt;
-    if (n > (uint32_t)(cap - kRound)) {
-      const uint64_t thr = engine_select(buf, (int)n, topk, &sh.esc, tid);
-      engine_compact<kTopkMaxPer>(buf, &sh.cnt, (int)n, thr, tid);
-      if (tid == 0) sh.thr = thr;
-      group_sync();
-    }
-    const uint64_t thr = sh.thr;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = base + u * 256 + tid;
-      const uint64_t key = rank_key(v[u], (uint32_t)j);
-      engine_append(buf, &sh.cnt, key, j < j1 && is_candidate(v[u]) && key >= thr);
-    }
-  }
-  finish_list(buf, &sh, topk, P, tid, t, nchunks, c, out_idx, out_val, nchunks > 1 ? partial : nullptr);
-}
-
-__global__ void __launch_bounds__(256) merge_kernel(const uint64_t* __restrict__ partial, int nchunks, int chunk,
-                                                    const int32_t* __restrict__ context_lens, int next_n,
-                                                    int causal, int max_len, int topk, int cap, int P,
-                                                    int32_t* out_idx, float* out_val) {
-  extern __shared__ uint64_t buf[];
-  __shared__ TopkShared sh;
+// One CTA per query row.  The row's visible logits are read straight from memory in a
+// few passes: a most-significant-digit radix select over the 64-bit ranking keys finds
+// the k-th key (passes stop as soon as the chosen bin holds exactly the keys still
+// needed), one more pass collects the keys at or above it -- exactly min(k, candidates)
+// of them -- into shared memory, where they are sorted and written.
+__global__ void __launch_bounds__(kRowNT) topk_rows_kernel(const float* __restrict__ logits, int64_t ld,
+                                                           const int32_t* __restrict__ context_lens, int next_n,
+                                                           int causal, int max_len, int topk, int P,
+                                                           int32_t* out_idx, float* out_val) {
+  extern __shared__ uint64_t sel[];     // P slots
+  __shared__ EngineScratch esc;
+  __shared__ uint32_t cnt;
+  constexpr int NT = kRowNT;
   const int tid = threadIdx.x;
   const int64_t t = blockIdx.x;
-  const int vis = visible_len(context_lens, (int)t, next_n, causal, max_len, false);
-  const int nl = min((vis + chunk - 1) / chunk, nchunks);
-  if (tid == 0) {
-    sh.cnt = 0;
-    sh.thr = 0;
-  }
-  const uint64_t* src = partial + (size_t)t * nchunks * topk;
-  const int64_t total = (int64_t)nl * topk;
-  for (int64_t base = 0; base < total; base += kRound) {
-    uint64_t v[4];
+  const int vis = visible_len(context_lens, (int)t, next_n, causal, max_len, tid == 0);
+  const float* row = logits + t * ld;
+  // radix select over the keys of this row
+  uint64_t prefix = 0, mask = 0;
+  uint32_t need = (uint32_t)topk;
+  bool all = false;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += NT) esc.hist[i] = 0;
+    group_sync<NT>();
+    for (int base = 0; base < vis; base += 4 * NT) {
+      uint64_t key[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t e = base + u * 256 + tid;
-      v[u] = e < total ? __ldg(src + e) : 0ull;
-    }
-    group_sync();
-    const uint32_t n = sh.cnt;
-    if (n > (uint32_t)(cap - kRound)) {
-      const uint64_t thr = engine_select(buf, (int)n, topk, &sh.esc, tid);
-      engine_compact<kTopkMaxPer>(buf, &sh.cnt, (int)n, thr, tid);
-      if (tid == 0) sh.thr = thr;
-      group_sync();
-    }
-    const uint64_t thr = sh.thr;
+      for (int u = 0; u < 4; ++u) key[u] = row_key(row, base + u * NT + tid, vis);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) engine_append(buf, &sh.cnt, v[u], v[u] != 0ull && v[u] >= thr);
+      for (int u = 0; u < 4; ++u)
+        hist_add(esc.hist, key[u] != 0ull && (key[u] & mask) == prefix, (uint32_t)(key[u] >> shift) & 255u);
+    }
+    group_sync<NT>();
+    if (tid < 32) pick_digit(esc.hist, esc.pick, need, tid);
+    group_sync<NT>();
+    if (shift == 56 && esc.pick[3] <= (uint32_t)topk) {
+      all = true;                       // at most k candidates: take every one
+      break;
+    }
+    const uint32_t d = esc.pick[0], above = esc.pick[1], inbin = esc.pick[2];
+    if (d > 255u) {                     // counts did not add up (cannot happen): keep every candidate
+      if (tid == 0) raise_error(DSA_DEVERR_OVERFLOW | (40u << 8));
+      all = true;
+      break;
+    }
+    need -= above;
+    prefix |= (uint64_t)d << shift;
+    mask |= (uint64_t)0xFF << shift;
+    if (inbin == need) break;
   }
-  finish_list(buf, &sh, topk, P, tid, t, 1, 0, out_idx, out_val, nullptr);
+  const uint64_t thr = all ? 1ull : prefix;
+  if (tid == 0) cnt = 0;
+  group_sync<NT>();
+  for (int base = 0; base < vis; base += NT) {
+    const uint64_t key = row_key(row, base + tid, vis);
+    engine_append(sel, &cnt, key, key != 0ull && key >= thr, (uint32_t)P, 41u);
+  }
+  group_sync<NT>();
+  const int m = min((int)cnt, P);
+  for (int e = m + tid; e < P; e += NT) sel[e] = 0ull;
+  group_sync<NT>();
+  engine_sort<NT>(sel, P, 1, P, tid);
+  for (int s = tid; s < topk; s += NT) {
+    const uint64_t key = sel[s];
+    out_idx[t * topk + s] = key ? index_of_key(key) : -1;
+    if (out_val) out_val[t * topk + s] = key ? value_of_key(key) : -INFINITY;
+  }
 }
 
-static int topk_cap(int topk) {
-  const int p2 = next_pow2(topk);
-  const int c0 = p2 > topk + kRound ? p2 : topk + kRound;
-  return ((c0 + 255) / 256) * 256;
+constexpr int kMergeNT = 512;       // merge: threads per row
+constexpr int kMergeKeys = 16384;   // merge: candidates held in shared memory at once
+
+// One CTA per query row of a split group.  The row's nl lists (nl * topk candidates)
+// are loaded into shared memory, a radix select finds the top-k threshold, the survivors
+// are sorted and written.  Rows with more candidates than fit stream through two
+// half-buffers that are cut back to the top-k as they fill.
+__global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restrict__ partial, int nl_max,
+                                                         const int32_t* __restrict__ dev_chunk, int chunk, int nq,
+                                                         const int32_t* __restrict__ context_lens, int next_n,
+                                                         int causal, int max_len, int topk, int P,
+                                                         int32_t* out_idx, float* out_val) {
+  extern __shared__ uint64_t mbuf[];            // kMergeKeys candidates + P sorted slots
+  __shared__ TopkShared sh;
+  constexpr int NT = kMergeNT;
+  const int tid = threadIdx.x;
+  const int64_t t = blockIdx.x;
+  if (dev_chunk) chunk = __ldg(dev_chunk);
+  const int b = (int)(t / next_n), i = (int)(t - (int64_t)b * next_n), gi = i / nq;
+  int L = __ldg(context_lens + b);
+  L = L < 0 ? 0 : (L > max_len ? max_len : L);
+  const int nreal = min(nq, next_n - gi * nq);
+  const int vis_max = causal ? min(max(L - next_n + gi * nq + nreal, 0), L) : L;
+  const int nl = min(max((vis_max + chunk - 1) / chunk, 1), nl_max);
+  if (nl == 1) return;                          // finished by the producing kernel
+  const uint64_t* src = partial + (size_t)t * nl_max * topk;
+  const int ntot = nl * topk;
+  uint64_t* out = mbuf + kMergeKeys;
+  uint64_t thr;
+  if (ntot <= kMergeKeys) {
+    for (int base = 0; base < ntot; base += 8 * NT) {
+      uint64_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = base + u * NT + tid;
+        v[u] = e < ntot ? __ldcg(src + e) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = base + u * NT + tid;
+        if (e < ntot) mbuf[e] = v[u];
+      }
+    }
+    group_sync<NT>();
+    thr = engine_select<NT>(mbuf, ntot, topk, &sh.esc, tid);
+    if (tid == 0) sh.cnt = 0;
+    group_sync<NT>();
+    for (int base = 0; base < ntot; base += NT) {
+      const int e = base + tid;
+      const uint64_t key = e < ntot ? mbuf[e] : 0ull;
+      engine_append(out, &sh.cnt, key, key != 0ull && key >= thr, (uint32_t)P, 30u);
+    }
+  } else {
+    constexpr int kHalf = kMergeKeys / 2;
+    uint64_t* cur = mbuf;
+    uint64_t* alt = mbuf + kHalf;
+    if (tid == 0) {
+      sh.cnt = 0;
+      sh.thr = 0;
+    }
+    for (int base = 0; base < ntot; base += 4 * NT) {
+      uint64_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = base + u * NT + tid;
+        v[u] = e < ntot ? __ldcg(src + e) : 0ull;
+      }
+      group_sync<NT>();
+      const uint32_t n = sh.cnt;
+      if (n > (uint32_t)(kHalf - 4 * NT)) {
+        const uint64_t th = engine_select<NT>(cur, (int)n, topk, &sh.esc, tid);
+        engine_compact_to<NT>(cur, alt, &sh.cnt, (int)n, th, tid, (uint32_t)kHalf);
+        uint64_t* tmp = cur;
+        cur = alt;
+        alt = tmp;
+        if (tid == 0) sh.thr = th;
+        group_sync<NT>();
+      }
+      const uint64_t th = sh.thr;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        engine_append(cur, &sh.cnt, v[u], v[u] != 0ull && v[u] >= th, (uint32_t)kHalf, 31u);
+    }
+    group_sync<NT>();
+    const uint32_t n = sh.cnt;
+    thr = engine_select<NT>(cur, (int)n, topk, &sh.esc, tid);
+    if (tid == 0) sh.cnt = 0;
+    group_sync<NT>();
+    for (int base = 0; base < (int)n; base += NT) {
+      const int e = base + tid;
+      const uint64_t key = e < (int)n ? cur[e] : 0ull;
+      engine_append(out, &sh.cnt, key, key != 0ull && key >= thr, (uint32_t)P, 32u);
+    }
+  }
+  group_sync<NT>();
+  const int m = (int)sh.cnt;
+  for (int e = m + tid; e < P; e += NT) out[e] = 0ull;
+  group_sync<NT>();
+  engine_sort<NT>(out, P, 1, P, tid);
+  for (int s = tid; s < topk; s += NT) {
+    const uint64_t key = out[s];
+    out_idx[t * topk + s] = key ? index_of_key(key) : -1;
+    if (out_val) out_val[t * topk + s] = key ? value_of_key(key) : -INFINITY;
+  }
 }
 
 TopkPlan plan_topk(const dsa_queries& qs, int topk) {
   TopkPlan pl{};
   pl.pow2 = next_pow2(topk);
-  pl.cap = topk_cap(topk);
-  pl.smem = (size_t)pl.cap * 8;
-  const int64_t T = (int64_t)qs.B * qs.next_n;
-  const int64_t full = qs.max_context_len > 0 ? qs.max_context_len : 1;
-  int64_t chunk = full;
-  if (T < 1216) {
-    int64_t want = (full * T + 1215) / 1216;
-    want = (want + kRound - 1) / kRound * kRound;
-    chunk = want < 8192 ? 8192 : want;
-    if (chunk > full) chunk = full;
-  }
-  pl.chunk = (int)chunk;
-  pl.nchunks = (int)((full + chunk - 1) / chunk);
-  pl.ws_bytes = pl.nchunks > 1 ? (size_t)T * pl.nchunks * topk * 8 : 0;
+  pl.smem = (size_t)pl.pow2 * 8;
+  pl.ws_bytes = 0;
   return pl;
 }
 
 cudaError_t launch_topk(const float* logits, int64_t ld, const dsa_queries& qs, int topk, int32_t* out_idx,
                         float* out_val, void* ws, const TopkPlan& pl, cudaStream_t stream) {
+  (void)ws;
   const int64_t T = (int64_t)qs.B * qs.next_n;
   if (T <= 0) return cudaSuccess;
-  uint64_t* partial = reinterpret_cast<uint64_t*>(ws);
   cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
-  topk_rows_kernel<<<(unsigned)(T * pl.nchunks), 256, pl.smem, stream>>>(
-      logits, ld, qs.context_lens, qs.next_n, qs.causal, qs.max_context_len, topk, pl.chunk, pl.nchunks, pl.cap,
-      pl.pow2, out_idx, out_val, partial);
+  topk_rows_kernel<<<(unsigned)T, kRowNT, pl.smem, stream>>>(logits, ld, qs.context_lens, qs.next_n, qs.causal,
+                                                            qs.max_context_len, topk, pl.pow2, out_idx, out_val);
   note_launch();
-  e = cudaGetLastError();
-  if (e != cudaSuccess || pl.nchunks == 1) return e;
-  return launch_merge(partial, pl.nchunks, pl.chunk, qs, topk, out_idx, out_val, stream);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_merge(const uint64_t* partial, int nchunks, int chunk, const dsa_queries& qs, int topk,
-                         int32_t* out_idx, float* out_val, cudaStream_t stream) {
+cudaError_t launch_merge(const uint64_t* partial, int nl_max, const int32_t* dev_chunk, int chunk, int nq,
+                         const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val, cudaStream_t stream) {
   const int64_t T = (int64_t)qs.B * qs.next_n;
   if (T <= 0) return cudaSuccess;
-  const int cap = topk_cap(topk);
-  const size_t smem = (size_t)cap * 8;
+  const int P = next_pow2(topk);
+  const size_t smem = (size_t)(kMergeKeys + P) * 8;
   cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  merge_kernel<<<(unsigned)T, 256, smem, stream>>>(partial, nchunks, chunk, qs.context_lens, qs.next_n, qs.causal,
-                                                   qs.max_context_len, topk, cap, next_pow2(topk), out_idx,
-                                                   out_val);
+  merge_kernel<<<(unsigned)T, kMergeNT, smem, stream>>>(partial, nl_max, dev_chunk, chunk, nq, qs.context_lens,
+                                                        qs.next_n, qs.causal, qs.max_context_len, topk, P, out_idx,
+                                                        out_val);
   note_launch();
   return cudaGetLastError();
 }

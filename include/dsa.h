@@ -63,8 +63,11 @@ typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1 } dsa_dtype;
 typedef enum { DSA_OP_TOPK = 1, DSA_OP_LOGITS_TOPK = 2 } dsa_op;
 
 /* Bits of the per-device error word (see dsa_device_error). */
-#define DSA_DEVERR_INDEX   1u   /* a block id / block-table column was out of range */
-#define DSA_DEVERR_TIMEOUT 2u   /* a bounded device-side wait expired               */
+#define DSA_DEVERR_INDEX    1u  /* a block id / block-table column was out of range    */
+#define DSA_DEVERR_TIMEOUT  2u  /* a bounded device-side wait expired                  */
+#define DSA_DEVERR_OVERFLOW 4u  /* an on-chip candidate buffer would have overflowed:
+                                   the candidate was dropped (an internal error; bits
+                                   8..15 then name the library's internal site)        */
 
 /*
  * Key source of the indexer (the shared MQA key of xkernels issue #27,

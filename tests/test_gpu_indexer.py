@@ -66,9 +66,20 @@ def test_mtp_pairs_paged():
 
 def test_decode_split_rows():
     # few sequences with long rows: the key range is split over CTAs and merged
-    wl = parity.make_case(61, [30000, 9000, 200], next_n=1, block_size=64, topk=512)
+    wl = parity.make_case(61, [30000, 9000, 200, 0], next_n=1, block_size=64, topk=512)
     qs = dsa.make_queries(wl.B, wl.next_n, 0x1000, wl.max_context_len, True)
     assert dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, qs, 512) > 0
+    check_case(wl)
+
+
+def test_decode_split_mtp_rows():
+    # two queries per group, split rows, a group with no visible key
+    wl = parity.make_case(62, [40000, 3, 0, 17000], next_n=2, block_size=32, topk=1024)
+    check_case(wl)
+
+
+def test_decode_split_fp8():
+    wl = parity.make_case(63, [20000, 5000], next_n=1, block_size=64, dtype="e4m3", topk=512)
     check_case(wl)
 
 
