@@ -70,6 +70,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "dsa_indexer_logits_topk": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, dsa_keys,
                                             dsa_queries, c_int, c_void_p, c_void_p, c_void_p, c_size_t,
                                             c_void_p]),
+        "dsa_indexer_logits_topk_noalloc": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, dsa_keys,
+                                                    dsa_queries, c_int, c_void_p, c_void_p, c_void_p]),
         "mxfp4_paged_gather": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_int, c_void_p, c_int64,
                                        c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
         "dsa_workspace_bytes": (c_size_t, [c_int, c_int, dsa_queries, c_int]),
@@ -138,6 +140,15 @@ def dsa_indexer_logits_topk(q, q_scale, dtype, weights, H, D, keys, qs, topk, ou
     _check(load().dsa_indexer_logits_topk(_ptr(q), _ptr(q_scale), int(dtype), _ptr(weights), int(H), int(D), keys,
                                           qs, int(topk), _ptr(out_idx), _ptr(out_val), _ptr(ws), int(ws_bytes),
                                           _stream(stream)), "dsa_indexer_logits_topk")
+
+
+def dsa_indexer_logits_topk_noalloc(q, q_scale, dtype, weights, H, D, keys, qs, topk, out_idx, out_val,
+                                    stream=None):
+    """The fused call without a caller workspace, for callers that cannot allocate
+    device memory (scratch is a fixed 16 MiB array inside the library)."""
+    _check(load().dsa_indexer_logits_topk_noalloc(_ptr(q), _ptr(q_scale), int(dtype), _ptr(weights), int(H),
+                                                  int(D), keys, qs, int(topk), _ptr(out_idx), _ptr(out_val),
+                                                  _stream(stream)), "dsa_indexer_logits_topk_noalloc")
 
 
 def mxfp4_paged_gather(kv_fp4, kv_scale, num_blocks, block_size, D, block_table, bt_stride, sel_pos, B, next_n,

@@ -176,6 +176,30 @@ dsa_status mxfp4_paged_gather(const uint8_t* kv_fp4, const uint8_t* kv_scale, in
                               const int32_t* sel_pos, int B, int next_n, int topk,
                               uint16_t* out, void* stream);
 
+/*
+ * dsa_indexer_logits_topk_noalloc -- dsa_indexer_logits_topk for callers that cannot
+ * allocate device memory: a process whose device memory is all reserved at start-up
+ * and handed out by its own pool, or a latency-critical loop that cannot afford
+ * cudaMalloc / cudaFree (cudaFree waits for the whole device).  (The pages have no
+ * counterpart: this is a convenience of this library.)
+ * Same arguments and results as dsa_indexer_logits_topk, without ws / ws_bytes: the
+ * scratch lives in a fixed 16 MiB array in the library's device image, which every
+ * GPU that loads the library holds until the process exits.
+ *  - A batch whose dsa_workspace_bytes(DSA_OP_LOGITS_TOPK, ...) exceeds 16 MiB is
+ *    rejected with DSA_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *    make that first call before any stream capture.
+ *  - All calls share the one array; the call itself rewrites every part it reads
+ *    (its work list, counter and per-chunk lists), so stale contents never matter.
+ *    Calls whose executions overlap on the GPU (other streams, other threads) race on
+ *    the array: serialise them.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+dsa_status dsa_indexer_logits_topk_noalloc(const void* q, const float* q_scale, dsa_dtype dtype,
+                                           const float* weights, int H, int D, dsa_keys keys,
+                                           dsa_queries qs, int topk, int32_t* out_idx, float* out_val,
+                                           void* stream);
+
 /* Workspace bytes the op needs for this batch shape (host only, no device work). */
 size_t dsa_workspace_bytes(dsa_op op, dsa_dtype dtype, dsa_queries qs, int topk);
 
