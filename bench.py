@@ -45,10 +45,17 @@ WORKLOADS = {
 }
 
 
-def make_workload(name: str, seed: int):
+def make_workload(name: str, seed: int, batch: int = 0):
+    """The named workload; `batch` > 0 shrinks the sequence count of the decode batches
+    (a smaller case of the same kernel for profiler captures)."""
     from deepseek_v4_sparse_dsa_gb300 import synth
-    return {"flash_decode": synth.make_flash_decode, "pro_mtp": synth.make_pro_mtp,
-            "prefill": synth.make_prefill, "fp8_chunked": synth.make_fp8_chunked}[name](seed=seed)
+    fn = {"flash_decode": synth.make_flash_decode, "pro_mtp": synth.make_pro_mtp,
+          "prefill": synth.make_prefill, "fp8_chunked": synth.make_fp8_chunked}[name]
+    if batch > 0:
+        if name not in ("flash_decode", "pro_mtp"):
+            raise SystemExit("--batch applies to the decode workloads only")
+        return fn(seed=seed, B=batch)
+    return fn(seed=seed)
 
 
 def load_peaks():
@@ -168,7 +175,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     dsa.load()
     info = WORKLOADS[args.workload]
-    wl = make_workload(args.workload, info["seed"] + rank)
+    wl = make_workload(args.workload, info["seed"] + rank, args.batch)
     db = DeviceBatch.from_workload(wl, dev)
     stream = torch.cuda.current_stream(dev)
     T, k = wl.T, wl.topk
@@ -278,7 +285,7 @@ def run_ours(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if wl.dtype == "e4m3" else "bf16",
         "data": "synthetic (seeded SplitMix64 generator; no dataset or weights)",
-        "config": {"workload": args.workload, "desc": info["desc"], "B": wl.B, "next_n": wl.next_n,
+        "config": {"workload": args.workload + (f"_b{wl.B}" if args.batch else ""), "desc": info["desc"], "B": wl.B, "next_n": wl.next_n,
                    "topk": k, "sum_context": int(wl.context_lens.sum()), "seed": info["seed"],
                    "l2": "inputs larger than L2" if work["fused_bytes"] > L2_BYTES else "L2 not flushed",
                    "parallelism": f"replicas x{world}"},
@@ -334,7 +341,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     info = WORKLOADS[args.workload]
-    wl = make_workload(args.workload, info["seed"])
+    wl = make_workload(args.workload, info["seed"], args.batch)
     for _ in range(args.warmup):
         oracle_sample(wl, 0.0)
     rows = 0
@@ -352,7 +359,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.T * statistics.mean(per_step),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded SplitMix64 generator; no dataset or weights)",
-        "config": {"workload": args.workload, "desc": info["desc"], "B": wl.B, "next_n": wl.next_n,
+        "config": {"workload": args.workload + (f"_b{wl.B}" if args.batch else ""), "desc": info["desc"], "B": wl.B, "next_n": wl.next_n,
                    "topk": wl.topk},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
@@ -367,6 +374,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="flash_decode", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=0, help="sequences of a decode workload (0: its default)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
