@@ -106,6 +106,48 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
 }
 
 // ---------------------------------------------------------------------------------
+// Work plan of the fused score + top-k (written by plan_kernel, read by the indexer and
+// merge kernels).  Query groups lie end to end on a line; group u spans positions
+// [a0, a1): `cost` positions for its fixed per-item cost, then one per key tile.  The
+// line is cut into slices of Q positions, one per CTA.  A group whose tiles fall in more
+// than one slice is split: each of those slices ranks its piece into an unsorted top-k
+// list in slot 2 * slice (the piece starts at the slice start: the "head") or
+// 2 * slice + 1 (the piece ends the slice: the "tail"); a slice has at most one of each.
+// ---------------------------------------------------------------------------------
+// Header (int32): Q, line length, split-group count, cost, mode, work counter, 0, 0.
+// Mode kPlanSlices: CTA i takes slice i.  Mode kPlanGroups (every group is short next
+// to a slice): CTAs take whole groups from a longest-first list through the counter.
+constexpr int kPlanHeader = 8;
+constexpr int kPlanSlices = 0;
+constexpr int kPlanGroups = 1;
+
+__device__ __forceinline__ int first_tile_slice(int a0, int cost, int Q) { return (a0 + cost) / Q; }
+__device__ __forceinline__ int last_tile_slice(int a1, int Q) { return (a1 - 1) / Q; }
+
+__device__ __forceinline__ bool group_is_split(int a0, int a1, int cost, int Q) {
+  return a1 - a0 > cost && first_tile_slice(a0, cost, Q) != last_tile_slice(a1, Q);
+}
+
+__device__ __forceinline__ int split_slot(int slice, int a0, int cost, int Q) {
+  return 2 * slice + ((a0 + cost > slice * Q) ? 1 : 0);
+}
+
+// ---------------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with the programmatic-serialisation
+// attribute may start while the kernel before it in the stream is still running; it
+// must call grid_dependency_wait() before touching anything that kernel writes (the
+// wait returns once that kernel has completed and its writes are visible; without the
+// attribute it returns at once).  grid_launch_dependents() lets the next such kernel
+// start early.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -3,18 +3,20 @@
 // Score (xkernels issue #27 "DSA indexer + attention: validate/provide gfx942 forward
 // path", comment 2 "What shipped"):  logits[t, j] = sum_h w[t, h] * relu(q[t, h, :] . k[j, :]).
 //
-// Work item = (sequence b, a group of NQ query rows, a chunk of keys).  The contraction
-// runs key-major: A = a tile of 128 keys x D (K-major, shared memory), B = the NQ*64
-// (query, head) rows of q x D, so the accumulator D[key, (query, head)] sits in tensor
-// memory with one key per TMEM lane.  An epilogue thread owns one key and reduces its
-// 64 head columns in registers: ReLU, weight and head sum need no cross-thread traffic.
+// Work item = (sequence b, a group of NQ query rows, a range of key tiles).  The
+// contraction runs key-major: A = a tile of 128 keys x D (K-major, shared memory), B =
+// the NQ*64 (query, head) rows of q x D, so the accumulator D[key, (query, head)] sits in
+// tensor memory with one key per TMEM lane.  An epilogue thread owns one key and reduces
+// its 64 head columns in registers: ReLU, weight and head sum need no cross-thread traffic.
 //
 // The kernel is persistent.  In top-k mode a one-CTA plan kernel first reads the actual
-// context lengths, picks the key chunk (about two items per CTA, at most 16 chunks per
-// query group) and writes a longest-first work list; CTAs take items from it through an
-// atomic counter.  (Logits mode, which has no workspace, walks fixed chunks with a
-// static stride.)  Warp roles (64 + 128 * EG threads):
-//   warp 0     producer: fetches items, publishes their descriptors, loads each item's
+// context lengths and lays every query group's key tiles end to end, each group weighted
+// by its tiles plus a fixed per-item cost; CTA i takes the i-th of gridDim.x equal slices
+// of that line.  A group inside one slice is finished by one CTA; a group cut by slice
+// boundaries leaves one unsorted top-k list per slice that the merge kernel (topk.cu)
+// ranks.  (Logits mode, which has no workspace, walks fixed chunks with a static
+// stride.)  Warp roles (64 + 128 * EG threads):
+//   warp 0     producer: walks its items, publishes their descriptors, loads each item's
 //              Q tile and streams key tiles into an S-stage ring with TMA (paged keys:
 //              one box per page, block ids read from a shared-memory window the whole
 //              warp refills); it runs ahead of the other roles across item boundaries
@@ -24,8 +26,7 @@
 // Epilogue: tcgen05.ld of each query's 64 head sums, fp32 ReLU * weight head sum in a
 // fixed order, then a store of the score row (logits mode) or an insert into a per-query
 // candidate buffer in shared memory (top-k mode) that a radix select cuts back to the
-// top-k whenever it fills.  A group whose keys fit one chunk gets its sorted rows here;
-// split groups write unsorted per-chunk lists that the merge kernel (topk.cu) ranks.
+// top-k whenever it fills.  Unsplit groups get their sorted rows here.
 //
 // Every wait is bounded (see common.cuh); a timeout abandons the work, flags
 // DSA_DEVERR_TIMEOUT, waits for this CTA's own copies and MMAs, frees TMEM and returns.
@@ -51,24 +52,25 @@ struct IndexerParams {
   int64_t ld;
   int32_t* out_idx;
   float* out_val;
-  uint64_t* partial;        // [T][nl_max][topk] ranking keys of split rows
-  const int32_t* plan;      // device work list (top-k mode): chunk, item count, items
-  uint32_t* work;           // item counter of the work list
+  uint64_t* partial;        // [slice][head, tail][NQ][topk] ranking keys of split groups
+  const int32_t* plan;      // top-k mode: plan header (slice length, total, split count, item cost)
+  const int32_t* prefix;    // top-k mode: [units + 1] start of each query group on the line
+  const int32_t* ufirst;    // top-k mode: [slices] the group holding each slice's first position
+  const int32_t* order;     // top-k mode: [units] groups longest first (plan mode kPlanGroups)
+  uint32_t* work;           // top-k mode: work counter in the plan header (plan mode kPlanGroups)
   int32_t block_size;
   int32_t B, next_n, causal, max_len;
   int32_t ngroups, nchunks, chunk;  // static schedule (logits mode)
-  int32_t nl_max;           // list slots per row in `partial`
   int32_t topk, cap, pow2, stages;
 };
-
-// Layout of the device work list written by plan_kernel.
-constexpr int kPlanHeader = 4;      // int32: chunk (keys), item count, reserved x2
-constexpr int kMaxLists = 16;       // key chunks per query group at most (split rows)
 
 constexpr int kMaxPer = 10;        // candidate capacity per query <= 256 * kMaxPer
 
 struct ItemInfo {
-  int32_t valid, b, g, c, L, nreal, vis_max, ks, ntiles, t0, chunk, nl;
+  int32_t valid, b, g, L, nreal, vis_max;
+  int32_t ks, ke, ntiles;   // keys [ks, ke) in ntiles tiles of 128
+  int32_t t0, chunk;        // first query row; chunk length (logits mode: masked tail)
+  int32_t split, slot;      // top-k mode: group cut by slice boundaries; its list slot
   int32_t vis[4];
 };
 
@@ -101,14 +103,14 @@ __device__ __forceinline__ float head_sum(const float (&s)[64], const float* w) 
   return (a0 + a1) + (a2 + a3);
 }
 
-// Descriptor of work item (query group u = b * ngroups + gi, key chunk c).
+// Query group u = b * ngroups + gi: its sequence, rows and visible key counts.
 template <int NQ>
-__device__ void decode_item(const IndexerParams& p, int u, int c, int chunk, ItemInfo& it) {
+__device__ void decode_group(const IndexerParams& p, int u, ItemInfo& it) {
   const int b = u / p.ngroups;
   const int gi = u - b * p.ngroups;
   int L = __ldg(p.context_lens + b);
   if (L < 0 || L > p.max_len) {
-    if (c == 0 && gi == 0) raise_error(DSA_DEVERR_INDEX);
+    raise_error(DSA_DEVERR_INDEX);
     L = L < 0 ? 0 : p.max_len;
   }
   const int i0 = gi * NQ;
@@ -119,21 +121,61 @@ __device__ void decode_item(const IndexerParams& p, int u, int c, int chunk, Ite
     if (q < nreal) v = p.causal ? min(max(L - p.next_n + i0 + q + 1, 0), L) : L;
     it.vis[q] = v;
   }
-  const int vis_max = p.causal ? min(max(L - p.next_n + i0 + nreal, 0), L) : L;
-  const int ks = c * chunk;
-  const int ke = min(ks + chunk, vis_max);
   it.valid = 1;
   it.b = b;
   it.g = gi;
-  it.c = c;
   it.L = L;
   it.nreal = nreal;
-  it.vis_max = vis_max;
-  it.ks = ks;
-  it.ntiles = ke > ks ? (ke - ks + 127) / 128 : 0;
+  it.vis_max = p.causal ? min(max(L - p.next_n + i0 + nreal, 0), L) : L;
   it.t0 = b * p.next_n + i0;
-  it.chunk = chunk;
-  it.nl = max((vis_max + chunk - 1) / chunk, 1);
+  it.split = 0;
+  it.slot = 0;
+  it.chunk = 0;
+}
+
+// Logits mode: group u, fixed key chunk c.
+template <int NQ>
+__device__ void decode_chunk_item(const IndexerParams& p, int u, int c, ItemInfo& it) {
+  decode_group<NQ>(p, u, it);
+  const int ks = c * p.chunk;
+  const int ke = min(ks + p.chunk, it.vis_max);
+  it.ks = ks;
+  it.ke = ke > ks ? ke : ks;
+  it.ntiles = ke > ks ? (ke - ks + 127) / 128 : 0;
+  it.chunk = p.chunk;
+}
+
+// Top-k mode: the next item of slice [r0, r1) of the plan's line, walking groups from
+// *u on.  A group with line span [a0, a1) spends its first `cost` positions on its fixed
+// item cost and then has one position per key tile; a group without tiles belongs to
+// the slice that holds its position a0.  Returns false when the slice holds no more.
+template <int NQ>
+__device__ bool next_slice_item(const IndexerParams& p, int slice, int r0, int r1, int Q, int cost, int units,
+                                int* u, ItemInfo& it) {
+  while (*u < units) {
+    const int g = *u;
+    const int a0 = __ldcg(p.prefix + g), a1 = __ldcg(p.prefix + g + 1);
+    if (a0 >= r1) return false;
+    *u = g + 1;
+    const int tiles = a1 - a0 - cost;
+    if (tiles <= 0) {
+      if (a0 / Q != slice) continue;
+      decode_group<NQ>(p, g, it);
+      it.ks = it.ke = it.ntiles = 0;
+      return true;
+    }
+    const int rs = a0 + cost;
+    const int lo = max(r0, rs), hi = min(r1, a1);
+    if (lo >= hi) continue;
+    decode_group<NQ>(p, g, it);
+    it.ks = (lo - rs) * 128;
+    it.ke = min((hi - rs) * 128, it.vis_max);
+    it.ntiles = hi - lo;
+    it.split = group_is_split(a0, a1, cost, Q) ? 1 : 0;
+    it.slot = split_slot(slice, a0, cost, Q);
+    return true;
+  }
+  return false;
 }
 
 // Visible key tiles of query group u (its last real query sees the most keys).
@@ -148,148 +190,137 @@ __device__ __forceinline__ int group_tiles(const int32_t* context_lens, int u, i
   return (vis + 127) / 128;
 }
 
-// Builds the work list of the fused call from the actual context lengths: picks the key
-// chunk (a multiple of 128) so that there are about `target` items and at most nl_max
-// chunks per query group, then orders the items longest first: whole chunks, then the
-// groups' remainders by decreasing length, then groups without visible keys (they only
-// report empty rows).  Items are (u << 8) | c.  One CTA of 1024 threads.
+// Plan of the fused call.  Lays the query groups end to end on a line, group u taking
+// `cost` + (its visible key tiles) positions (prefix[u] = its start, prefix[units] = the
+// line length S), and cuts the line into `slices` equal slices of Q = ceil(S / slices)
+// positions.  When the longest group fills at most half a slice, whole groups balance
+// well enough: mode kPlanGroups, with the groups listed longest first in `order` (by
+// buckets of equal length).  Otherwise mode kPlanSlices: the group holding each slice's
+// first position goes to ufirst, the groups whose tiles fall in more than one slice to
+// `split`.  One CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ context_lens, int B, int next_n,
-                                                    int causal, int max_len, int nq, int ngroups, int target,
-                                                    int nl_max, int32_t* __restrict__ plan, uint32_t* work) {
+                                                    int causal, int max_len, int nq, int ngroups, int slices,
+                                                    int cost, int32_t* plan, int32_t* prefix, int32_t* ufirst,
+                                                    int32_t* split, int32_t* order) {
+  grid_launch_dependents();                 // the indexer's set-up may overlap this kernel
   constexpr int kBuckets = 4096;
-  __shared__ unsigned long long s_sum[32];
-  __shared__ int s_max[32];
+  __shared__ int s_warp[32];
+  __shared__ int s_carry, s_nsplit, s_max;
   __shared__ int s_hist[kBuckets];
-  __shared__ int s_scan[32];
-  __shared__ int s_misc[4];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int units = B * ngroups;
-  // 1. total and longest group, in tiles
-  unsigned long long lsum = 0;
-  int lmax = 0;
-  for (int u = tid; u < units; u += 1024) {
-    const int t = group_tiles(context_lens, u, ngroups, nq, next_n, causal, max_len);
-    lsum += (unsigned long long)t;
-    lmax = max(lmax, t);
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
-    lmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
-  }
-  if (lane == 0) {
-    s_sum[wid] = lsum;
-    s_max[wid] = lmax;
-  }
-  for (int i = tid; i < kBuckets; i += 1024) s_hist[i] = 0;
-  __syncthreads();
   if (tid == 0) {
-    unsigned long long sum = 0;
-    int mx = 0;
-    for (int w = 0; w < 32; ++w) {
-      sum += s_sum[w];
-      mx = max(mx, s_max[w]);
-    }
-    long long ct = (long long)((sum + (unsigned long long)target - 1) / (unsigned long long)target);
-    if (ct < 16) ct = 16;                                   // at least 2048 keys per chunk
-    const long long need = ((long long)mx + nl_max - 1) / nl_max;
-    if (ct < need) ct = need;
-    if (ct >= mx) ct = mx > 0 ? mx : 1;                     // no group needs splitting
-    s_misc[0] = (int)ct;
-    s_misc[1] = (int)((ct + kBuckets - 1) / kBuckets);      // tiles per ordering bucket
-    *work = 0u;
+    s_carry = 0;
+    s_nsplit = 0;
+    s_max = 0;
   }
   __syncthreads();
-  const int ct = s_misc[0];
-  const int per = s_misc[1];
-  // 2. whole chunks in group order; remainders counted per length bucket
-  int base = 0;
+  // 1. prefix sums of the group weights; longest group
+  int lmax = 0;
   for (int u0 = 0; u0 < units; u0 += 1024) {
     const int u = u0 + tid;
-    int nfull = 0;
-    if (u < units) {
-      const int t = group_tiles(context_lens, u, ngroups, nq, next_n, causal, max_len);
-      nfull = t / ct;
-      const int rem = t - nfull * ct;
-      if (rem > 0) atomicAdd(&s_hist[kBuckets - 1 - (rem - 1) / per], 1);     // longest first
-    }
-    int incl = nfull;
+    const int tiles = u < units ? group_tiles(context_lens, u, ngroups, nq, next_n, causal, max_len) : 0;
+    const int w = u < units ? tiles + cost : 0;
+    lmax = max(lmax, tiles);
+    int x = w;
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += y;
+      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
     }
-    if (lane == 31) s_scan[wid] = incl;
+    if (lane == 31) s_warp[wid] = x;
     __syncthreads();
     if (wid == 0) {
-      int v = s_scan[lane], x = v;
+      const int v = s_warp[lane];
+      int z = v;
       for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
+        const int y = __shfl_up_sync(0xFFFFFFFFu, z, o);
+        if (lane >= o) z += y;
       }
-      s_scan[lane] = x - v;                                 // exclusive
-      if (lane == 31) s_misc[2] = x;
+      s_warp[lane] = z - v;
     }
     __syncthreads();
-    const int start = base + s_scan[wid] + incl - nfull;
-    for (int c = 0; c < nfull; ++c) plan[kPlanHeader + start + c] = (u << 8) | c;
-    base += s_misc[2];
+    const int start = s_carry + s_warp[wid] + x - w;
+    if (u < units) prefix[u] = start;
+    __syncthreads();
+    if (tid == 1023) s_carry = start + w;
     __syncthreads();
   }
-  // 3. bucket offsets (exclusive scan over buckets, longest first), then remainders
-  {
-    int v[kBuckets / 1024], sum = 0;
-#pragma unroll
-    for (int i = 0; i < kBuckets / 1024; ++i) {
-      v[i] = s_hist[tid * (kBuckets / 1024) + i];
-      sum += v[i];
+  for (int o = 16; o > 0; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+  if (lane == 0) atomicMax(&s_max, lmax);
+  for (int i = tid; i < kBuckets; i += 1024) s_hist[i] = 0;
+  __syncthreads();
+  const int S = s_carry;
+  const int mx = s_max;
+  const int Q = S > 0 ? (S + slices - 1) / slices : 1;
+  const int mode = (int64_t)2 * (mx + cost) <= Q ? kPlanGroups : kPlanSlices;
+  if (tid == 0) prefix[units] = S;
+  __syncthreads();
+  if (mode == kPlanSlices) {
+    // 2. first group of every slice; split groups
+    for (int u = tid; u < units; u += 1024) {
+      const int a0 = prefix[u], a1 = prefix[u + 1];
+      for (int r = (a0 + Q - 1) / Q; r < slices && (int64_t)r * Q < a1; ++r) ufirst[r] = u;
+      if (group_is_split(a0, a1, cost, Q)) {
+        const int at = atomicAdd(&s_nsplit, 1);
+        if (at < slices) split[at] = u;
+      }
     }
-    int incl = sum;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += y;
+  } else {
+    // 2'. groups longest first: counting sort over length buckets
+    const int per = (mx + kBuckets) / kBuckets;             // tiles per bucket (>= 1)
+    for (int u = tid; u < units; u += 1024) {
+      const int tiles = prefix[u + 1] - prefix[u] - cost;
+      atomicAdd(&s_hist[kBuckets - 1 - tiles / per], 1);
     }
-    if (lane == 31) s_scan[wid] = incl;
     __syncthreads();
-    if (wid == 0) {
-      int w = s_scan[lane], x = w;
+    {
+      int v[kBuckets / 1024], sum = 0;
+#pragma unroll
+      for (int i = 0; i < kBuckets / 1024; ++i) {
+        v[i] = s_hist[tid * (kBuckets / 1024) + i];
+        sum += v[i];
+      }
+      int incl = sum;
       for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
       }
-      s_scan[lane] = x - w;
-      if (lane == 31) s_misc[3] = base + x;
+      if (lane == 31) s_warp[wid] = incl;
+      __syncthreads();
+      if (wid == 0) {
+        const int w0 = s_warp[lane];
+        int z = w0;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, z, o);
+          if (lane >= o) z += y;
+        }
+        s_warp[lane] = z - w0;
+      }
+      __syncthreads();
+      int acc = s_warp[wid] + incl - sum;
+#pragma unroll
+      for (int i = 0; i < kBuckets / 1024; ++i) {
+        s_hist[tid * (kBuckets / 1024) + i] = acc;
+        acc += v[i];
+      }
     }
     __syncthreads();
-    int acc = base + s_scan[wid] + incl - sum;
-#pragma unroll
-    for (int i = 0; i < kBuckets / 1024; ++i) {
-      s_hist[tid * (kBuckets / 1024) + i] = acc;
-      acc += v[i];
-    }
-  }
-  __syncthreads();
-  for (int u = tid; u < units; u += 1024) {
-    const int t = group_tiles(context_lens, u, ngroups, nq, next_n, causal, max_len);
-    const int nfull = t / ct;
-    const int rem = t - nfull * ct;
-    if (rem > 0) {
-      const int pos = atomicAdd(&s_hist[kBuckets - 1 - (rem - 1) / per], 1);
-      plan[kPlanHeader + pos] = (u << 8) | nfull;
-    }
-  }
-  __syncthreads();
-  // 4. groups without visible keys
-  if (tid == 0) s_misc[2] = s_misc[3];
-  __syncthreads();
-  for (int u = tid; u < units; u += 1024) {
-    if (group_tiles(context_lens, u, ngroups, nq, next_n, causal, max_len) == 0) {
-      const int pos = atomicAdd(&s_misc[2], 1);
-      plan[kPlanHeader + pos] = (u << 8);
+    for (int u = tid; u < units; u += 1024) {
+      const int tiles = prefix[u + 1] - prefix[u] - cost;
+      order[atomicAdd(&s_hist[kBuckets - 1 - tiles / per], 1)] = u;
     }
   }
   __syncthreads();
   if (tid == 0) {
-    plan[0] = ct * 128;
-    plan[1] = s_misc[2];
+    plan[0] = Q;
+    plan[1] = S;
+    plan[2] = min(s_nsplit, slices);
+    plan[3] = cost;
+    plan[4] = mode;
+    plan[5] = 0;                            // work counter (mode kPlanGroups)
+    plan[6] = 0;
+    plan[7] = 0;
+    if (s_nsplit > slices) raise_error(DSA_DEVERR_OVERFLOW | (50u << 8));
   }
 }
 
@@ -362,16 +393,26 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     // ============================ producer (whole warp) ============================
     // Lane 0 owns the barriers and issues every copy; the other lanes help load the
     // block table into a shared window so no copy waits on a dependent global load.
-    int plan_chunk = p.chunk, plan_items = p.B * p.ngroups * p.nchunks;
+    // Top-k mode: this CTA's slice [r0, r1) of the plan's line (the plan kernel may
+    // still be running: wait for it first).  Logits mode: items blockIdx.x + k * grid.
+    const int units = p.B * p.ngroups;
+    int Q = 1, cost = 0, r0 = 0, r1 = 0, ucur = units, mode = kPlanSlices;
+    int next = (int)blockIdx.x;
+    const int chunk_items = units * p.nchunks;
     if (p.plan) {
-      plan_chunk = __ldg(p.plan);
-      plan_items = __ldg(p.plan + 1);
+      grid_dependency_wait();
+      Q = __ldcg(p.plan);
+      const int S = __ldcg(p.plan + 1);
+      cost = __ldcg(p.plan + 3);
+      mode = __ldcg(p.plan + 4);
+      r0 = (int)blockIdx.x * Q;
+      r1 = min(r0 + Q, S);
+      if (mode == kPlanSlices && r0 < S) ucur = __ldcg(p.ufirst + blockIdx.x);
     }
-    int next = 0;
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      next = p.plan ? (int)atomicAdd(p.work, 1u) : (int)blockIdx.x;
+      if (p.plan && mode == kPlanGroups) next = (int)atomicAdd(p.work, 1u);   // one item ahead
     }
     int tiles_issued = 0, items_issued = 0;
     int last_issue[8];
@@ -384,20 +425,25 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         ok = mbar_wait(iempty0 + 8 * slot, ((uint32_t)(n >> 1) & 1u) ^ 1u, limit, abort_flag);
         ItemInfo it;
         it.valid = 0;
-        if (ok && next < plan_items) {
-          const int cur = next;
-          next = p.plan ? (int)atomicAdd(p.work, 1u) : next + (int)gridDim.x;
-          int u, c;
-          if (p.plan) {
-            const int code = __ldg(p.plan + kPlanHeader + cur);
-            u = code >> 8;
-            c = code & 255;
-          } else {
-            u = cur / p.nchunks;
-            c = cur - u * p.nchunks;
+        if (ok) {
+          if (p.plan && mode == kPlanSlices) {
+            have = next_slice_item<NQ>(p, (int)blockIdx.x, r0, r1, Q, cost, units, &ucur, it) ? 1 : 0;
+          } else if (p.plan) {
+            if (next < units) {
+              const int g = __ldcg(p.order + next);
+              next = (int)atomicAdd(p.work, 1u);
+              decode_group<NQ>(p, g, it);
+              it.ks = 0;
+              it.ke = it.vis_max;
+              it.ntiles = (it.vis_max + 127) / 128;
+              have = 1;
+            }
+          } else if (next < chunk_items) {
+            const int u = next / p.nchunks;
+            decode_chunk_item<NQ>(p, u, next - u * p.nchunks, it);
+            next += (int)gridDim.x;
+            have = 1;
           }
-          decode_item<NQ>(p, u, c, plan_chunk, it);
-          have = 1;
         }
         es->info[slot] = it;
       }
@@ -424,7 +470,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       // its key tiles
-      const int ke = min(it.ks + it.chunk, it.vis_max);
+      const int ke = it.ke;
       int win0 = -1;                                        // first page held in the window
       for (int i = 0; i < it.ntiles; ++i) {
         const int T = tiles_issued + i;
@@ -493,6 +539,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
       tiles_issued += it.ntiles;
     }
     if (lane == 0) {
+      grid_launch_dependents();             // every copy is issued: the merge may start launching
       if (!ok) {
         raise_error(DSA_DEVERR_TIMEOUT);
         *abort_flag = 1;
@@ -684,7 +731,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
           }
         }
         group_sync<NT>();
-        if (it.nl == 1) {
+        if (!it.split) {
           // the whole group in one item: final, sorted rows
           const int P = p.pow2;
           for (int q = 0; q < NQ; ++q) {
@@ -703,14 +750,13 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
             }
           }
         } else {
-          // this chunk's top-k of every query row, unsorted and zero-padded; the merge
-          // kernel ranks the group's lists
+          // this piece's top-k of every query row, unsorted and zero-padded, in the
+          // slice's list slot; the merge kernel ranks the group's lists
           for (int q = 0; q < it.nreal; ++q) {
-            const int64_t t = it.t0 + q;
             const int cn = (int)es->cnt[q];
             const uint64_t* buf = ebuf + (size_t)q * cap;
             for (int s = et; s < p.topk; s += NT)
-              p.partial[((size_t)t * p.nl_max + it.c) * p.topk + s] = s < cn ? buf[s] : 0ull;
+              p.partial[((size_t)it.slot * NQ + q) * p.topk + s] = s < cn ? buf[s] : 0ull;
           }
         }
       }
@@ -765,7 +811,7 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, uint64_t rows, uint32_
 
 constexpr size_t kSmemLimit = 232448;   // max dynamic shared memory per CTA (227 KB)
 constexpr size_t kSmemHalf = 115712;    // two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
-constexpr int64_t kSplitUnits = 1216;   // fewer query groups than this: rows may be split
+constexpr int64_t kSplitUnits = 1216;   // logits mode: fewer query groups than this: split key chunks
 
 size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap) {
   const size_t elt = fp8 ? 1 : 2;
@@ -835,16 +881,27 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
   pl.nchunks = (int)((qs.max_context_len + chunk - 1) / chunk);
   if (pl.nchunks < 1) pl.nchunks = 1;
   pl.items = units * pl.nchunks;
-  // top-k mode: the device plans its own chunks; workspace = [plan][work counter][partial lists]
-  pl.nl_max = units < kSplitUnits ? kMaxLists : 1;
+  // top-k mode: one slice of the plan's line per resident CTA; workspace = [plan header]
+  // [prefix: units + 1][ufirst: slices][split: slices][order: units][partial lists: 2 per slice]
+  pl.slices = device_sm_count() * pl.ctas_per_sm;
+  pl.cost = pl.nq == 4 ? 8 : 3;   // per-item cost in tile units: Q tile, drain, final ranking
   if (tk) {
-    size_t off = ((size_t)(kPlanHeader + units * pl.nl_max) * 4 + 15) / 16 * 16;
-    pl.work_off = off;
-    off += 16;
+    const int64_t max_tiles = ((int64_t)qs.max_context_len + 127) / 128;
+    if (units * (max_tiles + pl.cost) >= (int64_t)INT32_MAX) pl.ok = false;   // line positions are int32
+    size_t off = (size_t)kPlanHeader * 4;
+    pl.prefix_off = off;
+    off += (size_t)(units + 1) * 4;
+    pl.ufirst_off = off;
+    off += (size_t)pl.slices * 4;
+    pl.split_off = off;
+    off += (size_t)pl.slices * 4;
+    pl.order_off = off;
+    off += (size_t)units * 4;
+    off = (off + 15) / 16 * 16;
     pl.partial_off = off;
-    if (pl.nl_max > 1) off += (size_t)qs.B * qs.next_n * pl.nl_max * topk * 8;
+    off += (size_t)pl.slices * 2 * pl.nq * topk * 8;
     pl.ws_bytes = off;
-    pl.items = units * pl.nl_max;
+    pl.items = units;
   }
   return pl;
 }
@@ -855,8 +912,19 @@ static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, cons
   auto kern = indexer_kernel<kFP8, NQ, kTopk, EG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)grid, 64 + 128 * EG, pl.smem, st>>>(mq, mk, prm);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(64 + 128 * EG);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kTopk ? 1 : 0;   // top-k mode follows its plan kernel and may overlap it
+  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, prm);
   note_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -903,21 +971,26 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   prm.pow2 = pl.pow2;
   prm.out_idx = a.out_idx;
   prm.out_val = a.out_val;
-  prm.nl_max = pl.nl_max;
   const bool tk = a.topk > 0;
-  const int slots = device_sm_count() * pl.ctas_per_sm;
-  int64_t grid = slots;
+  int64_t grid = device_sm_count() * pl.ctas_per_sm;
   cudaError_t e;
+  int32_t* split = nullptr;
   if (tk) {
     char* ws = static_cast<char*>(a.ws);
     int32_t* plan = reinterpret_cast<int32_t*>(ws);
+    int32_t* prefix = reinterpret_cast<int32_t*>(ws + pl.prefix_off);
+    int32_t* ufirst = reinterpret_cast<int32_t*>(ws + pl.ufirst_off);
+    split = reinterpret_cast<int32_t*>(ws + pl.split_off);
+    int32_t* order = reinterpret_cast<int32_t*>(ws + pl.order_off);
     prm.plan = plan;
-    prm.work = reinterpret_cast<uint32_t*>(ws + pl.work_off);
-    prm.partial = pl.nl_max > 1 ? reinterpret_cast<uint64_t*>(ws + pl.partial_off) : nullptr;
-    const int target = pl.nl_max > 1 ? 2 * slots : 1;   // about two items per CTA when rows split
-    plan_kernel<<<1, 1024, 0, stream>>>(a.qs.context_lens, a.qs.B, a.qs.next_n, a.qs.causal,
-                                        a.qs.max_context_len, pl.nq, pl.ngroups, target, pl.nl_max, plan,
-                                        prm.work);
+    prm.prefix = prefix;
+    prm.ufirst = ufirst;
+    prm.order = order;
+    prm.work = reinterpret_cast<uint32_t*>(plan + 5);
+    prm.partial = reinterpret_cast<uint64_t*>(ws + pl.partial_off);
+    grid = pl.slices;
+    plan_kernel<<<1, 1024, 0, stream>>>(a.qs.context_lens, a.qs.B, a.qs.next_n, a.qs.causal, a.qs.max_context_len,
+                                        pl.nq, pl.ngroups, pl.slices, pl.cost, plan, prefix, ufirst, split, order);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else if (grid > pl.items) {
@@ -929,9 +1002,10 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   else
     e = tk ? dispatch_nq<false, true>(mq, mk, prm, pl, (int)grid, stream)
            : dispatch_nq<false, false>(mq, mk, prm, pl, (int)grid, stream);
-  if (e != cudaSuccess || !tk || pl.nl_max == 1) return e;
-  // rows split over several chunks: rank each group's lists
-  return launch_merge(prm.partial, pl.nl_max, prm.plan, 0, pl.nq, a.qs, a.topk, a.out_idx, a.out_val, stream);
+  if (e != cudaSuccess || !tk) return e;
+  // groups cut by slice boundaries: rank their lists
+  return launch_merge(prm.partial, prm.plan, prm.prefix, split, pl.slices, pl.nq, a.qs, a.topk, a.out_idx,
+                      a.out_val, stream);
 }
 
 DSA_DEFINE_TU_ERROR_ACCESSORS(indexer)

@@ -22,14 +22,14 @@ struct IndexerPlan {
   int chunk;         // logits mode: keys per work item (multiple of 128)
   int nchunks;       // logits mode: ceil(max_context_len / chunk)
   int ngroups;       // ceil(next_n / nq)
-  int nl_max;        // top-k mode: key chunks per query group at most (1 = rows never split)
+  int slices;        // top-k mode: CTAs, one slice of the plan's line each
+  int cost;          // top-k mode: fixed cost of one work item, in key tiles
   int cap;           // candidate-buffer capacity per query row (top-k mode)
   int pow2;          // next power of two >= topk
   size_t smem;       // dynamic shared memory per CTA
-  int64_t items;     // work items (upper bound)
+  int64_t items;     // logits mode: work items; top-k mode: query groups
   size_t ws_bytes;   // workspace bytes (top-k mode)
-  size_t work_off;   // byte offset of the work-item counter in ws
-  size_t partial_off;  // byte offset of the partial lists in ws
+  size_t prefix_off, ufirst_off, split_off, order_off, partial_off;   // byte offsets of the plan's arrays in ws
   bool ok;           // false: shape does not fit this build
 };
 
@@ -67,12 +67,13 @@ TopkPlan plan_topk(const dsa_queries& qs, int topk);
 cudaError_t launch_topk(const float* logits, int64_t ld, const dsa_queries& qs, int topk, int32_t* out_idx,
                         float* out_val, void* ws, const TopkPlan& plan, cudaStream_t stream);
 
-// Ranks the partial lists of split rows.  partial: [T][nl_max][topk] ranking keys (0 =
-// empty).  Row t belongs to a group of nq query rows whose longest visible range spans
-// nl = ceil(vis / chunk) chunks (chunk read from dev_chunk when given); rows with nl == 1
-// were finished by the producing kernel and are skipped.
-cudaError_t launch_merge(const uint64_t* partial, int nl_max, const int32_t* dev_chunk, int chunk, int nq,
-                         const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val, cudaStream_t stream);
+// Ranks the partial lists of the query groups the fused kernel split (see the work plan
+// in common.cuh): partial = [slices][2][nq][topk] ranking keys (0 = empty); plan =
+// header, prefix = group starts on the line, split = the split groups (count in the
+// header).  Launched as a programmatic dependent of the fused kernel.
+cudaError_t launch_merge(const uint64_t* partial, const int32_t* plan, const int32_t* prefix, const int32_t* split,
+                         int slices, int nq, const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val,
+                         cudaStream_t stream);
 
 // ------------------------------------------------------------------ gather (gather.cu)
 cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_t num_blocks, int bs,

@@ -111,30 +111,39 @@ __global__ void __launch_bounds__(kRowNT) topk_rows_kernel(const float* __restri
 constexpr int kMergeNT = 512;       // merge: threads per row
 constexpr int kMergeKeys = 16384;   // merge: candidates held in shared memory at once
 
-// One CTA per query row of a split group.  The row's nl lists (nl * topk candidates)
-// are loaded into shared memory, a radix select finds the top-k threshold, the survivors
-// are sorted and written.  Rows with more candidates than fit stream through two
-// half-buffers that are cut back to the top-k as they fill.
-__global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restrict__ partial, int nl_max,
-                                                         const int32_t* __restrict__ dev_chunk, int chunk, int nq,
-                                                         const int32_t* __restrict__ context_lens, int next_n,
-                                                         int causal, int max_len, int topk, int P,
+// One CTA per (split group, query row): block m handles row m % nq of the (m / nq)-th
+// split group of the plan.  The row's lists (one per slice the group's tiles fall in,
+// nl * topk candidates) are loaded into shared memory, a radix select finds the top-k
+// threshold, the survivors are sorted and written.  Rows with more candidates than fit
+// stream through two half-buffers that are cut back to the top-k as they fill.
+__global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restrict__ partial,
+                                                         const int32_t* plan, const int32_t* prefix,
+                                                         const int32_t* split, int nq, int next_n, int topk, int P,
                                                          int32_t* out_idx, float* out_val) {
   extern __shared__ uint64_t mbuf[];            // kMergeKeys candidates + P sorted slots
   __shared__ TopkShared sh;
   constexpr int NT = kMergeNT;
   const int tid = threadIdx.x;
-  const int64_t t = blockIdx.x;
-  if (dev_chunk) chunk = __ldg(dev_chunk);
-  const int b = (int)(t / next_n), i = (int)(t - (int64_t)b * next_n), gi = i / nq;
-  int L = __ldg(context_lens + b);
-  L = L < 0 ? 0 : (L > max_len ? max_len : L);
-  const int nreal = min(nq, next_n - gi * nq);
-  const int vis_max = causal ? min(max(L - next_n + gi * nq + nreal, 0), L) : L;
-  const int nl = min(max((vis_max + chunk - 1) / chunk, 1), nl_max);
-  if (nl == 1) return;                          // finished by the producing kernel
-  const uint64_t* src = partial + (size_t)t * nl_max * topk;
+  grid_dependency_wait();                       // the fused kernel's lists are complete
+  const int blk = (int)blockIdx.x;
+  const int si = blk / nq, q = blk - si * nq;
+  if (si >= __ldcg(plan + 2)) return;
+  const int Q = __ldcg(plan), cost = __ldcg(plan + 3);
+  const int g = __ldcg(split + si);
+  const int ngroups = (next_n + nq - 1) / nq;
+  const int b = g / ngroups, gi = g - b * ngroups;
+  if (gi * nq + q >= next_n) return;            // padding row of the last group
+  const int64_t t = (int64_t)b * next_n + gi * nq + q;
+  const int a0 = __ldcg(prefix + g), a1 = __ldcg(prefix + g + 1);
+  const int s0 = first_tile_slice(a0, cost, Q);
+  const int nl = last_tile_slice(a1, Q) - s0 + 1;
   const int ntot = nl * topk;
+  // candidate e: slot s of list l = e / topk
+  auto src_of = [&](int e) -> const uint64_t* {
+    const int l = e / topk;
+    const int r = s0 + l;
+    return partial + ((size_t)split_slot(r, a0, cost, Q) * nq + q) * topk + (e - l * topk);
+  };
   uint64_t* out = mbuf + kMergeKeys;
   uint64_t thr;
   if (ntot <= kMergeKeys) {
@@ -143,7 +152,7 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int e = base + u * NT + tid;
-        v[u] = e < ntot ? __ldcg(src + e) : 0ull;
+        v[u] = e < ntot ? __ldcg(src_of(e)) : 0ull;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -173,7 +182,7 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int e = base + u * NT + tid;
-        v[u] = e < ntot ? __ldcg(src + e) : 0ull;
+        v[u] = e < ntot ? __ldcg(src_of(e)) : 0ull;
       }
       group_sync<NT>();
       const uint32_t n = sh.cnt;
@@ -235,18 +244,28 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const dsa_queries& qs, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_merge(const uint64_t* partial, int nl_max, const int32_t* dev_chunk, int chunk, int nq,
-                         const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val, cudaStream_t stream) {
-  const int64_t T = (int64_t)qs.B * qs.next_n;
-  if (T <= 0) return cudaSuccess;
+cudaError_t launch_merge(const uint64_t* partial, const int32_t* plan, const int32_t* prefix, const int32_t* split,
+                         int slices, int nq, const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val,
+                         cudaStream_t stream) {
+  if ((int64_t)qs.B * qs.next_n <= 0 || slices <= 0) return cudaSuccess;
   const int P = next_pow2(topk);
   const size_t smem = (size_t)(kMergeKeys + P) * 8;
   cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  merge_kernel<<<(unsigned)T, kMergeNT, smem, stream>>>(partial, nl_max, dev_chunk, chunk, nq, qs.context_lens,
-                                                        qs.next_n, qs.causal, qs.max_context_len, topk, P, out_idx,
-                                                        out_val);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(slices * nq));    // at most slices - 1 split groups
+  cfg.blockDim = dim3(kMergeNT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, merge_kernel, partial, plan, prefix, split, nq, (int)qs.next_n, topk, P, out_idx,
+                         out_val);
   note_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -145,8 +145,9 @@ dsa_status dsa_indexer_topk(const float* logits, int64_t ld_logits, dsa_queries 
  * pass that never writes the T x max_context_len logits to memory: the scores
  * are ranked on chip as the tensor cores produce them.  Arguments as for the
  * two calls above; the result is bit-identical to running them in sequence.
- * ws: at least dsa_workspace_bytes(DSA_OP_LOGITS_TOPK, dtype, qs, topk) bytes
- * (partial top-k lists of key ranges; contents on entry do not matter).
+ * ws: at least dsa_workspace_bytes(DSA_OP_LOGITS_TOPK, dtype, qs, topk) bytes, 8-byte
+ * aligned (the work plan, 8 bytes per query group, and two partial top-k lists per
+ * CTA of the current device; contents on entry do not matter).
  */
 dsa_status dsa_indexer_logits_topk(const void* q, const float* q_scale, dsa_dtype dtype,
                                    const float* weights, int H, int D, dsa_keys keys,
@@ -190,7 +191,7 @@ dsa_status mxfp4_paged_gather(const uint8_t* kv_fp4, const uint8_t* kv_scale, in
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
  *    make that first call before any stream capture.
  *  - All calls share the one array; the call itself rewrites every part it reads
- *    (its work list, counter and per-chunk lists), so stale contents never matter.
+ *    (its work plan and partial top-k lists), so stale contents never matter.
  *    Calls whose executions overlap on the GPU (other streams, other threads) race on
  *    the array: serialise them.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
@@ -200,7 +201,9 @@ dsa_status dsa_indexer_logits_topk_noalloc(const void* q, const float* q_scale, 
                                            dsa_queries qs, int topk, int32_t* out_idx, float* out_val,
                                            void* stream);
 
-/* Workspace bytes the op needs for this batch shape (host only, no device work). */
+/* Workspace bytes the op needs for this batch shape on the current device (host only,
+ * no device work; the fused call's plan has one slice per resident CTA, so the size
+ * depends on the device's SM count). */
 size_t dsa_workspace_bytes(dsa_op op, dsa_dtype dtype, dsa_queries qs, int topk);
 
 /* Static text for a status code. */

@@ -51,13 +51,18 @@ def _qs(B=1, n=1, L=4096, causal=True):
 
 
 def test_workspace_plans_are_host_only(lib):
-    # decode-shaped batches split each row's keys and need partial lists
+    ws = lambda qs, k: dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, qs, k)
+    # the fused call's workspace: the plan (8 B per query group) plus two partial top-k
+    # lists per CTA (one CTA per slice of the work, at least one per SM)
     flash = dsa.make_queries(64, 1, 0x1000, 65536, True)
-    n = dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, flash, 512)
-    assert n >= 64 * 512 * 8 * 2
-    # a prefill-sized batch never splits rows: only the device work list (4 B per group)
+    n = ws(flash, 512)
+    assert n >= 148 * 2 * 512 * 8
+    assert ws(dsa.make_queries(128, 1, 0x1000, 65536, True), 512) - n == 64 * 8
+    # the partial lists grow linearly with k, whatever the batch
     prefill = dsa.make_queries(1, 16384, 0x1000, 16384, True)
-    assert 0 < dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, prefill, 512) < 64 * 1024
+    for qs in (flash, prefill):
+        assert ws(qs, 1024) - ws(qs, 512) == 2 * (ws(qs, 512) - ws(qs, 256)) > 0
+    assert ws(prefill, 512) > 4096 * 4
     # the standalone top-k needs no workspace at any shape
     assert dsa.dsa_workspace_bytes(dsa.DSA_OP_TOPK, dsa.DSA_BF16, prefill, 512) == 0
     assert dsa.dsa_workspace_bytes(dsa.DSA_OP_TOPK, dsa.DSA_BF16, flash, 512) == 0

@@ -45,9 +45,9 @@ def test_noalloc_matches_workspace_call_twice():
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch():
-    # 256 single-query sequences of up to 1M keys at k = 2048 need far more than 16 MiB
+    # four query rows per sequence at k = 2048: the partial top-k lists alone need ~20 MB
     lens = torch.full((256,), 1 << 20, dtype=torch.int32, device="cuda")
-    qs = dsa.make_queries(256, 1, lens, 1 << 20, True)
+    qs = dsa.make_queries(256, 4, lens, 1 << 20, True)
     assert dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, qs, 2048) > 16 << 20
     keys = dsa.dsa_keys(0x100000, None, 0x100000, 1 << 14, 64, 1 << 20)
     before = dsa.dsa_launch_count()
