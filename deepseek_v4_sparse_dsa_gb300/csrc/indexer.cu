@@ -52,7 +52,8 @@ struct IndexerParams {
   int64_t ld;
   int32_t* out_idx;
   float* out_val;
-  uint64_t* partial;        // [slice][head, tail][NQ][topk] ranking keys of split groups
+  uint64_t* partial;        // [slice][head, tail][NQ][cap] candidate keys of split groups' pieces
+  uint64_t* partial_meta;   // [slice][head, tail][NQ][2]: candidate count, piece threshold
   const int32_t* plan;      // top-k mode: plan header (slice length, total, split count, item cost)
   const int32_t* prefix;    // top-k mode: [units + 1] start of each query group on the line
   const int32_t* ufirst;    // top-k mode: [slices] the group holding each slice's first position
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
   uint8_t* q_s = smem;
   uint8_t* k_s = smem + Q_BYTES;                         // S stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(k_s + (size_t)S * K_BYTES);
-  // full[S] | empty[S] | tfull[2] | tempty[2] | qfull | qempty | ifull[2] | iempty[2] | mmadone | pad
+  // full[S] | empty[S] | tfull[2] | tempty[2] | qfull | qempty | ifull[2] | iempty[2] | mmadone | tmemfree
   EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 12);
   uint64_t* ebuf = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(es) + sizeof(EpiSmem<NQ>) + 15) & ~uintptr_t(15));
@@ -356,6 +357,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
   const uint32_t qfull = smem_u32(bars + 2 * S + 4), qempty = smem_u32(bars + 2 * S + 5);
   const uint32_t ifull0 = smem_u32(bars + 2 * S + 6), iempty0 = smem_u32(bars + 2 * S + 8);
   const uint32_t mmadone = smem_u32(bars + 2 * S + 10);
+  const uint32_t tmemfree = smem_u32(bars + 2 * S + 11);   // every epilogue warp is done with TMEM
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     mbar_init(qfull, 1);
     mbar_init(qempty, 1);
     mbar_init(mmadone, 1);
+    mbar_init(tmemfree, 4 * EG);
     es->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -591,10 +594,15 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         raise_error(DSA_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
-      // Every MMA issued so far must finish before TMEM is released.
+      // Every MMA issued so far must finish, and every epilogue warp must be done
+      // reading, before TMEM is released.
       mma_commit(mmadone);
       mbar_wait(mmadone, 0, kCleanupWaitNs, nullptr);
+      mbar_wait(tmemfree, 0, kCleanupWaitNs, nullptr);
     }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
   } else {
     // ============================ epilogue ============================
     const int et = threadIdx.x - 64;            // 0..NT-1
@@ -639,6 +647,15 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
       const float* wq = &es->w[slot][0][0];
       const int niter = (it.ntiles + EG - 1) / EG;
       const int first = ((grp - T0) % EG + EG) % EG;   // this group's first local tile
+      // Block id of this thread's key in local tile i (-1: past the row or the table).
+      // Read one tile ahead so the load overlaps the wait for the accumulator.
+      auto page_of = [&](int i) -> int64_t {
+        const int jj = it.ks + i * 128 + row;
+        const int64_t pg = jj / bs;
+        return (jj < it.L && pg < p.bt_stride) ? (int64_t)__ldg(p.block_table + (int64_t)it.b * p.bt_stride + pg)
+                                               : (int64_t)-1;
+      };
+      int64_t blk_next = (paged && first < it.ntiles) ? page_of(first) : -1;
       for (int m = 0; m < niter; ++m) {
         if (kTopk) {
           group_sync<NT>();
@@ -662,9 +679,8 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         bool valid = true;
         float kscale = 1.f;
         if (paged) {
-          const int64_t pg = j / bs;
-          int64_t blk = -1;
-          if (j < it.L && pg < p.bt_stride) blk = __ldg(p.block_table + (int64_t)it.b * p.bt_stride + pg);
+          const int64_t blk = blk_next;
+          if (i + EG < it.ntiles) blk_next = page_of(i + EG);
           valid = blk >= 0 && blk < p.num_blocks;
           if (kFP8 && valid) kscale = __ldg(p.k_scale + blk * bs + (j % bs));
         } else {
@@ -719,7 +735,8 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         const int f1 = min(it.ks + it.chunk, p.max_len);
         for (int q = 0; q < it.nreal; ++q)
           for (int jj = f0 + et; jj < f1; jj += NT) p.logits[(int64_t)(it.t0 + q) * p.ld + jj] = -INFINITY;
-      } else {
+      } else if (!it.split) {
+        // the whole group in one item: cut back to the top-k, sort, final rows
         group_sync<NT>();
 #pragma unroll 1
         for (int q = 0; q < NQ; ++q) {
@@ -731,32 +748,35 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
           }
         }
         group_sync<NT>();
-        if (!it.split) {
-          // the whole group in one item: final, sorted rows
-          const int P = p.pow2;
-          for (int q = 0; q < NQ; ++q) {
-            const int cn = (int)es->cnt[q];
-            for (int e = cn + et; e < P; e += NT) ebuf[(size_t)q * cap + e] = 0ull;
+        const int P = p.pow2;
+        for (int q = 0; q < NQ; ++q) {
+          const int cn = (int)es->cnt[q];
+          for (int e = cn + et; e < P; e += NT) ebuf[(size_t)q * cap + e] = 0ull;
+        }
+        group_sync<NT>();
+        engine_sort<NT>(ebuf, cap, NQ, P, et);
+        for (int q = 0; q < it.nreal; ++q) {
+          const int64_t t = it.t0 + q;
+          const uint64_t* buf = ebuf + (size_t)q * cap;
+          for (int s = et; s < p.topk; s += NT) {
+            const uint64_t key = buf[s];
+            p.out_idx[t * p.topk + s] = key ? index_of_key(key) : -1;
+            if (p.out_val) p.out_val[t * p.topk + s] = key ? value_of_key(key) : -INFINITY;
           }
-          group_sync<NT>();
-          engine_sort<NT>(ebuf, cap, NQ, P, et);
-          for (int q = 0; q < it.nreal; ++q) {
-            const int64_t t = it.t0 + q;
-            const uint64_t* buf = ebuf + (size_t)q * cap;
-            for (int s = et; s < p.topk; s += NT) {
-              const uint64_t key = buf[s];
-              p.out_idx[t * p.topk + s] = key ? index_of_key(key) : -1;
-              if (p.out_val) p.out_val[t * p.topk + s] = key ? value_of_key(key) : -INFINITY;
-            }
-          }
-        } else {
-          // this piece's top-k of every query row, unsorted and zero-padded, in the
-          // slice's list slot; the merge kernel ranks the group's lists
-          for (int q = 0; q < it.nreal; ++q) {
-            const int cn = (int)es->cnt[q];
-            const uint64_t* buf = ebuf + (size_t)q * cap;
-            for (int s = et; s < p.topk; s += NT)
-              p.partial[((size_t)it.slot * NQ + q) * p.topk + s] = s < cn ? buf[s] : 0ull;
+        }
+      } else {
+        // a piece of a split group: its candidates as they stand (unsorted, at least
+        // its top-k) with their count and the piece's threshold, in the slice's list
+        // slot; the merge kernel ranks the group's lists
+        group_sync<NT>();
+        for (int q = 0; q < it.nreal; ++q) {
+          const int cn = (int)es->cnt[q];
+          const size_t l = (size_t)it.slot * NQ + q;
+          const uint64_t* buf = ebuf + (size_t)q * cap;
+          for (int s = et; s < cn; s += NT) p.partial[l * cap + s] = buf[s];
+          if (et == 0) {
+            p.partial_meta[2 * l] = (uint64_t)cn;
+            p.partial_meta[2 * l + 1] = es->thr[q];
           }
         }
       }
@@ -764,14 +784,13 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
       group_sync<NT>();
       if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
     }
+    // this warp's TMEM reads are complete
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tmemfree);
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
-  }
+  // No CTA-wide barrier here: the warps leave as their roles end (warp 1 last frees
+  // TMEM); shared memory stays valid until every thread of the CTA has exited.
 }
 
 // =====================================================================================
@@ -882,7 +901,8 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
   if (pl.nchunks < 1) pl.nchunks = 1;
   pl.items = units * pl.nchunks;
   // top-k mode: one slice of the plan's line per resident CTA; workspace = [plan header]
-  // [prefix: units + 1][ufirst: slices][split: slices][order: units][partial lists: 2 per slice]
+  // [prefix: units + 1][ufirst: slices][split: slices][order: units]
+  // [partial lists: 2 per slice, cap keys per query row][their counts and thresholds]
   pl.slices = device_sm_count() * pl.ctas_per_sm;
   pl.cost = pl.nq == 4 ? 8 : 3;   // per-item cost in tile units: Q tile, drain, final ranking
   if (tk) {
@@ -899,7 +919,9 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
     off += (size_t)units * 4;
     off = (off + 15) / 16 * 16;
     pl.partial_off = off;
-    off += (size_t)pl.slices * 2 * pl.nq * topk * 8;
+    off += (size_t)pl.slices * 2 * pl.nq * pl.cap * 8;
+    pl.meta_off = off;
+    off += (size_t)pl.slices * 2 * pl.nq * 16;
     pl.ws_bytes = off;
     pl.items = units;
   }
@@ -988,6 +1010,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
     prm.order = order;
     prm.work = reinterpret_cast<uint32_t*>(plan + 5);
     prm.partial = reinterpret_cast<uint64_t*>(ws + pl.partial_off);
+    prm.partial_meta = reinterpret_cast<uint64_t*>(ws + pl.meta_off);
     grid = pl.slices;
     plan_kernel<<<1, 1024, 0, stream>>>(a.qs.context_lens, a.qs.B, a.qs.next_n, a.qs.causal, a.qs.max_context_len,
                                         pl.nq, pl.ngroups, pl.slices, pl.cost, plan, prefix, ufirst, split, order);
@@ -1004,8 +1027,8 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
            : dispatch_nq<false, false>(mq, mk, prm, pl, (int)grid, stream);
   if (e != cudaSuccess || !tk) return e;
   // groups cut by slice boundaries: rank their lists
-  return launch_merge(prm.partial, prm.plan, prm.prefix, split, pl.slices, pl.nq, a.qs, a.topk, a.out_idx,
-                      a.out_val, stream);
+  return launch_merge(prm.partial, prm.partial_meta, pl.cap, prm.plan, prm.prefix, split, pl.slices, pl.nq, a.qs,
+                      a.topk, a.out_idx, a.out_val, stream);
 }
 
 DSA_DEFINE_TU_ERROR_ACCESSORS(indexer)

@@ -29,7 +29,7 @@ struct IndexerPlan {
   size_t smem;       // dynamic shared memory per CTA
   int64_t items;     // logits mode: work items; top-k mode: query groups
   size_t ws_bytes;   // workspace bytes (top-k mode)
-  size_t prefix_off, ufirst_off, split_off, order_off, partial_off;   // byte offsets of the plan's arrays in ws
+  size_t prefix_off, ufirst_off, split_off, order_off, partial_off, meta_off;   // byte offsets in ws
   bool ok;           // false: shape does not fit this build
 };
 
@@ -68,12 +68,13 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const dsa_queries& qs, 
                         float* out_val, void* ws, const TopkPlan& plan, cudaStream_t stream);
 
 // Ranks the partial lists of the query groups the fused kernel split (see the work plan
-// in common.cuh): partial = [slices][2][nq][topk] ranking keys (0 = empty); plan =
-// header, prefix = group starts on the line, split = the split groups (count in the
-// header).  Launched as a programmatic dependent of the fused kernel.
-cudaError_t launch_merge(const uint64_t* partial, const int32_t* plan, const int32_t* prefix, const int32_t* split,
-                         int slices, int nq, const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val,
-                         cudaStream_t stream);
+// in common.cuh): partial = [slices][2][nq][lcap] candidate keys, meta = [slices][2][nq]
+// x (count, threshold); plan = header, prefix = group starts on the line, split = the
+// split groups (count in the header).  Launched as a programmatic dependent of the
+// fused kernel.
+cudaError_t launch_merge(const uint64_t* partial, const uint64_t* meta, int lcap, const int32_t* plan,
+                         const int32_t* prefix, const int32_t* split, int slices, int nq, const dsa_queries& qs,
+                         int topk, int32_t* out_idx, float* out_val, cudaStream_t stream);
 
 // ------------------------------------------------------------------ gather (gather.cu)
 cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_t num_blocks, int bs,

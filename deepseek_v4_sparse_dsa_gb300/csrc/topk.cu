@@ -112,18 +112,24 @@ constexpr int kMergeNT = 512;       // merge: threads per row
 constexpr int kMergeKeys = 16384;   // merge: candidates held in shared memory at once
 
 // One CTA per (split group, query row): block m handles row m % nq of the (m / nq)-th
-// split group of the plan.  The row's lists (one per slice the group's tiles fall in,
-// nl * topk candidates) are loaded into shared memory, a radix select finds the top-k
-// threshold, the survivors are sorted and written.  Rows with more candidates than fit
-// stream through two half-buffers that are cut back to the top-k as they fill.
+// split group of the plan.  The row's lists (one per slice the group's tiles fall in)
+// hold each piece's candidates -- a superset of its top-k -- and the piece's threshold
+// (its k-th best key at its last cut-back, or 0).  The largest of those thresholds is a
+// lower bound of the row's k-th best key: only keys at or above it are loaded.  They
+// collect in one half of the shared buffer, which is cut back to the top-k whenever it
+// fills; a last radix select leaves exactly the row's top-k, each of which is written at
+// its rank (the number of selected keys above it).
 __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restrict__ partial,
+                                                         const uint64_t* __restrict__ meta, int lcap,
                                                          const int32_t* plan, const int32_t* prefix,
                                                          const int32_t* split, int nq, int next_n, int topk, int P,
                                                          int32_t* out_idx, float* out_val) {
-  extern __shared__ uint64_t mbuf[];            // kMergeKeys candidates + P sorted slots
+  extern __shared__ uint64_t mbuf[];            // kMergeKeys candidates + P selected
   __shared__ TopkShared sh;
+  __shared__ uint64_t s_floor[kMergeNT / 32];
   constexpr int NT = kMergeNT;
-  const int tid = threadIdx.x;
+  constexpr int kHalf = kMergeKeys / 2;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   grid_dependency_wait();                       // the fused kernel's lists are complete
   const int blk = (int)blockIdx.x;
   const int si = blk / nq, q = blk - si * nq;
@@ -137,52 +143,31 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
   const int a0 = __ldcg(prefix + g), a1 = __ldcg(prefix + g + 1);
   const int s0 = first_tile_slice(a0, cost, Q);
   const int nl = last_tile_slice(a1, Q) - s0 + 1;
-  const int ntot = nl * topk;
-  // candidate e: slot s of list l = e / topk
-  auto src_of = [&](int e) -> const uint64_t* {
-    const int l = e / topk;
-    const int r = s0 + l;
-    return partial + ((size_t)split_slot(r, a0, cost, Q) * nq + q) * topk + (e - l * topk);
-  };
-  uint64_t* out = mbuf + kMergeKeys;
-  uint64_t thr;
-  if (ntot <= kMergeKeys) {
-    for (int base = 0; base < ntot; base += 8 * NT) {
-      uint64_t v[8];
+  auto list_of = [&](int l) -> size_t { return (size_t)split_slot(s0 + l, a0, cost, Q) * nq + q; };
+  // 1. the floor: the largest piece threshold
+  uint64_t fl = 0;
+  for (int l = tid; l < nl; l += NT) fl = max(fl, __ldcg(meta + 2 * list_of(l) + 1));
+  for (int o = 16; o > 0; o >>= 1) fl = max(fl, __shfl_xor_sync(0xFFFFFFFFu, fl, o));
+  if (lane == 0) s_floor[wid] = fl;
+  if (tid == 0) sh.cnt = 0;
+  group_sync<NT>();
+  fl = 0;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int e = base + u * NT + tid;
-        v[u] = e < ntot ? __ldcg(src_of(e)) : 0ull;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int e = base + u * NT + tid;
-        if (e < ntot) mbuf[e] = v[u];
-      }
-    }
-    group_sync<NT>();
-    thr = engine_select<NT>(mbuf, ntot, topk, &sh.esc, tid);
-    if (tid == 0) sh.cnt = 0;
-    group_sync<NT>();
-    for (int base = 0; base < ntot; base += NT) {
-      const int e = base + tid;
-      const uint64_t key = e < ntot ? mbuf[e] : 0ull;
-      engine_append(out, &sh.cnt, key, key != 0ull && key >= thr, (uint32_t)P, 30u);
-    }
-  } else {
-    constexpr int kHalf = kMergeKeys / 2;
-    uint64_t* cur = mbuf;
-    uint64_t* alt = mbuf + kHalf;
-    if (tid == 0) {
-      sh.cnt = 0;
-      sh.thr = 0;
-    }
-    for (int base = 0; base < ntot; base += 4 * NT) {
+  for (int w = 0; w < NT / 32; ++w) fl = max(fl, s_floor[w]);
+  if (tid == 0) sh.thr = fl;
+  // 2. collect the keys at or above the running threshold, cutting back when full
+  uint64_t* cur = mbuf;
+  uint64_t* alt = mbuf + kHalf;
+  for (int l = 0; l < nl; ++l) {
+    const size_t li = list_of(l);
+    const int cnt = (int)min((uint64_t)lcap, __ldcg(meta + 2 * li));
+    const uint64_t* src = partial + li * lcap;
+    for (int base = 0; base < cnt; base += 4 * NT) {
       uint64_t v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int e = base + u * NT + tid;
-        v[u] = e < ntot ? __ldcg(src_of(e)) : 0ull;
+        v[u] = e < cnt ? __ldcg(src + e) : 0ull;
       }
       group_sync<NT>();
       const uint32_t n = sh.cnt;
@@ -192,7 +177,7 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
         uint64_t* tmp = cur;
         cur = alt;
         alt = tmp;
-        if (tid == 0) sh.thr = th;
+        if (tid == 0 && th > sh.thr) sh.thr = th;
         group_sync<NT>();
       }
       const uint64_t th = sh.thr;
@@ -200,26 +185,39 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
       for (int u = 0; u < 4; ++u)
         engine_append(cur, &sh.cnt, v[u], v[u] != 0ull && v[u] >= th, (uint32_t)kHalf, 31u);
     }
-    group_sync<NT>();
-    const uint32_t n = sh.cnt;
-    thr = engine_select<NT>(cur, (int)n, topk, &sh.esc, tid);
-    if (tid == 0) sh.cnt = 0;
-    group_sync<NT>();
-    for (int base = 0; base < (int)n; base += NT) {
-      const int e = base + tid;
-      const uint64_t key = e < (int)n ? cur[e] : 0ull;
-      engine_append(out, &sh.cnt, key, key != 0ull && key >= thr, (uint32_t)P, 32u);
-    }
   }
   group_sync<NT>();
-  const int m = (int)sh.cnt;
-  for (int e = m + tid; e < P; e += NT) out[e] = 0ull;
+  // 3. exactly the top-k (or every candidate when there are fewer)
+  const uint32_t n = sh.cnt;
+  const uint64_t thr = engine_select<NT>(cur, (int)n, topk, &sh.esc, tid);
+  uint64_t* out = mbuf + kMergeKeys;
+  if (tid == 0) sh.cnt = 0;
   group_sync<NT>();
-  engine_sort<NT>(out, P, 1, P, tid);
-  for (int s = tid; s < topk; s += NT) {
-    const uint64_t key = out[s];
-    out_idx[t * topk + s] = key ? index_of_key(key) : -1;
-    if (out_val) out_val[t * topk + s] = key ? value_of_key(key) : -INFINITY;
+  for (int base = 0; base < (int)n; base += NT) {
+    const int e = base + tid;
+    const uint64_t key = e < (int)n ? cur[e] : 0ull;
+    engine_append(out, &sh.cnt, key, key != 0ull && key >= thr, (uint32_t)P, 32u);
+  }
+  group_sync<NT>();
+  const int m = min((int)sh.cnt, P);
+  if (tid == 0 && (m & 1)) out[m] = 0ull;      // pairs below: a zero key ranks below all
+  group_sync<NT>();
+  // 4. each selected key goes to its rank; the rest of the row is padding
+  const ulonglong2* out2 = reinterpret_cast<const ulonglong2*>(out);
+  const int pairs = (m + 1) >> 1;
+  for (int e = tid; e < m; e += NT) {
+    const uint64_t key = out[e];
+    int r = 0;
+    for (int f = 0; f < pairs; ++f) {
+      const ulonglong2 x = out2[f];
+      r += (x.x > key) + (x.y > key);
+    }
+    out_idx[t * topk + r] = index_of_key(key);
+    if (out_val) out_val[t * topk + r] = value_of_key(key);
+  }
+  for (int s = m + tid; s < topk; s += NT) {
+    out_idx[t * topk + s] = -1;
+    if (out_val) out_val[t * topk + s] = -INFINITY;
   }
 }
 
@@ -244,12 +242,12 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const dsa_queries& qs, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_merge(const uint64_t* partial, const int32_t* plan, const int32_t* prefix, const int32_t* split,
-                         int slices, int nq, const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val,
-                         cudaStream_t stream) {
+cudaError_t launch_merge(const uint64_t* partial, const uint64_t* meta, int lcap, const int32_t* plan,
+                         const int32_t* prefix, const int32_t* split, int slices, int nq, const dsa_queries& qs,
+                         int topk, int32_t* out_idx, float* out_val, cudaStream_t stream) {
   if ((int64_t)qs.B * qs.next_n <= 0 || slices <= 0) return cudaSuccess;
   const int P = next_pow2(topk);
-  const size_t smem = (size_t)(kMergeKeys + P) * 8;
+  const size_t smem = (size_t)(kMergeKeys + P + 2) * 8;
   cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -262,8 +260,8 @@ cudaError_t launch_merge(const uint64_t* partial, const int32_t* plan, const int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, merge_kernel, partial, plan, prefix, split, nq, (int)qs.next_n, topk, P, out_idx,
-                         out_val);
+  e = cudaLaunchKernelEx(&cfg, merge_kernel, partial, meta, lcap, plan, prefix, split, nq, (int)qs.next_n, topk, P,
+                         out_idx, out_val);
   note_launch();
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
