@@ -419,6 +419,113 @@ __device__ uint64_t engine_select_global(const uint64_t* src, int n, int k, Engi
   return prefix;
 }
 
+// Cheap cut-back of a candidate buffer that only has to stay a superset of its top-k:
+// finds a threshold T with at least k of the nonzero keys of buf[0, n) at or above it
+// from one 512-bin histogram of the keys' values (bins linear in the order-preserving
+// image of the value, between its smallest and largest), keeps the keys >= T packed to
+// the front (*cnt = their number) and returns T.  Returns 0 and leaves buf alone when
+// the histogram cannot bring the count to `room` or less (values too concentrated, e.g.
+// ties) or there are at most k keys; the caller then selects exactly.  `bins` holds 512
+// words of shared scratch; needs n <= NT * MAXPER.
+constexpr int kCutBins = 512;
+
+template <int NT, int MAXPER>
+__device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k, uint32_t room, uint32_t* bins,
+                                      EngineScratch* sc, int tid) {
+  constexpr int NW = NT / 32;
+  constexpr int BPT = kCutBins / NT;               // bins per thread in the scan
+  static_assert(kCutBins % NT == 0 && NW <= 16, "group size");
+  const int lane = tid & 31, w = tid >> 5;
+  uint64_t keep[MAXPER];
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u, nz = 0u;
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i) {
+    const int e = tid + i * NT;
+    keep[i] = (e < n) ? buf[e] : 0ull;
+    if (keep[i]) {
+      const uint32_t o = (uint32_t)(keep[i] >> 32);
+      lo = min(lo, o);
+      hi = max(hi, o);
+      ++nz;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+    nz += __shfl_xor_sync(0xFFFFFFFFu, nz, o);
+  }
+  uint32_t* wred = sc->hist;                        // [0, 3 * NW): per-warp lo, hi, count
+  if (lane == 0) {
+    wred[w] = lo;
+    wred[NW + w] = hi;
+    wred[2 * NW + w] = nz;
+  }
+  for (int i = tid; i < kCutBins; i += NT) bins[i] = 0u;
+  group_sync<NT>();
+  lo = 0xFFFFFFFFu;
+  hi = 0u;
+  nz = 0u;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    lo = min(lo, wred[i]);
+    hi = max(hi, wred[NW + i]);
+    nz += wred[2 * NW + i];
+  }
+  if (nz <= (uint32_t)k || hi == lo) {
+    group_sync<NT>();                               // wred is read before it is reused
+    return 0ull;
+  }
+  const uint64_t span = (uint64_t)(hi - lo) + 1u;
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i)
+    if (keep[i]) atomicAdd(&bins[(uint32_t)(((uint64_t)((uint32_t)(keep[i] >> 32) - lo) * kCutBins) / span)], 1u);
+  group_sync<NT>();
+  // bin b* holding the k-th key from the top: thread tid scans bins
+  // [kCutBins - (tid + 1) * BPT, kCutBins - tid * BPT) top down
+  uint32_t c[BPT], sum = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    c[i] = bins[kCutBins - 1 - tid * BPT - i];
+    sum += c[i];
+  }
+  uint32_t incl = sum;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t* wsum = sc->hist + 3 * NW;               // [3 * NW, 4 * NW): per-warp totals
+  if (lane == 31) wsum[w] = incl;
+  group_sync<NT>();
+  uint32_t before = 0;
+  for (int i = 0; i < w; ++i) before += wsum[i];
+  uint32_t above = before + incl - sum;
+  if (above < (uint32_t)k && (uint32_t)k <= above + sum) {
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      if (above < (uint32_t)k && (uint32_t)k <= above + c[i]) {
+        sc->pick[0] = (uint32_t)(kCutBins - 1 - tid * BPT - i);
+        sc->pick[1] = above + c[i];
+      }
+      above += c[i];
+    }
+  }
+  group_sync<NT>();
+  const uint32_t b = sc->pick[0], count = sc->pick[1];
+  if (count > room) {
+    group_sync<NT>();
+    return 0ull;
+  }
+  // smallest value image in bins >= b
+  const uint32_t tord = lo + (uint32_t)(((uint64_t)b * span + kCutBins - 1) / kCutBins);
+  if (tid == 0) *cnt = 0;
+  group_sync<NT>();
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i)
+    engine_append(buf, cnt, keep[i], keep[i] != 0ull && (uint32_t)(keep[i] >> 32) >= tord, (uint32_t)(NT * MAXPER), 3u);
+  group_sync<NT>();
+  return (uint64_t)tord << 32;
+}
+
 // Keeps the keys >= thr of buf[0, n), packed to the front; *cnt becomes their
 // number.  Holds the keys in registers meanwhile: needs n <= NT * MAXPER.
 template <int NT, int MAXPER>

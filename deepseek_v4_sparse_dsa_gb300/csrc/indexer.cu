@@ -21,7 +21,7 @@
 //              one box per page, block ids read from a shared-memory window the whole
 //              warp refills); it runs ahead of the other roles across item boundaries
 //   warp 1     TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 2..  EG epilogue groups of 4 warps; global tile T uses TMEM buffer T & 1 and
+//   warps 2..  EG epilogue groups of 4 warps; global tile T uses TMEM buffer T % NB and
 //              epilogue group T % EG
 // Epilogue: tcgen05.ld of each query's 64 head sums, fp32 ReLU * weight head sum in a
 // fixed order, then a store of the score row (logits mode) or an insert into a per-query
@@ -63,6 +63,7 @@ struct IndexerParams {
   int32_t B, next_n, causal, max_len;
   int32_t ngroups, nchunks, chunk;  // static schedule (logits mode)
   int32_t topk, cap, pow2, stages;
+  int32_t nbuf_log2;        // log2 of the TMEM accumulator buffers (1 or 2)
 };
 
 constexpr int kMaxPer = 10;        // candidate capacity per query <= 256 * kMaxPer
@@ -89,6 +90,7 @@ struct EpiSmem {
   uint32_t cnt[4];
   uint64_t thr[4];
   EngineScratch esc;
+  uint32_t bins[kCutBins];
 };
 
 __device__ __forceinline__ float head_sum(const float (&s)[64], const float* w) {
@@ -338,7 +340,9 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
   constexpr uint32_t K_CHUNK = 128 * 128;          // 128 keys x 128 bytes
   constexpr uint32_t K_BYTES = K_CHUNK * KCH;
   constexpr int KSTEPS = KCH * 4;                  // 32 bytes of K per MMA
-  constexpr uint32_t TMEM_COLS = (2 * N < 32) ? 32 : (uint32_t)next_pow2(2 * N);
+  const int NBL = p.nbuf_log2;                     // NB = 2^NBL accumulator buffers in TMEM
+  const int NBM = (1 << NBL) - 1;
+  const uint32_t TMEM_COLS = ((N << NBL) < 32) ? 32u : (uint32_t)next_pow2(N << NBL);
   constexpr uint32_t IDESC = kFP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N);
 
   extern __shared__ uint8_t smem_raw[];
@@ -347,17 +351,17 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
   uint8_t* q_s = smem;
   uint8_t* k_s = smem + Q_BYTES;                         // S stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(k_s + (size_t)S * K_BYTES);
-  // full[S] | empty[S] | tfull[2] | tempty[2] | qfull | qempty | ifull[2] | iempty[2] | mmadone | tmemfree
-  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 12);
+  // full[S] | empty[S] | tfull[4] | tempty[4] | qfull | qempty | ifull[2] | iempty[2] | mmadone | tmemfree
+  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 16);
   uint64_t* ebuf = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(es) + sizeof(EpiSmem<NQ>) + 15) & ~uintptr_t(15));
 
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
-  const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
-  const uint32_t qfull = smem_u32(bars + 2 * S + 4), qempty = smem_u32(bars + 2 * S + 5);
-  const uint32_t ifull0 = smem_u32(bars + 2 * S + 6), iempty0 = smem_u32(bars + 2 * S + 8);
-  const uint32_t mmadone = smem_u32(bars + 2 * S + 10);
-  const uint32_t tmemfree = smem_u32(bars + 2 * S + 11);   // every epilogue warp is done with TMEM
+  const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 4);
+  const uint32_t qfull = smem_u32(bars + 2 * S + 8), qempty = smem_u32(bars + 2 * S + 9);
+  const uint32_t ifull0 = smem_u32(bars + 2 * S + 10), iempty0 = smem_u32(bars + 2 * S + 12);
+  const uint32_t mmadone = smem_u32(bars + 2 * S + 14);
+  const uint32_t tmemfree = smem_u32(bars + 2 * S + 15);   // every epilogue warp is done with TMEM
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -372,9 +376,11 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < 4; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
       mbar_init(tempty0 + 8 * a, 4);
+    }
+    for (int a = 0; a < 2; ++a) {
       mbar_init(ifull0 + 8 * a, 1);
       mbar_init(iempty0 + 8 * a, 1 + 4 * EG);
     }
@@ -566,9 +572,9 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         const uint32_t qbase = smem_u32(q_s);
         for (int i = 0; i < it.ntiles; ++i, ++T) {
           const int s = T % S;
-          const int a = T & 1;
+          const int a = T & NBM;
           ok = mbar_wait(full0 + 8 * s, (uint32_t)(T / S) & 1u, limit, abort_flag) &&
-               mbar_wait(tempty0 + 8 * a, ((uint32_t)(T >> 1) & 1u) ^ 1u, limit, abort_flag);
+               mbar_wait(tempty0 + 8 * a, ((uint32_t)(T >> NBL) & 1u) ^ 1u, limit, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint32_t stage = smem_u32(k_s + (size_t)s * K_BYTES);
@@ -663,10 +669,17 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
           for (int q = 0; q < NQ; ++q) {
             const uint32_t cn = es->cnt[q];
             if (cn > (uint32_t)(cap - 128 * EG)) {
+              // cut back to a superset of the top-k; exactly only if the histogram
+              // cannot free enough room
               uint64_t* buf = ebuf + (size_t)q * cap;
-              const uint64_t thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
-              engine_compact<NT, kMaxPer * 2 / EG>(buf, &es->cnt[q], (int)cn, thr, et);
-              if (et == 0) es->thr[q] = thr;
+              const uint32_t room = (uint32_t)min((cap + p.topk) / 2, cap - 256 * EG);
+              uint64_t thr = engine_cut_approx<NT, kMaxPer * 2 / EG>(buf, &es->cnt[q], (int)cn, p.topk, room,
+                                                                     es->bins, &es->esc, et);
+              if (thr == 0ull) {
+                thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
+                engine_compact<NT, kMaxPer * 2 / EG>(buf, &es->cnt[q], (int)cn, thr, et);
+              }
+              if (et == 0 && thr > es->thr[q]) es->thr[q] = thr;
               group_sync<NT>();
             }
           }
@@ -674,7 +687,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         const int i = EG * m + first;
         if (i >= it.ntiles) continue;
         const int T = T0 + i;
-        const int a = T & 1;
+        const int a = T & NBM;
         const int j = it.ks + i * 128 + row;
         bool valid = true;
         float kscale = 1.f;
@@ -687,7 +700,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
           valid = j < p.num_rows;
           if (kFP8 && valid) kscale = __ldg(p.k_scale + j);
         }
-        bool okt = (lane == 0) ? mbar_wait(tfull0 + 8 * a, (uint32_t)(T >> 1) & 1u, limit, abort_flag) : true;
+        bool okt = (lane == 0) ? mbar_wait(tfull0 + 8 * a, (uint32_t)(T >> NBL) & 1u, limit, abort_flag) : true;
         okt = __shfl_sync(0xFFFFFFFFu, okt ? 1 : 0, 0) != 0;
         if (!okt) {
           if (lane == 0) {
@@ -837,7 +850,7 @@ size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap) {
   size_t s = 1024;                                    // alignment slack
   s += (size_t)nq * 64 * 128 * elt;                  // Q tile
   s += (size_t)stages * 128 * 128 * elt;             // key ring
-  s += (size_t)(2 * stages + 12) * 8;                // barriers
+  s += (size_t)(2 * stages + 16) * 8;                // barriers
   s += sizeof(EpiSmem<4>) + 16;
   if (topk) s += (size_t)nq * cap * 8;
   return s;
@@ -858,7 +871,8 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
   }
   pl.ok = true;
   // One epilogue group (192 threads) for one or two query rows per item, with two CTAs
-  // per SM where shared memory allows; two groups (320 threads) for four rows.
+  // per SM where shared memory allows; otherwise (and for four rows) one CTA per SM
+  // with two groups (320 threads).
   for (;;) {
     pl.eg = pl.nq <= 2 ? 1 : 2;
     int st = 4;
@@ -882,8 +896,13 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
       pl.ctas_per_sm = 2;
     }
   }
+  if (pl.ctas_per_sm == 1) pl.eg = 2;   // one CTA per SM: two epilogue groups share its tiles
   if (tk && (pl.cap < topk + 128 * pl.eg || pl.cap < pl.pow2)) pl.ok = false;
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
+  // as many accumulator buffers (up to 4) as TMEM holds for the CTAs sharing an SM, so
+  // the MMAs can run ahead of an epilogue busy cutting its candidates back
+  pl.nbuf_log2 = 2;
+  while (pl.nbuf_log2 > 1 && pl.ctas_per_sm * next_pow2((pl.nq * 64) << pl.nbuf_log2) > 512) --pl.nbuf_log2;
   pl.ngroups = (qs.next_n + pl.nq - 1) / pl.nq;
   const int64_t units = (int64_t)qs.B * pl.ngroups;
   // logits mode: static chunks of the longest row, split when groups are few
@@ -953,9 +972,11 @@ static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, cons
 template <bool kFP8, bool kTopk>
 static cudaError_t dispatch_nq(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& prm,
                                const IndexerPlan& pl, int grid, cudaStream_t st) {
-  switch (pl.nq) {
-    case 1: return launch_one<kFP8, 1, kTopk, 1>(mq, mk, prm, pl, grid, st);
-    case 2: return launch_one<kFP8, 2, kTopk, 1>(mq, mk, prm, pl, grid, st);
+  switch (pl.nq * 2 + pl.eg) {
+    case 3: return launch_one<kFP8, 1, kTopk, 1>(mq, mk, prm, pl, grid, st);
+    case 4: return launch_one<kFP8, 1, kTopk, 2>(mq, mk, prm, pl, grid, st);
+    case 5: return launch_one<kFP8, 2, kTopk, 1>(mq, mk, prm, pl, grid, st);
+    case 6: return launch_one<kFP8, 2, kTopk, 2>(mq, mk, prm, pl, grid, st);
     default: return launch_one<kFP8, 4, kTopk, 2>(mq, mk, prm, pl, grid, st);
   }
 }
@@ -986,6 +1007,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   prm.nchunks = pl.nchunks;
   prm.chunk = pl.chunk;
   prm.stages = pl.stages;
+  prm.nbuf_log2 = pl.nbuf_log2;
   prm.logits = a.logits;
   prm.ld = a.ld;
   prm.topk = a.topk;

@@ -18,6 +18,7 @@ struct IndexerPlan {
   int nq;            // query rows per work item (1, 2 or 4)
   int eg;            // epilogue warp groups of 128 threads (1 or 2)
   int stages;        // key-tile pipeline depth
+  int nbuf_log2;     // log2 of the TMEM accumulator buffers
   int ctas_per_sm;   // resident CTAs per SM the shared memory allows (1 or 2)
   int chunk;         // logits mode: keys per work item (multiple of 128)
   int nchunks;       // logits mode: ceil(max_context_len / chunk)

@@ -127,6 +127,8 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
   extern __shared__ uint64_t mbuf[];            // kMergeKeys candidates + P selected
   __shared__ TopkShared sh;
   __shared__ uint64_t s_floor[kMergeNT / 32];
+  __shared__ uint32_t s_off[33], s_li[32];
+  __shared__ uint32_t mbins[kCutBins];
   constexpr int NT = kMergeNT;
   constexpr int kHalf = kMergeKeys / 2;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -155,28 +157,56 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
 #pragma unroll
   for (int w = 0; w < NT / 32; ++w) fl = max(fl, s_floor[w]);
   if (tid == 0) sh.thr = fl;
-  // 2. collect the keys at or above the running threshold, cutting back when full
+  // 2. collect the keys at or above the running threshold, cutting back when full;
+  //    lists are taken 32 at a time, their keys as one flat range
   uint64_t* cur = mbuf;
   uint64_t* alt = mbuf + kHalf;
-  for (int l = 0; l < nl; ++l) {
-    const size_t li = list_of(l);
-    const int cnt = (int)min((uint64_t)lcap, __ldcg(meta + 2 * li));
-    const uint64_t* src = partial + li * lcap;
-    for (int base = 0; base < cnt; base += 4 * NT) {
+  for (int c0 = 0; c0 < nl; c0 += 32) {
+    const int nc = min(32, nl - c0);
+    if (wid == 0) {
+      uint32_t cn = 0;
+      size_t li = 0;
+      if (lane < nc) {
+        li = list_of(c0 + lane);
+        cn = (uint32_t)min((uint64_t)lcap, __ldcg(meta + 2 * li));
+      }
+      uint32_t incl = cn;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      s_off[lane + 1] = incl;
+      s_li[lane] = (uint32_t)li;
+      if (lane == 0) s_off[0] = 0;
+    }
+    group_sync<NT>();
+    const int total = (int)s_off[nc];
+    for (int base = 0; base < total; base += 4 * NT) {
       uint64_t v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int e = base + u * NT + tid;
-        v[u] = e < cnt ? __ldcg(src + e) : 0ull;
+        v[u] = 0ull;
+        if (e < total) {
+          int l = 0;                            // last list with s_off[l] <= e
+#pragma unroll
+          for (int step = 16; step > 0; step >>= 1)
+            if (l + step < nc && (int)s_off[l + step] <= e) l += step;
+          v[u] = __ldcg(partial + (size_t)s_li[l] * lcap + (e - (int)s_off[l]));
+        }
       }
       group_sync<NT>();
       const uint32_t n = sh.cnt;
       if (n > (uint32_t)(kHalf - 4 * NT)) {
-        const uint64_t th = engine_select<NT>(cur, (int)n, topk, &sh.esc, tid);
-        engine_compact_to<NT>(cur, alt, &sh.cnt, (int)n, th, tid, (uint32_t)kHalf);
-        uint64_t* tmp = cur;
-        cur = alt;
-        alt = tmp;
+        uint64_t th = engine_cut_approx<NT, kHalf / NT>(cur, &sh.cnt, (int)n, topk, (uint32_t)(kHalf / 2), mbins,
+                                                        &sh.esc, tid);
+        if (th == 0ull) {
+          th = engine_select<NT>(cur, (int)n, topk, &sh.esc, tid);
+          engine_compact_to<NT>(cur, alt, &sh.cnt, (int)n, th, tid, (uint32_t)kHalf);
+          uint64_t* tmp = cur;
+          cur = alt;
+          alt = tmp;
+        }
         if (tid == 0 && th > sh.thr) sh.thr = th;
         group_sync<NT>();
       }
@@ -185,10 +215,15 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
       for (int u = 0; u < 4; ++u)
         engine_append(cur, &sh.cnt, v[u], v[u] != 0ull && v[u] >= th, (uint32_t)kHalf, 31u);
     }
+    group_sync<NT>();                           // s_off / s_li are rewritten next round
   }
-  group_sync<NT>();
-  // 3. exactly the top-k (or every candidate when there are fewer)
-  const uint32_t n = sh.cnt;
+  // 3. exactly the top-k (or every candidate when there are fewer): a histogram cut
+  //    first, then the radix select over what is left
+  uint32_t n = sh.cnt;
+  if (n > (uint32_t)topk) {
+    engine_cut_approx<NT, kHalf / NT>(cur, &sh.cnt, (int)n, topk, n, mbins, &sh.esc, tid);
+    n = sh.cnt;
+  }
   const uint64_t thr = engine_select<NT>(cur, (int)n, topk, &sh.esc, tid);
   uint64_t* out = mbuf + kMergeKeys;
   if (tid == 0) sh.cnt = 0;
