@@ -4,10 +4,11 @@
 // elements (2^(b-127), 0xFF -> 0), dequantised to bf16; padded slots give zero rows.
 //
 // HBM-bound: 68 bytes read and 256 bytes written per live row.  A warp owns 32 rows per
-// step: each lane resolves one row's source (sel_pos -> block table -> cache row) with
-// independent loads, then the warp moves the rows four at a time (8 lanes x 8 nibble
-// bytes per row, one 32-byte store per lane), with all eight groups' loads in flight
-// before any decode.
+// step.  Each lane resolves one row's source (sel_pos -> block table -> cache row); the
+// warp then moves the rows two at a time, 16 lanes per row: a lane loads 4 nibble bytes
+// (8 elements) and their scale byte and writes 16 bytes, so every store instruction
+// writes two whole 256-byte rows.  The next step's positions and block-table entries
+// are fetched while the current rows are in flight.
 #include "common.cuh"
 #include "launch.h"
 
@@ -38,24 +39,40 @@ __device__ __forceinline__ uint32_t e2m1_bf16_fast(uint32_t n, uint32_t base) {
   return (c != 0u ? v : 0u) | s;
 }
 
-__device__ __forceinline__ void decode16(uint2 w, uint32_t b, uint4& lo, uint4& hi) {
-  uint32_t o[8];
-  if (b >= 2u && b <= 252u) {
-    const uint32_t base = (b - 1u) << 7;
+// Decode table: entry `byte` holds the bf16 pair of its two nibbles (low nibble in the
+// low half) at scale byte b = 2, and a mask of the nonzero halves.  For 2 <= b <= 252
+// the pair at scale b is entry + ((b - 2) << 7 in both halves, masked): that moves the
+// exponent field of each nonzero half (at most 0x7F40 with the sign clear, so no carry
+// crosses a half) and leaves signed zeros alone.
+__device__ __forceinline__ uint2 lut_entry(uint32_t byte) {
+  uint32_t v = 0, m = 0;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t byte = ((k < 4 ? w.x : w.y) >> (8 * (k & 3))) & 0xFFu;
-      o[k] = e2m1_bf16_fast(byte & 0xFu, base) | (e2m1_bf16_fast(byte >> 4, base) << 16);
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t n = (byte >> (4 * h)) & 0xFu;
+    v |= e2m1_bf16_fast(n, 1u << 7) << (16 * h);
+    if (n & 7u) m |= 0xFFFFu << (16 * h);
+  }
+  return make_uint2(v, m);
+}
+
+// Eight elements (nibble bytes of w, low nibble first) times 2^(b-127) as bf16 pairs.
+__device__ __forceinline__ uint4 decode8(uint32_t w, uint32_t b, const uint2* lut) {
+  uint32_t o[4];
+  if (b >= 2u && b <= 252u) {
+    const uint32_t adj = ((b - 2u) << 7) * 0x10001u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint2 e = lut[(w >> (8 * k)) & 0xFFu];
+      o[k] = e.x + (adj & e.y);
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t byte = ((k < 4 ? w.x : w.y) >> (8 * (k & 3))) & 0xFFu;
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t byte = (w >> (8 * k)) & 0xFFu;
       o[k] = e2m1_bf16_general(byte & 0xFu, (int)b) | (e2m1_bf16_general(byte >> 4, (int)b) << 16);
     }
   }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
@@ -64,67 +81,74 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
                : "memory");
 }
 
-__global__ void __launch_bounds__(256) mxfp4_gather_kernel(const uint8_t* __restrict__ fp4,
-                                                           const uint8_t* __restrict__ scale,
-                                                           int64_t num_blocks, int bs,
-                                                           const int32_t* __restrict__ table,
-                                                           int64_t bt_stride,
-                                                           const int32_t* __restrict__ sel,
-                                                           int next_n, int topk, int64_t rows,
-                                                           uint16_t* __restrict__ out) {
+struct GatherArgs {
+  const uint8_t* fp4;
+  const uint8_t* scale;
+  int64_t num_blocks;
+  int bs;
+  const int32_t* table;
+  int64_t bt_stride;
+  const int32_t* sel;
+  int64_t rows_per_seq;     // next_n * topk
+  int64_t rows;
+  uint16_t* out;
+};
+
+// Cache row of output row r with selected position pos (-1: zero row).
+__device__ __forceinline__ int64_t gather_source(const GatherArgs& g, int64_t r, int32_t pos) {
+  if (r >= g.rows || pos < 0) return -1;
+  const int64_t b = r / g.rows_per_seq;
+  const int32_t col = pos / g.bs;
+  if (col < g.bt_stride) {
+    const int32_t blk = __ldg(g.table + b * g.bt_stride + col);
+    if (blk >= 0 && blk < g.num_blocks) return (int64_t)blk * g.bs + pos % g.bs;
+  }
+  raise_error(DSA_DEVERR_INDEX);
+  return -1;
+}
+
+__global__ void __launch_bounds__(256) mxfp4_gather_kernel(const GatherArgs g) {
+  __shared__ uint2 lut[256];
+  lut[threadIdx.x] = lut_entry(threadIdx.x);
+  __syncthreads();
+  grid_dependency_wait();              // positions may come from the kernel just before
   const uint32_t lane = threadIdx.x & 31u;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int sub = (int)(lane >> 3);    // row within a group of four
-  const int part = (int)(lane & 7u);   // 16 elements: nibble bytes 8*part .. 8*part+7
-  for (int64_t r0 = warp * 32; r0 < rows; r0 += nwarps * 32) {
-    // 1. each lane resolves one row: -1 = write zeros
-    int64_t src = -1;
+  const int64_t step = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int sub = (int)(lane >> 4);    // row within a pair
+  const int part = (int)(lane & 15u);  // elements 8 * part .. 8 * part + 7
+  int64_t r0 = warp * 32;
+  int64_t src_next = -1;
+  if (r0 < g.rows) {
     const int64_t r = r0 + lane;
-    if (r < rows) {
-      const int32_t pos = __ldg(sel + r);
-      if (pos >= 0) {
-        const int64_t b = (r / topk) / next_n;
-        const int64_t col = pos / bs;
-        bool ok = false;
-        if (col < bt_stride) {
-          const int32_t blk = __ldg(table + b * bt_stride + col);
-          if (blk >= 0 && blk < num_blocks) {
-            src = (int64_t)blk * bs + pos % bs;
-            ok = true;
-          }
+    src_next = gather_source(g, r, r < g.rows ? __ldg(g.sel + r) : -1);
+  }
+  for (; r0 < g.rows; r0 += step * 32) {
+    const int64_t src = src_next;
+    const int64_t r1 = r0 + step * 32 + lane;
+    const int32_t pos_next = r1 < g.rows ? __ldg(g.sel + r1) : -1;   // in flight meanwhile
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t w[8], sb[8];
+      int64_t srow[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        srow[k] = __shfl_sync(0xFFFFFFFFu, src, h * 16 + 2 * k + sub);
+        w[k] = 0u;
+        sb[k] = 255u;
+        if (srow[k] >= 0) {
+          w[k] = __ldg(reinterpret_cast<const uint32_t*>(g.fp4 + srow[k] * 64) + part);
+          sb[k] = __ldg(g.scale + srow[k] * 4 + (part >> 2));
         }
-        if (!ok) raise_error(DSA_DEVERR_INDEX);
       }
-    }
-    // 2. eight groups of four rows; issue every load first
-    uint2 w[8];
-    uint32_t sb[8];
-    int64_t srow[8];
+      if (h == 0) src_next = gather_source(g, r1, pos_next);
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      srow[g] = __shfl_sync(0xFFFFFFFFu, src, g * 4 + sub);
-      w[g] = make_uint2(0u, 0u);
-      sb[g] = 255u;
-      if (srow[g] >= 0) {
-        w[g] = __ldg(reinterpret_cast<const uint2*>(fp4 + srow[g] * 64 + part * 8));
-        sb[g] = __ldg(scale + srow[g] * 4 + (part >> 1));
+      for (int k = 0; k < 8; ++k) {
+        const int64_t row = r0 + h * 16 + 2 * k + sub;
+        if (row >= g.rows) continue;
+        const uint4 v = srow[k] >= 0 ? decode8(w[k], sb[k], lut) : make_uint4(0u, 0u, 0u, 0u);
+        st_stream(reinterpret_cast<uint4*>(g.out + row * 128) + part, v);
       }
-    }
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int64_t row = r0 + g * 4 + sub;
-      if (row >= rows) continue;
-      uint4 lo, hi;
-      if (srow[g] >= 0) {
-        decode16(w[g], sb[g], lo, hi);
-      } else {
-        lo = make_uint4(0u, 0u, 0u, 0u);
-        hi = lo;
-      }
-      uint4* dst = reinterpret_cast<uint4*>(out + row * 128 + part * 16);
-      st_stream(dst, lo);
-      st_stream(dst + 1, hi);
     }
   }
 }
@@ -133,13 +157,22 @@ cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_
                                 const int32_t* table, int64_t bt_stride, const int32_t* sel, int next_n,
                                 int topk, int64_t rows, uint16_t* out, int num_sms, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
+  GatherArgs g{fp4, scale, num_blocks, bs, table, bt_stride, sel, (int64_t)next_n * topk, rows, out};
   const int64_t warps_needed = (rows + 31) / 32;
   const int64_t blocks_needed = (warps_needed + 7) / 8;
-  const int64_t cap = (int64_t)num_sms * 8;   // 8 blocks of 256 threads per SM
-  const int grid = (int)(blocks_needed < cap ? blocks_needed : cap);
-  mxfp4_gather_kernel<<<grid, 256, 0, stream>>>(fp4, scale, num_blocks, bs, table, bt_stride, sel, next_n,
-                                                topk, rows, out);
+  const int64_t cap = (int64_t)num_sms * 4;   // resident blocks of 256 threads per SM
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(blocks_needed < cap ? blocks_needed : cap));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, mxfp4_gather_kernel, g);
   note_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
   constexpr int kHalf = kMergeKeys / 2;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   grid_dependency_wait();                       // the fused kernel's lists are complete
+  grid_launch_dependents();                     // a gather of the results may set up meanwhile
   const int blk = (int)blockIdx.x;
   const int si = blk / nq, q = blk - si * nq;
   if (si >= __ldcg(plan + 2)) return;
