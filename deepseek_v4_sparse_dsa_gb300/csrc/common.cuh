@@ -236,6 +236,26 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// tmem_ld64 split in two, so the load of one block of columns can overlap work on the
+// previous one: tmem_ld64_issue starts the load, tmem_ld64_wait completes every load the
+// thread has issued and marks `r` as written only then (its registers are operands, so
+// the compiler cannot move their uses above the wait).
+__device__ __forceinline__ void tmem_ld64_issue(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld64_wait(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63]) : : "memory");
+}
+
 // ---------------------------------------------------------------------------------
 // Ranking key of the tie rule: larger value first, then smaller index.
 // High 32 bits: order-preserving image of the fp32 value (-0.0 folded onto +0.0);
@@ -268,11 +288,11 @@ __device__ __forceinline__ bool is_candidate(float v) { return v > -INFINITY; }
 
 // ---------------------------------------------------------------------------------
 // Shared-memory top-k engine.  Run by a group of NT threads (a multiple of 128) that
-// synchronise on named barrier 1; `tid` = 0..NT-1 within the group.
+// synchronise on named barrier `bar` (1 unless given); `tid` = 0..NT-1 within the group.
 // ---------------------------------------------------------------------------------
 template <int NT>
-__device__ __forceinline__ void group_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+__device__ __forceinline__ void group_sync(int bar = 1) {
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(NT) : "memory");
 }
 
 struct EngineScratch {
@@ -298,6 +318,37 @@ __device__ __forceinline__ void engine_append(uint64_t* buf, uint32_t* cnt, uint
     const uint32_t slot = base + __popc(m & ((1u << lane) - 1u));
     if (slot < cap) buf[slot] = key;
     else raise_error(DSA_DEVERR_OVERFLOW | ((site & 0xFFu) << 8));
+  }
+}
+
+// engine_append for NQ candidate buffers at once (buffer q at buf + q * stride, count
+// cnt[q]): one round of shared atomics, issued back to back by lane 0, for all of them.
+template <int NQ>
+__device__ __forceinline__ void engine_append_multi(uint64_t* buf, size_t stride, uint32_t* cnt,
+                                                    const uint64_t (&key)[NQ], const bool (&take)[NQ],
+                                                    uint32_t cap, uint32_t site) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t below = (1u << lane) - 1u;
+  uint32_t m[NQ], base[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    m[q] = __ballot_sync(0xFFFFFFFFu, take[q]);
+    base[q] = 0u;
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      if (m[q]) base[q] = atomicAdd(&cnt[q], (uint32_t)__popc(m[q]));
+  }
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    if (m[q] == 0u) continue;
+    const uint32_t b = __shfl_sync(0xFFFFFFFFu, base[q], 0);
+    if (take[q]) {
+      const uint32_t slot = b + __popc(m[q] & below);
+      if (slot < cap) buf[q * stride + slot] = key[q];
+      else raise_error(DSA_DEVERR_OVERFLOW | ((site & 0xFFu) << 8));
+    }
   }
 }
 
@@ -349,28 +400,28 @@ __device__ __forceinline__ void pick_digit(uint32_t* hist, uint32_t* pick, uint3
 // 1 when there are at most k of them.  Most-significant-digit-first radix select over
 // 8-bit digits; zero slots are ignored.
 template <int NT>
-__device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScratch* sc, int tid) {
+__device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScratch* sc, int tid, int bar = 1) {
   uint64_t prefix = 0, mask = 0;
   uint32_t need = (uint32_t)k;
   for (int shift = 56; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += NT) sc->hist[i] = 0;
-    group_sync<NT>();
+    group_sync<NT>(bar);
     for (int base = 0; base < n; base += NT) {
       const int e = base + tid;
       const uint64_t key = e < n ? buf[e] : 0ull;
       hist_add(sc->hist, key != 0ull && (key & mask) == prefix, (uint32_t)(key >> shift) & 255u);
     }
-    group_sync<NT>();
+    group_sync<NT>(bar);
     if (tid < 32) pick_digit(sc->hist, sc->pick, need, tid);   // lane l: digits 255-8l .. 248-8l
-    group_sync<NT>();
+    group_sync<NT>(bar);
     if (shift == 56 && sc->pick[3] <= (uint32_t)k) {           // at most k keys: take them all
-      group_sync<NT>();
+      group_sync<NT>(bar);
       return 1ull;
     }
     const uint32_t d = sc->pick[0], above = sc->pick[1], inbin = sc->pick[2];
     if (d > 255u) {                // counts did not add up: keep everything (never drops a key)
       if (tid == 0) raise_error(DSA_DEVERR_OVERFLOW | (42u << 8));
-      group_sync<NT>();
+      group_sync<NT>(bar);
       return 1ull;
     }
     need -= above;
@@ -378,7 +429,7 @@ __device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScrat
     mask |= (uint64_t)0xFF << shift;
     if (inbin == need) break;      // every key with this prefix belongs to the set
   }
-  group_sync<NT>();                // everyone has read pick[] before it is reused
+  group_sync<NT>(bar);                // everyone has read pick[] before it is reused
   return prefix;
 }
 
@@ -419,6 +470,45 @@ __device__ uint64_t engine_select_global(const uint64_t* src, int n, int k, Engi
   return prefix;
 }
 
+// Writes the keys of keep[] that are nonzero and >= thr (t_ord: compare only the high
+// 32 bits against t_hi) to the front of buf, in thread order, with one prefix sum over
+// the group instead of an atomic per key; *cnt becomes their number.  Every key of buf
+// must already sit in some thread's keep[] (the writes may overwrite any slot).  Uses
+// sc->hist[0, NT/32) as scratch; ends with a group barrier.
+template <int NT, int MAXPER, bool kByOrd>
+__device__ __forceinline__ void engine_scatter(uint64_t* buf, uint32_t* cnt, const uint64_t (&keep)[MAXPER],
+                                               uint64_t thr, uint32_t t_hi, EngineScratch* sc, int tid, int bar) {
+  constexpr int NW = NT / 32;
+  const int lane = tid & 31, w = tid >> 5;
+  uint32_t mine = 0;
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i) {
+    const bool t = kByOrd ? (keep[i] != 0ull && (uint32_t)(keep[i] >> 32) >= t_hi) : (keep[i] != 0ull && keep[i] >= thr);
+    mine += t ? 1u : 0u;
+  }
+  uint32_t incl = mine;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sc->hist[w] = incl;
+  group_sync<NT>(bar);
+  uint32_t off = incl - mine, total = 0;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    const uint32_t c = sc->hist[i];
+    if (i < w) off += c;
+    total += c;
+  }
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i) {
+    const bool t = kByOrd ? (keep[i] != 0ull && (uint32_t)(keep[i] >> 32) >= t_hi) : (keep[i] != 0ull && keep[i] >= thr);
+    if (t) buf[off++] = keep[i];
+  }
+  if (tid == 0) *cnt = total;
+  group_sync<NT>(bar);
+}
+
 // Cheap cut-back of a candidate buffer that only has to stay a superset of its top-k:
 // finds a threshold T with at least k of the nonzero keys of buf[0, n) at or above it
 // from one 512-bin histogram of the keys' values (bins linear in the order-preserving
@@ -431,7 +521,7 @@ constexpr int kCutBins = 512;
 
 template <int NT, int MAXPER>
 __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k, uint32_t room, uint32_t* bins,
-                                      EngineScratch* sc, int tid) {
+                                      EngineScratch* sc, int tid, int bar = 1) {
   constexpr int NW = NT / 32;
   constexpr int BPT = kCutBins / NT;               // bins per thread in the scan
   static_assert(kCutBins % NT == 0 && NW <= 16, "group size");
@@ -461,7 +551,7 @@ __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k
     wred[2 * NW + w] = nz;
   }
   for (int i = tid; i < kCutBins; i += NT) bins[i] = 0u;
-  group_sync<NT>();
+  group_sync<NT>(bar);
   lo = 0xFFFFFFFFu;
   hi = 0u;
   nz = 0u;
@@ -472,14 +562,14 @@ __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k
     nz += wred[2 * NW + i];
   }
   if (nz <= (uint32_t)k || hi == lo) {
-    group_sync<NT>();                               // wred is read before it is reused
+    group_sync<NT>(bar);                               // wred is read before it is reused
     return 0ull;
   }
   const uint64_t span = (uint64_t)(hi - lo) + 1u;
 #pragma unroll
   for (int i = 0; i < MAXPER; ++i)
     if (keep[i]) atomicAdd(&bins[(uint32_t)(((uint64_t)((uint32_t)(keep[i] >> 32) - lo) * kCutBins) / span)], 1u);
-  group_sync<NT>();
+  group_sync<NT>(bar);
   // bin b* holding the k-th key from the top: thread tid scans bins
   // [kCutBins - (tid + 1) * BPT, kCutBins - tid * BPT) top down
   uint32_t c[BPT], sum = 0;
@@ -495,7 +585,7 @@ __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k
   }
   uint32_t* wsum = sc->hist + 3 * NW;               // [3 * NW, 4 * NW): per-warp totals
   if (lane == 31) wsum[w] = incl;
-  group_sync<NT>();
+  group_sync<NT>(bar);
   uint32_t before = 0;
   for (int i = 0; i < w; ++i) before += wsum[i];
   uint32_t above = before + incl - sum;
@@ -509,40 +599,31 @@ __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k
       above += c[i];
     }
   }
-  group_sync<NT>();
+  group_sync<NT>(bar);
   const uint32_t b = sc->pick[0], count = sc->pick[1];
   if (count > room) {
-    group_sync<NT>();
+    group_sync<NT>(bar);
     return 0ull;
   }
   // smallest value image in bins >= b
   const uint32_t tord = lo + (uint32_t)(((uint64_t)b * span + kCutBins - 1) / kCutBins);
-  if (tid == 0) *cnt = 0;
-  group_sync<NT>();
-#pragma unroll
-  for (int i = 0; i < MAXPER; ++i)
-    engine_append(buf, cnt, keep[i], keep[i] != 0ull && (uint32_t)(keep[i] >> 32) >= tord, (uint32_t)(NT * MAXPER), 3u);
-  group_sync<NT>();
+  engine_scatter<NT, MAXPER, true>(buf, cnt, keep, 0ull, tord, sc, tid, bar);
   return (uint64_t)tord << 32;
 }
 
 // Keeps the keys >= thr of buf[0, n), packed to the front; *cnt becomes their
-// number.  Holds the keys in registers meanwhile: needs n <= NT * MAXPER.
+// number.  Holds the keys in registers meanwhile: needs n <= NT * MAXPER.  The caller
+// has passed a group barrier since buf and n were last written.
 template <int NT, int MAXPER>
-__device__ void engine_compact(uint64_t* buf, uint32_t* cnt, int n, uint64_t thr, int tid) {
+__device__ void engine_compact(uint64_t* buf, uint32_t* cnt, int n, uint64_t thr, EngineScratch* sc, int tid,
+                               int bar = 1) {
   uint64_t keep[MAXPER];
 #pragma unroll
   for (int i = 0; i < MAXPER; ++i) {
     const int e = tid + i * NT;
     keep[i] = (e < n) ? buf[e] : 0ull;
   }
-  group_sync<NT>();
-  if (tid == 0) *cnt = 0;
-  group_sync<NT>();
-#pragma unroll
-  for (int i = 0; i < MAXPER; ++i)
-    engine_append(buf, cnt, keep[i], keep[i] != 0ull && keep[i] >= thr, (uint32_t)(NT * MAXPER), 1u);
-  group_sync<NT>();
+  engine_scatter<NT, MAXPER, false>(buf, cnt, keep, thr, 0u, sc, tid, bar);
 }
 
 // Copies the keys >= thr of src[0, n) to the front of dst (capacity dcap); *cnt becomes
@@ -580,6 +661,63 @@ __device__ void engine_sort(uint64_t* buf, int stride, int nlist, int P, int tid
         }
       }
       group_sync<NT>();
+    }
+  }
+}
+
+// As engine_sort for one list, run by a single warp (no block barrier): sorts the P
+// (power of two) keys at buf in descending order.
+__device__ __forceinline__ void warp_sort(uint64_t* buf, int P) {
+  const int lane = threadIdx.x & 31;
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int half = size >> 1; half > 0; half >>= 1) {
+      for (int t = lane; t < (P >> 1); t += 32) {
+        const int i = 2 * t - (t & (half - 1));
+        const int j = i + half;
+        const uint64_t x = buf[i], y = buf[j];
+        const bool desc = (i & size) == 0;
+        if ((x < y) == desc) {
+          buf[i] = y;
+          buf[j] = x;
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// Sorts 32 * KPL keys held by one warp in registers in descending order; element
+// e = r * 32 + lane is x[r] of that lane.  Same bitonic network as engine_sort: pairs
+// closer than 32 exchange through shuffles, the others within a thread.
+template <int KPL>
+__device__ __forceinline__ void warp_sort_regs(uint64_t (&x)[KPL]) {
+  const int lane = threadIdx.x & 31;
+  constexpr int N = 32 * KPL;
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+    for (int half = size >> 1; half > 0; half >>= 1) {
+      if (half >= 32) {
+        const int rh = half >> 5;
+#pragma unroll
+        for (int r = 0; r < KPL; ++r) {
+          if ((r & rh) == 0) {
+            const bool desc = ((r * 32 + lane) & size) == 0;
+            const uint64_t a = x[r], b = x[r + rh];
+            const bool sw = (a < b) == desc;
+            x[r] = sw ? b : a;
+            x[r + rh] = sw ? a : b;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < KPL; ++r) {
+          const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, x[r], half);
+          const bool desc = ((r * 32 + lane) & size) == 0;
+          const bool keep_max = ((lane & half) == 0) == desc;
+          x[r] = keep_max ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
+        }
+      }
     }
   }
 }

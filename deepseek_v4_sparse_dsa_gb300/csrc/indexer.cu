@@ -93,17 +93,38 @@ struct EpiSmem {
   uint32_t bins[kCutBins];
 };
 
-__device__ __forceinline__ float head_sum(const float (&s)[64], const float* w) {
+__device__ __forceinline__ float head_sum(const uint32_t (&s)[64], const float* w) {
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
   for (int h = 0; h < 64; h += 4) {
     const float4 wv = *reinterpret_cast<const float4*>(w + h);
-    a0 = fmaf(wv.x, fmaxf(s[h + 0], 0.f), a0);
-    a1 = fmaf(wv.y, fmaxf(s[h + 1], 0.f), a1);
-    a2 = fmaf(wv.z, fmaxf(s[h + 2], 0.f), a2);
-    a3 = fmaf(wv.w, fmaxf(s[h + 3], 0.f), a3);
+    a0 = fmaf(wv.x, fmaxf(__uint_as_float(s[h + 0]), 0.f), a0);
+    a1 = fmaf(wv.y, fmaxf(__uint_as_float(s[h + 1]), 0.f), a1);
+    a2 = fmaf(wv.z, fmaxf(__uint_as_float(s[h + 2]), 0.f), a2);
+    a3 = fmaf(wv.w, fmaxf(__uint_as_float(s[h + 3]), 0.f), a3);
   }
   return (a0 + a1) + (a2 + a3);
+}
+
+// Head sums of the NQ query rows of one key (this thread's TMEM lane) from the
+// accumulator columns at `tcol`: the load of row q + 1 overlaps the sum of row q.
+template <int NQ>
+__device__ __forceinline__ void head_sums(uint32_t tcol, const float* wq, float (&v)[NQ]) {
+  uint32_t ra[64], rb[64];
+  tmem_ld64_issue(tcol, ra);
+  tmem_ld64_wait(ra);
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    if (q & 1) {
+      if (q + 1 < NQ) tmem_ld64_issue(tcol + (uint32_t)((q + 1) * 64), ra);
+      v[q] = head_sum(rb, wq + q * 64);
+      if (q + 1 < NQ) tmem_ld64_wait(ra);
+    } else {
+      if (q + 1 < NQ) tmem_ld64_issue(tcol + (uint32_t)((q + 1) * 64), rb);
+      v[q] = head_sum(ra, wq + q * 64);
+      if (q + 1 < NQ) tmem_ld64_wait(rb);
+    }
+  }
 }
 
 // Query group u = b * ngroups + gi: its sequence, rows and visible key counts.
@@ -327,11 +348,50 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
 }
 
+// One warp: sorts the cn (<= 32 * KPL) keys at buf in registers and writes the first
+// k of them as the row's indices (and values), -1 / -inf past the candidates.
+template <int KPL>
+__device__ __forceinline__ void rank_row(const uint64_t* buf, int cn, int k, bool real, int32_t* out_idx,
+                                         float* out_val) {
+  const int lane = threadIdx.x & 31;
+  uint64_t x[KPL];
+#pragma unroll
+  for (int r = 0; r < KPL; ++r) {
+    const int e = r * 32 + lane;
+    x[r] = e < cn ? buf[e] : 0ull;
+  }
+  warp_sort_regs<KPL>(x);
+  if (!real) return;
+#pragma unroll
+  for (int r = 0; r < KPL; ++r) {
+    const int s = r * 32 + lane;
+    if (s < k) {
+      out_idx[s] = x[r] ? index_of_key(x[r]) : -1;
+      if (out_val) out_val[s] = x[r] ? value_of_key(x[r]) : -INFINITY;
+    }
+  }
+}
+
+// As rank_row for rows of more than 1024 keys: zero-pads buf to P, sorts it in shared
+// memory with one warp.
+__device__ __forceinline__ void rank_row_smem(uint64_t* buf, int cn, int P, int k, bool real, int32_t* out_idx,
+                                              float* out_val) {
+  const int lane = threadIdx.x & 31;
+  for (int e = cn + lane; e < P; e += 32) buf[e] = 0ull;
+  __syncwarp();
+  warp_sort(buf, P);
+  if (!real) return;
+  for (int s = lane; s < k; s += 32) {
+    const uint64_t key = buf[s];
+    out_idx[s] = key ? index_of_key(key) : -1;
+    if (out_val) out_val[s] = key ? value_of_key(key) : -INFINITY;
+  }
+}
+
 template <bool kFP8, int NQ, bool kTopk, int EG>
 __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const IndexerParams p) {
-  constexpr int NT = 128 * EG;                     // epilogue threads
   constexpr int N = NQ * 64;                       // MMA N: (query, head) rows
   constexpr int ELT = kFP8 ? 1 : 2;                // bytes per element
   constexpr int KCH = kFP8 ? 1 : 2;                // 128-byte K chunks per row (D = 128)
@@ -378,7 +438,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     }
     for (int a = 0; a < 4; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, 4);          // the 4 warps of the group that read the tile
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(ifull0 + 8 * a, 1);
@@ -611,13 +671,18 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     tmem_dealloc(tmem_base, TMEM_COLS);
   } else {
     // ============================ epilogue ============================
-    const int et = threadIdx.x - 64;            // 0..NT-1
+    // EG groups of 4 warps take the tiles in turn (global tile T goes to group T % EG);
+    // all NT threads share the per-row candidate buffers and cut them back together.
+    constexpr int NT = 128 * EG;
+    constexpr int MAXPER = kMaxPer * 2 / EG;     // candidate slots per thread in a cut-back
+    const int et = threadIdx.x - 64;             // 0..NT-1
     const int grp = (warp - 2) >> 2;
-    const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-    const int row = quarter * 32 + lane;        // key row within the tile
+    const int ew = warp - 2;                     // epilogue warp 0..4*EG-1
+    const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
+    const int row = quarter * 32 + lane;         // key row within the tile
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const int cap = p.cap;
-    int T0 = 0;                                 // global index of the item's first tile
+    int T0 = 0;                                  // global index of the item's first tile
     for (int n = 0;; ++n) {
       const int slot = n & 1;
       bool ok = (lane == 0) ? mbar_wait(ifull0 + 8 * slot, (uint32_t)(n >> 1) & 1u, limit, abort_flag) : true;
@@ -626,9 +691,9 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         raise_error(DSA_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
-      // One thread decides for the whole group between two barriers (the abort flag may
-      // change at any time); an expired wait means the producer is gone: stop as on the
-      // end-of-work descriptor.
+      // One thread decides for all epilogue warps between two barriers (the abort flag
+      // may change at any time); an expired wait means the producer is gone: stop as on
+      // the end-of-work descriptor.
       group_sync<NT>();
       if (et == 0) es->stop = (*abort_flag != 0) || !es->info[slot].valid;
       group_sync<NT>();
@@ -645,7 +710,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         }
         es->w[slot][q][h] = w;
       }
-      if (kTopk && et < 4) {
+      if (kTopk && et < NQ) {
         es->cnt[et] = 0;
         es->thr[et] = 0;
       }
@@ -662,6 +727,9 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
                                                : (int64_t)-1;
       };
       int64_t blk_next = (paged && first < it.ntiles) ? page_of(first) : -1;
+      float ks_next = 1.f;                      // contiguous E4M3 keys: scale of the next tile's key
+      if (kFP8 && !paged && first < it.ntiles && it.ks + first * 128 + row < p.num_rows)
+        ks_next = __ldg(p.k_scale + it.ks + first * 128 + row);
       for (int m = 0; m < niter; ++m) {
         if (kTopk) {
           group_sync<NT>();
@@ -673,11 +741,11 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
               // cannot free enough room
               uint64_t* buf = ebuf + (size_t)q * cap;
               const uint32_t room = (uint32_t)min((cap + p.topk) / 2, cap - 256 * EG);
-              uint64_t thr = engine_cut_approx<NT, kMaxPer * 2 / EG>(buf, &es->cnt[q], (int)cn, p.topk, room,
-                                                                     es->bins, &es->esc, et);
+              uint64_t thr = engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, room, es->bins,
+                                                           &es->esc, et);
               if (thr == 0ull) {
                 thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
-                engine_compact<NT, kMaxPer * 2 / EG>(buf, &es->cnt[q], (int)cn, thr, et);
+                engine_compact<NT, MAXPER>(buf, &es->cnt[q], (int)cn, thr, &es->esc, et);
               }
               if (et == 0 && thr > es->thr[q]) es->thr[q] = thr;
               group_sync<NT>();
@@ -698,7 +766,11 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
           if (kFP8 && valid) kscale = __ldg(p.k_scale + blk * bs + (j % bs));
         } else {
           valid = j < p.num_rows;
-          if (kFP8 && valid) kscale = __ldg(p.k_scale + j);
+          if (kFP8) {
+            kscale = ks_next;
+            const int jn = j + EG * 128;
+            if (i + EG < it.ntiles && jn < p.num_rows) ks_next = __ldg(p.k_scale + jn);
+          }
         }
         bool okt = (lane == 0) ? mbar_wait(tfull0 + 8 * a, (uint32_t)(T >> NBL) & 1u, limit, abort_flag) : true;
         okt = __shfl_sync(0xFFFFFFFFu, okt ? 1 : 0, 0) != 0;
@@ -712,13 +784,12 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         __syncwarp();
         tc_fence_after();
         float v[NQ];
+        head_sums<NQ>(t_lane + (uint32_t)(a * N), wq, v);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-          float acc[64];
-          tmem_ld64(t_lane + (uint32_t)(a * N + q * 64), acc);
-          float s = head_sum(acc, wq + q * 64);
-          if (kFP8) s = s * kscale;
-          v[q] = canon_zero(s);
+          float sq = v[q];
+          if (kFP8) sq = sq * kscale;
+          v[q] = canon_zero(sq);
         }
         tc_fence_before();
         __syncwarp();
@@ -732,12 +803,14 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
                 p.logits[(int64_t)(it.t0 + q) * p.ld + j] = (valid && j < it.vis[q]) ? v[q] : -INFINITY;
           }
         } else {
+          uint64_t key[NQ];
+          bool take[NQ];
 #pragma unroll
           for (int q = 0; q < NQ; ++q) {
-            const uint64_t key = rank_key(v[q], (uint32_t)j);
-            const bool take = valid && j < it.vis[q] && is_candidate(v[q]) && key >= es->thr[q];
-            engine_append(ebuf + (size_t)q * cap, &es->cnt[q], key, take, (uint32_t)cap, 10u);
+            key[q] = rank_key(v[q], (uint32_t)j);
+            take[q] = valid && j < it.vis[q] && is_candidate(v[q]) && key[q] >= es->thr[q];
           }
+          engine_append_multi<NQ>(ebuf, (size_t)cap, es->cnt, key, take, (uint32_t)cap, 10u);
         }
       }
       T0 += it.ntiles;
@@ -749,33 +822,37 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         for (int q = 0; q < it.nreal; ++q)
           for (int jj = f0 + et; jj < f1; jj += NT) p.logits[(int64_t)(it.t0 + q) * p.ld + jj] = -INFINITY;
       } else if (!it.split) {
-        // the whole group in one item: cut back to the top-k, sort, final rows
+        // the whole group in one item: cut each row's candidates back to at most SN
+        // (histogram first, the exact radix select only if that is not enough), then one
+        // warp per row sorts them in registers and writes the first k
+        const int P = p.pow2;
+        const int SN = P <= 128 ? 256 : (P <= 512 ? 2 * P : P);   // keys sorted per row
         group_sync<NT>();
 #pragma unroll 1
         for (int q = 0; q < NQ; ++q) {
-          const uint32_t cn = es->cnt[q];
-          if (cn > (uint32_t)p.topk) {
-            uint64_t* buf = ebuf + (size_t)q * cap;
+          uint32_t cn = es->cnt[q];
+          uint64_t* buf = ebuf + (size_t)q * cap;
+          if (cn > (uint32_t)SN) {
+            engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, (uint32_t)SN, es->bins, &es->esc, et);
+            cn = es->cnt[q];
+          }
+          if (cn > (uint32_t)SN) {
             const uint64_t thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
-            engine_compact<NT, kMaxPer * 2 / EG>(buf, &es->cnt[q], (int)cn, thr, et);
+            engine_compact<NT, MAXPER>(buf, &es->cnt[q], (int)cn, thr, &es->esc, et);
           }
         }
         group_sync<NT>();
-        const int P = p.pow2;
-        for (int q = 0; q < NQ; ++q) {
+        for (int q = ew; q < NQ; q += 4 * EG) {
+          uint64_t* buf = ebuf + (size_t)q * cap;
           const int cn = (int)es->cnt[q];
-          for (int e = cn + et; e < P; e += NT) ebuf[(size_t)q * cap + e] = 0ull;
-        }
-        group_sync<NT>();
-        engine_sort<NT>(ebuf, cap, NQ, P, et);
-        for (int q = 0; q < it.nreal; ++q) {
           const int64_t t = it.t0 + q;
-          const uint64_t* buf = ebuf + (size_t)q * cap;
-          for (int s = et; s < p.topk; s += NT) {
-            const uint64_t key = buf[s];
-            p.out_idx[t * p.topk + s] = key ? index_of_key(key) : -1;
-            if (p.out_val) p.out_val[t * p.topk + s] = key ? value_of_key(key) : -INFINITY;
-          }
+          const bool real = q < it.nreal;
+          int32_t* oi = p.out_idx + t * p.topk;
+          float* ov = p.out_val ? p.out_val + t * p.topk : nullptr;
+          if (SN == 256) rank_row<8>(buf, cn, p.topk, real, oi, ov);
+          else if (SN == 512) rank_row<16>(buf, cn, p.topk, real, oi, ov);
+          else if (SN == 1024) rank_row<32>(buf, cn, p.topk, real, oi, ov);
+          else rank_row_smem(buf, cn, P, p.topk, real, oi, ov);
         }
       } else {
         // a piece of a split group: its candidates as they stand (unsorted, at least
@@ -896,8 +973,8 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
       pl.ctas_per_sm = 2;
     }
   }
-  if (pl.ctas_per_sm == 1) pl.eg = 2;   // one CTA per SM: two epilogue groups share its tiles
-  if (tk && (pl.cap < topk + 128 * pl.eg || pl.cap < pl.pow2)) pl.ok = false;
+  if (pl.ctas_per_sm == 1 && pl.nq >= 2) pl.eg = 2;   // one CTA per SM: two groups take turns
+  if (tk && (pl.cap < topk + 256 || pl.cap < pl.pow2)) pl.ok = false;
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
   // as many accumulator buffers (up to 4) as TMEM holds for the CTAs sharing an SM, so
   // the MMAs can run ahead of an epilogue busy cutting its candidates back
@@ -974,7 +1051,6 @@ static cudaError_t dispatch_nq(const CUtensorMap& mq, const CUtensorMap& mk, con
                                const IndexerPlan& pl, int grid, cudaStream_t st) {
   switch (pl.nq * 2 + pl.eg) {
     case 3: return launch_one<kFP8, 1, kTopk, 1>(mq, mk, prm, pl, grid, st);
-    case 4: return launch_one<kFP8, 1, kTopk, 2>(mq, mk, prm, pl, grid, st);
     case 5: return launch_one<kFP8, 2, kTopk, 1>(mq, mk, prm, pl, grid, st);
     case 6: return launch_one<kFP8, 2, kTopk, 2>(mq, mk, prm, pl, grid, st);
     default: return launch_one<kFP8, 4, kTopk, 2>(mq, mk, prm, pl, grid, st);
