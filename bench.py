@@ -46,14 +46,16 @@ WORKLOADS = {
 
 
 def make_workload(name: str, seed: int, batch: int = 0):
-    """The named workload; `batch` > 0 shrinks the sequence count of the decode batches
-    (a smaller case of the same kernel for profiler captures)."""
+    """The named workload; `batch` > 0 shrinks it for profiler captures: the sequence
+    count of a decode batch, or the tokens T = K of the prefill."""
     from deepseek_v4_sparse_dsa_gb300 import synth
     fn = {"flash_decode": synth.make_flash_decode, "pro_mtp": synth.make_pro_mtp,
           "prefill": synth.make_prefill, "fp8_chunked": synth.make_fp8_chunked}[name]
     if batch > 0:
+        if name == "prefill":
+            return fn(seed=seed, T=batch)
         if name not in ("flash_decode", "pro_mtp"):
-            raise SystemExit("--batch applies to the decode workloads only")
+            raise SystemExit("--batch applies to the decode and prefill workloads only")
         return fn(seed=seed, B=batch)
     return fn(seed=seed)
 
@@ -374,7 +376,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="flash_decode", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--batch", type=int, default=0, help="sequences of a decode workload (0: its default)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences of a decode workload, tokens of the prefill (0: the workload's own size)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
