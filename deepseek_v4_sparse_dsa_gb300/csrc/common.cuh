@@ -352,15 +352,11 @@ __device__ __forceinline__ void engine_append_multi(uint64_t* buf, size_t stride
   }
 }
 
-// hist[bin] += 1 for every lane with `take`; one shared atomic per distinct bin per warp
-// (keys of a candidate set share their leading digits, so bins are heavily contended).
-// All 32 lanes must call it together.
+// hist[bin] += 1 for every lane with `take`: one shared atomic per lane (measured
+// faster on sm_103 than aggregating equal bins with a match first, even when the keys
+// of a candidate set crowd into a few bins).  All 32 lanes must call it together.
 __device__ __forceinline__ void hist_add(uint32_t* hist, bool take, uint32_t bin) {
-  const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t active = __ballot_sync(0xFFFFFFFFu, take);
-  if (!take) return;
-  const uint32_t peers = __match_any_sync(active, bin);
-  if (lane == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+  if (take) atomicAdd(&hist[bin], 1u);
 }
 
 // Picks the digit of the current radix pass: the bin holding the `need`-th largest key,
@@ -470,22 +466,34 @@ __device__ uint64_t engine_select_global(const uint64_t* src, int n, int k, Engi
   return prefix;
 }
 
-// Writes the keys of keep[] that are nonzero and >= thr (t_ord: compare only the high
-// 32 bits against t_hi) to the front of buf, in thread order, with one prefix sum over
-// the group instead of an atomic per key; *cnt becomes their number.  Every key of buf
-// must already sit in some thread's keep[] (the writes may overwrite any slot).  Uses
-// sc->hist[0, NT/32) as scratch; ends with a group barrier.
-template <int NT, int MAXPER, bool kByOrd>
-__device__ __forceinline__ void engine_scatter(uint64_t* buf, uint32_t* cnt, const uint64_t (&keep)[MAXPER],
-                                               uint64_t thr, uint32_t t_hi, EngineScratch* sc, int tid, int bar) {
+// Histogram bin of value image o for a cut-back over [lo, lo + span): (o - lo) * mul / 2^32
+// with mul = floor(2^32 * kCutBins / span), monotone in o and below kCutBins.
+__device__ __forceinline__ uint32_t cut_bin(uint32_t o, uint32_t lo, uint32_t mul) {
+  return (uint32_t)(((uint64_t)(o - lo) * mul) >> 32);
+}
+
+// Writes the keys of keep[] that are nonzero and >= thr (kByBin: whose cut_bin is at
+// least bmin) to the front of buf, in thread order, with one prefix sum over the group
+// instead of an atomic per key; *cnt becomes their number; returns the smallest value
+// image written.  Every key of buf must already sit in some thread's keep[] (the writes
+// may overwrite any slot).  Uses sc->hist[0, 2 * NT/32) as scratch; ends with a group
+// barrier.
+template <int NT, int MAXPER, bool kByBin>
+__device__ __forceinline__ uint32_t engine_scatter(uint64_t* buf, uint32_t* cnt, const uint64_t (&keep)[MAXPER],
+                                                   uint64_t thr, uint32_t lo, uint32_t mul, uint32_t bmin,
+                                                   EngineScratch* sc, int tid, int bar) {
   constexpr int NW = NT / 32;
   const int lane = tid & 31, w = tid >> 5;
-  uint32_t mine = 0;
+  uint32_t mine = 0, omin = 0xFFFFFFFFu;
 #pragma unroll
   for (int i = 0; i < MAXPER; ++i) {
-    const bool t = kByOrd ? (keep[i] != 0ull && (uint32_t)(keep[i] >> 32) >= t_hi) : (keep[i] != 0ull && keep[i] >= thr);
+    const uint32_t o = (uint32_t)(keep[i] >> 32);
+    const bool t = kByBin ? (keep[i] != 0ull && cut_bin(o, lo, mul) >= bmin) : (keep[i] != 0ull && keep[i] >= thr);
     mine += t ? 1u : 0u;
+    if (t) omin = min(omin, o);
   }
+  for (int o = 16; o > 0; o >>= 1) omin = min(omin, __shfl_xor_sync(0xFFFFFFFFu, omin, o));
+  if (lane == 0) sc->hist[NW + w] = omin;
   uint32_t incl = mine;
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
@@ -494,26 +502,31 @@ __device__ __forceinline__ void engine_scatter(uint64_t* buf, uint32_t* cnt, con
   if (lane == 31) sc->hist[w] = incl;
   group_sync<NT>(bar);
   uint32_t off = incl - mine, total = 0;
+  omin = 0xFFFFFFFFu;
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
     const uint32_t c = sc->hist[i];
     if (i < w) off += c;
     total += c;
+    omin = min(omin, sc->hist[NW + i]);
   }
 #pragma unroll
   for (int i = 0; i < MAXPER; ++i) {
-    const bool t = kByOrd ? (keep[i] != 0ull && (uint32_t)(keep[i] >> 32) >= t_hi) : (keep[i] != 0ull && keep[i] >= thr);
+    const bool t = kByBin ? (keep[i] != 0ull && cut_bin((uint32_t)(keep[i] >> 32), lo, mul) >= bmin)
+                          : (keep[i] != 0ull && keep[i] >= thr);
     if (t) buf[off++] = keep[i];
   }
   if (tid == 0) *cnt = total;
   group_sync<NT>(bar);
+  return omin;
 }
 
 // Cheap cut-back of a candidate buffer that only has to stay a superset of its top-k:
-// finds a threshold T with at least k of the nonzero keys of buf[0, n) at or above it
-// from one 512-bin histogram of the keys' values (bins linear in the order-preserving
-// image of the value, between its smallest and largest), keeps the keys >= T packed to
-// the front (*cnt = their number) and returns T.  Returns 0 and leaves buf alone when
+// one 512-bin histogram of the keys' values (bins linear in the order-preserving image
+// of the value, between its smallest and largest) gives the bin holding the k-th key;
+// the keys in that bin and above are kept, packed to the front (*cnt = their number),
+// at least k of them, and the function returns T = (smallest kept value image) << 32,
+// a threshold at or below the k-th key.  Returns 0 and leaves buf alone when
 // the histogram cannot bring the count to `room` or less (values too concentrated, e.g.
 // ties) or there are at most k keys; the caller then selects exactly.  `bins` holds 512
 // words of shared scratch; needs n <= NT * MAXPER.
@@ -566,9 +579,10 @@ __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k
     return 0ull;
   }
   const uint64_t span = (uint64_t)(hi - lo) + 1u;
+  const uint32_t mul = (uint32_t)min(((uint64_t)kCutBins << 32) / span, (uint64_t)0xFFFFFFFFu);
 #pragma unroll
   for (int i = 0; i < MAXPER; ++i)
-    if (keep[i]) atomicAdd(&bins[(uint32_t)(((uint64_t)((uint32_t)(keep[i] >> 32) - lo) * kCutBins) / span)], 1u);
+    if (keep[i]) atomicAdd(&bins[cut_bin((uint32_t)(keep[i] >> 32), lo, mul)], 1u);
   group_sync<NT>(bar);
   // bin b* holding the k-th key from the top: thread tid scans bins
   // [kCutBins - (tid + 1) * BPT, kCutBins - tid * BPT) top down
@@ -605,9 +619,8 @@ __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k
     group_sync<NT>(bar);
     return 0ull;
   }
-  // smallest value image in bins >= b
-  const uint32_t tord = lo + (uint32_t)(((uint64_t)b * span + kCutBins - 1) / kCutBins);
-  engine_scatter<NT, MAXPER, true>(buf, cnt, keep, 0ull, tord, sc, tid, bar);
+  // keys in bins >= b stay; the threshold is the smallest value image among them
+  const uint32_t tord = engine_scatter<NT, MAXPER, true>(buf, cnt, keep, 0ull, lo, mul, b, sc, tid, bar);
   return (uint64_t)tord << 32;
 }
 
@@ -623,7 +636,7 @@ __device__ void engine_compact(uint64_t* buf, uint32_t* cnt, int n, uint64_t thr
     const int e = tid + i * NT;
     keep[i] = (e < n) ? buf[e] : 0ull;
   }
-  engine_scatter<NT, MAXPER, false>(buf, cnt, keep, thr, 0u, sc, tid, bar);
+  engine_scatter<NT, MAXPER, false>(buf, cnt, keep, thr, 0u, 0u, 0u, sc, tid, bar);
 }
 
 // Copies the keys >= thr of src[0, n) to the front of dst (capacity dcap); *cnt becomes

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kRowNT) topk_rows_kernel(const float* __restri
 }
 
 constexpr int kMergeNT = 512;       // merge: threads per row
-constexpr int kMergeKeys = 16384;   // merge: candidates held in shared memory at once
+constexpr int kMergeKeys = 24576;   // merge: candidates held in shared memory at once (two halves)
 
 // One CTA per (split group, query row): block m handles row m % nq of the (m / nq)-th
 // split group of the plan.  The row's lists (one per slice the group's tiles fall in)
