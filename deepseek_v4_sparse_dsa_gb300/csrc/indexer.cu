@@ -731,16 +731,19 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
       if (kFP8 && !paged && first < it.ntiles && it.ks + first * 128 + row < p.num_rows)
         ks_next = __ldg(p.k_scale + it.ks + first * 128 + row);
       for (int m = 0; m < niter; ++m) {
-        if (kTopk) {
+        // One group checks its buffers every CI tiles (one barrier per check), leaving
+        // room for CI tiles of appends; two groups check at every tile.
+        constexpr int CI = EG == 1 ? 2 : 1;
+        if (kTopk && m % CI == 0) {
           group_sync<NT>();
 #pragma unroll 1
           for (int q = 0; q < NQ; ++q) {
             const uint32_t cn = es->cnt[q];
-            if (cn > (uint32_t)(cap - 128 * EG)) {
+            if (cn > (uint32_t)(cap - 128 * EG * CI)) {
               // cut back to a superset of the top-k; exactly only if the histogram
               // cannot free enough room
               uint64_t* buf = ebuf + (size_t)q * cap;
-              const uint32_t room = (uint32_t)min((cap + p.topk) / 2, cap - 256 * EG);
+              const uint32_t room = (uint32_t)min((cap + p.topk) / 2, cap - 256 * EG * CI);
               uint64_t thr = engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, room, es->bins,
                                                            &es->esc, et);
               if (thr == 0ull) {
