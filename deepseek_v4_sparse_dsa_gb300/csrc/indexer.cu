@@ -93,16 +93,31 @@ struct EpiSmem {
   uint32_t bins[kCutBins];
 };
 
+// Two fp32 fused multiply-adds in one instruction (each lane rounded as fmaf).
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+
+// sum_h w[h] * relu(s[h]) in a fixed order: four interleaved partial sums p_r over
+// h = r (mod 4), then (p0 + p1) + (p2 + p3); pairs (p0, p1) and (p2, p3) advance with
+// one two-lane FMA each.
 __device__ __forceinline__ float head_sum(const uint32_t (&s)[64], const float* w) {
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  uint64_t a01 = 0ull, a23 = 0ull;
 #pragma unroll
   for (int h = 0; h < 64; h += 4) {
     const float4 wv = *reinterpret_cast<const float4*>(w + h);
-    a0 = fmaf(wv.x, fmaxf(__uint_as_float(s[h + 0]), 0.f), a0);
-    a1 = fmaf(wv.y, fmaxf(__uint_as_float(s[h + 1]), 0.f), a1);
-    a2 = fmaf(wv.z, fmaxf(__uint_as_float(s[h + 2]), 0.f), a2);
-    a3 = fmaf(wv.w, fmaxf(__uint_as_float(s[h + 3]), 0.f), a3);
+    a01 = fma2(pack2(wv.x, wv.y),
+               pack2(fmaxf(__uint_as_float(s[h + 0]), 0.f), fmaxf(__uint_as_float(s[h + 1]), 0.f)), a01);
+    a23 = fma2(pack2(wv.z, wv.w),
+               pack2(fmaxf(__uint_as_float(s[h + 2]), 0.f), fmaxf(__uint_as_float(s[h + 3]), 0.f)), a23);
   }
+  const float a0 = __uint_as_float((uint32_t)a01), a1 = __uint_as_float((uint32_t)(a01 >> 32));
+  const float a2 = __uint_as_float((uint32_t)a23), a3 = __uint_as_float((uint32_t)(a23 >> 32));
   return (a0 + a1) + (a2 + a3);
 }
 
