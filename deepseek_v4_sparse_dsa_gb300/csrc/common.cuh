@@ -394,12 +394,55 @@ __device__ __forceinline__ void pick_digit(uint32_t* hist, uint32_t* pick, uint3
 // Smallest key T such that exactly k of the distinct nonzero keys in buf[0, n) are >= T
 // (the k-th largest key, or a lower bound of it sharing all bits that decide the set);
 // 1 when there are at most k of them.  Most-significant-digit-first radix select over
-// 8-bit digits; zero slots are ignored.
+// 8-bit digits, starting at the highest byte in which the keys differ (one AND / OR
+// reduction finds it: candidates share their sign and exponent bits, and a pass over a
+// digit they all share would only pile every key into one bin); zero slots are ignored.
 template <int NT>
 __device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScratch* sc, int tid, int bar = 1) {
-  uint64_t prefix = 0, mask = 0;
+  constexpr int NW = NT / 32;
+  static_assert(5 * NW <= 256, "group size");
+  const int lane = tid & 31, w = tid >> 5;
+  uint64_t kand = ~0ull, kor = 0ull;
+  uint32_t nz = 0;
+  for (int e = tid; e < n; e += NT) {
+    const uint64_t key = buf[e];
+    if (key) {
+      kand &= key;
+      kor |= key;
+      ++nz;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    kand &= __shfl_xor_sync(0xFFFFFFFFu, kand, o);
+    kor |= __shfl_xor_sync(0xFFFFFFFFu, kor, o);
+    nz += __shfl_xor_sync(0xFFFFFFFFu, nz, o);
+  }
+  uint32_t* red = sc->hist;                         // per warp: and (2 words), or (2 words), count
+  if (lane == 0) {
+    red[5 * w + 0] = (uint32_t)kand;
+    red[5 * w + 1] = (uint32_t)(kand >> 32);
+    red[5 * w + 2] = (uint32_t)kor;
+    red[5 * w + 3] = (uint32_t)(kor >> 32);
+    red[5 * w + 4] = nz;
+  }
+  group_sync<NT>(bar);
+  kand = ~0ull;
+  kor = 0ull;
+  nz = 0;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    kand &= (uint64_t)red[5 * i] | ((uint64_t)red[5 * i + 1] << 32);
+    kor |= (uint64_t)red[5 * i + 2] | ((uint64_t)red[5 * i + 3] << 32);
+    nz += red[5 * i + 4];
+  }
+  group_sync<NT>(bar);                              // red is read before hist reuses it
+  if (nz <= (uint32_t)k) return 1ull;               // at most k keys: take them all
+  const int top = 63 - __clzll(kand ^ kor);         // highest bit in which keys differ
+  const int first = top & ~7;                       // its digit
+  uint64_t mask = first >= 56 ? 0ull : ~((1ull << (first + 8)) - 1ull);
+  uint64_t prefix = kand & mask;
   uint32_t need = (uint32_t)k;
-  for (int shift = 56; shift >= 0; shift -= 8) {
+  for (int shift = first; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += NT) sc->hist[i] = 0;
     group_sync<NT>(bar);
     for (int base = 0; base < n; base += NT) {
@@ -410,10 +453,6 @@ __device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScrat
     group_sync<NT>(bar);
     if (tid < 32) pick_digit(sc->hist, sc->pick, need, tid);   // lane l: digits 255-8l .. 248-8l
     group_sync<NT>(bar);
-    if (shift == 56 && sc->pick[3] <= (uint32_t)k) {           // at most k keys: take them all
-      group_sync<NT>(bar);
-      return 1ull;
-    }
     const uint32_t d = sc->pick[0], above = sc->pick[1], inbin = sc->pick[2];
     if (d > 255u) {                // counts did not add up: keep everything (never drops a key)
       if (tid == 0) raise_error(DSA_DEVERR_OVERFLOW | (42u << 8));
@@ -425,7 +464,7 @@ __device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScrat
     mask |= (uint64_t)0xFF << shift;
     if (inbin == need) break;      // every key with this prefix belongs to the set
   }
-  group_sync<NT>(bar);                // everyone has read pick[] before it is reused
+  group_sync<NT>(bar);             // everyone has read pick[] before it is reused
   return prefix;
 }
 
