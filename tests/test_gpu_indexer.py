@@ -157,3 +157,20 @@ def test_empty_and_degenerate_batches():
     assert np.isneginf(lg[[0, 1, 4, 5]]).all()
     assert (idx_f[[0, 1, 4, 5]] == -1).all()
     parity.assert_topk_exact(idx_f, lg, 4, val_f)
+
+
+@pytest.mark.parametrize("topk", [512, 2048])
+def test_one_long_row_over_many_slices(topk):
+    # one sequence long enough that its key tiles span every CTA's slice: the merge takes
+    # more than 32 lists per row and cuts its buffer back while collecting
+    wl = parity.make_case(121 + topk, [150000], next_n=1, block_size=64, topk=topk)
+    check_case(wl, jaccard=topk <= 1024)
+
+
+@pytest.mark.parametrize("topk", [64, 200, 2048])
+def test_many_short_rows_finished_in_one_item(topk):
+    # many short sequences: most query groups fit one CTA's slice and are ranked and
+    # written by the fused kernel itself (register sort for k <= 1024, shared memory above)
+    lens = synth.Rng(131).integers(100, 2000, 400, "lens")
+    wl = parity.make_case(131 + topk, lens, next_n=1, block_size=64, topk=topk)
+    check_case(wl, jaccard=topk <= 1024)
