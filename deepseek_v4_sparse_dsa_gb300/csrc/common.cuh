@@ -211,35 +211,11 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-// Each thread of the warp reads 64 consecutive 32-bit columns of its own TMEM lane.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  uint32_t r[64];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
-      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-        "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]),
-        "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
-        "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
-        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
-        "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// tmem_ld64 split in two, so the load of one block of columns can overlap work on the
-// previous one: tmem_ld64_issue starts the load, tmem_ld64_wait completes every load the
-// thread has issued and marks `r` as written only then (its registers are operands, so
-// the compiler cannot move their uses above the wait).
+// Each thread of the warp reads 64 consecutive 32-bit columns of its own TMEM lane, in
+// two steps so the load of one block of columns can overlap work on the previous one:
+// tmem_ld64_issue starts the load, tmem_ld64_wait completes every load the thread has
+// issued and marks `r` as written only then (its registers are operands, so the compiler
+// cannot move their uses above the wait).
 __device__ __forceinline__ void tmem_ld64_issue(uint32_t taddr, uint32_t (&r)[64]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
@@ -465,43 +441,6 @@ __device__ uint64_t engine_select(const uint64_t* buf, int n, int k, EngineScrat
     if (inbin == need) break;      // every key with this prefix belongs to the set
   }
   group_sync<NT>(bar);             // everyone has read pick[] before it is reused
-  return prefix;
-}
-
-// As engine_select, over the nonzero keys of a global-memory array (read through L2).
-// Returns 1 (take every nonzero key) when there are at most k of them.
-template <int NT>
-__device__ uint64_t engine_select_global(const uint64_t* src, int n, int k, EngineScratch* sc, int tid) {
-  uint64_t prefix = 0, mask = 0;
-  uint32_t need = (uint32_t)k;
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += NT) sc->hist[i] = 0;
-    group_sync<NT>();
-    for (int base = 0; base < n; base += 4 * NT) {
-      uint64_t key[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = base + u * NT + tid;
-        key[u] = e < n ? __ldcg(src + e) : 0ull;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        hist_add(sc->hist, key[u] != 0ull && (key[u] & mask) == prefix, (uint32_t)(key[u] >> shift) & 255u);
-    }
-    group_sync<NT>();
-    if (tid < 32) pick_digit(sc->hist, sc->pick, need, tid);
-    group_sync<NT>();
-    if (shift == 56 && sc->pick[3] <= (uint32_t)k) {
-      group_sync<NT>();
-      return 1ull;
-    }
-    const uint32_t d = sc->pick[0], above = sc->pick[1], inbin = sc->pick[2];
-    need -= above;
-    prefix |= (uint64_t)d << shift;
-    mask |= (uint64_t)0xFF << shift;
-    if (inbin == need) break;
-  }
-  group_sync<NT>();
   return prefix;
 }
 
