@@ -1,0 +1,59 @@
+"""The benchmark's roofline arithmetic (algorithmic flops and bytes per call), checked
+against closed forms for the configurations' shapes, and its JSON contract keys."""
+import numpy as np
+
+import bench
+from deepseek_v4_sparse_dsa_gb300.synth import Workload
+
+
+def _shape_only(B, next_n, lens, topk, dtype="bf16", causal=True, gather=False):
+    """A Workload carrying only what the roofline arithmetic reads (no tensors)."""
+    lens = np.asarray(lens, dtype=np.int32)
+    z = np.zeros(0, np.uint8)
+    return Workload("shape", B, next_n, lens, causal, topk, dtype, z, None, z, z, None, None, 64,
+                    kv_fp4=z if gather else None)
+
+
+def test_prefill_flops_closed_form():
+    # T = K = 16384, causal: query t sees t + 1 keys; 2 * 64 * 128 flops per visible pair
+    wl = _shape_only(1, 16384, [16384], 512)
+    T = 16384
+    assert bench.algorithmic_work(wl)["flops"] == 2 * 64 * 128 * (T * (T + 1) // 2)
+    assert abs(bench.algorithmic_work(wl)["flops"] - 2.199e12) / 2.199e12 < 1e-3
+
+
+def test_fp8_chunked_flops_closed_form():
+    # 8192 queries at positions 57344..65535 over 65536 keys
+    wl = _shape_only(1, 8192, [65536], 1024, dtype="e4m3", gather=True)
+    visible = sum(57344 + i + 1 for i in range(8192))
+    assert bench.algorithmic_work(wl)["flops"] == 2 * 64 * 128 * visible
+    assert abs(bench.algorithmic_work(wl)["flops"] - 8.246e12) / 8.246e12 < 1e-3
+    # gather: 68 B read + 256 B written + 4 B position per selected row
+    assert bench.algorithmic_work(wl)["gather_bytes"] == 8192 * 1024 * (68 + 256 + 4)
+
+
+def test_decode_bytes_read_every_key_once():
+    lens = [4096, 65536, 30000]
+    wl = _shape_only(3, 1, lens, 512)
+    w = bench.algorithmic_work(wl)
+    keys = sum(lens) * 128 * 2
+    q = 3 * 64 * 128 * 2 + 3 * 64 * 4          # bf16 q rows + fp32 head weights
+    out = 3 * 512 * 8 + 3 * 4                  # selections + context lengths
+    assert w["fused_bytes"] == keys + q + out
+    # two causal queries per sequence read the sequence's keys once
+    wl2 = _shape_only(3, 2, lens, 512)
+    assert bench.algorithmic_work(wl2)["fused_bytes"] - bench.algorithmic_work(wl)["fused_bytes"] == \
+        3 * (64 * 128 * 2 + 64 * 4) + 3 * 512 * 8
+
+
+def test_e4m3_key_scales_counted():
+    wl = _shape_only(1, 1, [1000], 64, dtype="e4m3", causal=False)
+    w = bench.algorithmic_work(wl)
+    assert w["fused_bytes"] == 1000 * 128 + 1000 * 4 + (64 * 128 + 64 * 4 + 64 * 4) + 64 * 8 + 4
+
+
+def test_workloads_and_metric_are_named():
+    assert set(bench.WORKLOADS) == {"flash_decode", "pro_mtp", "prefill", "fp8_chunked"}
+    assert bench.UNIT == "query-tokens/s"
+    peaks = bench.load_peaks()
+    assert peaks["hbm_gbs"] > 0 and peaks["bf16_tflops"] > 0 and peaks["source"] in ("measured", "fallback")
