@@ -3,9 +3,11 @@
 //  * per-translation-unit error word and wait limit (see dsa.h, dsa_device_error);
 //  * bounded mbarrier waits (time limit read from %globaltimer, never a hang);
 //  * TMA (cp.async.bulk.tensor) and tcgen05 (MMA into tensor memory) wrappers;
-//  * the ranking key of the top-k tie rule and a shared-memory top-k engine
-//    (candidate buffer + radix select + bitonic sort) used by the fused indexer,
-//    the standalone top-k and the merge of partial top-k lists.
+//  * the ranking key of the top-k tie rule and a shared-memory top-k engine (candidate
+//    buffer, histogram cut-back, radix select, prefix-sum compaction, bitonic sorts in
+//    shared memory or in one warp's registers) used by the fused indexer, the standalone
+//    top-k and the merge of partial top-k lists;
+//  * the layout of the fused call's work plan and programmatic-dependent-launch hooks.
 #pragma once
 
 #include <cstdint>

@@ -11,11 +11,13 @@
 //
 // The kernel is persistent.  In top-k mode a one-CTA plan kernel first reads the actual
 // context lengths and lays every query group's key tiles end to end, each group weighted
-// by its tiles plus a fixed per-item cost; CTA i takes the i-th of gridDim.x equal slices
-// of that line.  A group inside one slice is finished by one CTA; a group cut by slice
-// boundaries leaves one unsorted top-k list per slice that the merge kernel (topk.cu)
-// ranks.  (Logits mode, which has no workspace, walks fixed chunks with a static
-// stride.)  Warp roles (64 + 128 * EG threads):
+// by its tiles plus a fixed per-item cost.  When every group is short next to a CTA's
+// share, CTAs take whole groups longest first through an atomic counter; otherwise CTA
+// i takes the i-th of gridDim.x equal slices of that line: a group inside one slice is
+// finished by one CTA, a group cut by slice boundaries leaves one unsorted candidate
+// list per slice that the merge kernel (topk.cu) ranks.  (Logits mode, which has no
+// workspace, walks fixed chunks with a static stride.)  Warp roles (64 + 128 * EG
+// threads):
 //   warp 0     producer: walks its items, publishes their descriptors, loads each item's
 //              Q tile and streams key tiles into an S-stage ring with TMA (paged keys:
 //              one box per page, block ids read from a shared-memory window the whole
@@ -25,8 +27,9 @@
 //              epilogue group T % EG
 // Epilogue: tcgen05.ld of each query's 64 head sums, fp32 ReLU * weight head sum in a
 // fixed order, then a store of the score row (logits mode) or an insert into a per-query
-// candidate buffer in shared memory (top-k mode) that a radix select cuts back to the
-// top-k whenever it fills.  Unsplit groups get their sorted rows here.
+// candidate buffer in shared memory (top-k mode) that a histogram cut brings back to a
+// superset of the top-k whenever it fills.  Unsplit groups get their rows ranked here,
+// one warp per row.
 //
 // Every wait is bounded (see common.cuh); a timeout abandons the work, flags
 // DSA_DEVERR_TIMEOUT, waits for this CTA's own copies and MMAs, frees TMEM and returns.

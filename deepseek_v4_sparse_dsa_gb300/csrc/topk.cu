@@ -4,9 +4,9 @@
 // canonical top-k sort): larger value first, then the smaller key index; -0.0 == +0.0;
 // -inf / NaN never selected; short rows padded with -1.
 //
-// Both use the radix select, append and sort of common.cuh.  The standalone top-k reads
-// each row straight from memory (a few select passes, one collect pass); the merge ranks
-// the per-chunk lists the fused indexer kernel wrote for rows it split.
+// Both use the top-k engine of common.cuh.  The standalone top-k reads each row straight
+// from memory (a few select passes, one collect pass); the merge ranks the per-slice
+// candidate lists the fused indexer kernel wrote for the query groups it split.
 #include "common.cuh"
 #include "launch.h"
 
