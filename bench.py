@@ -398,7 +398,7 @@ def main():
     res = run_ours(args, rank, world)
     if res is not None:
         out, wl = res
-        if world == 1 or rank == 0:
+        if world == 1:                                   # the CPU baseline is an N = 1 figure
             rows, secs = oracle_sample(wl, args.cpu_baseline_seconds)
             out["cpu_baseline"] = {"value": rows / secs, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                                    "sample": f"{rows} of {wl.T} query rows (score, top-k, gather), "
