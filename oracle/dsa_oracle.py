@@ -33,6 +33,12 @@ Every function is the plain definition, written out, in float64:
 * ``e4m3_to_f64`` -- OCP E4M3 (bias 7, no infinities, S.1111.111 = NaN,
   subnormals m * 2^-9), the byte format README "DeepSeek V4 Flash on a single
   AMD MI300X" ("FP8 format") contrasts with AMD's FNUZ variant.
+* ``indexer_logits(..., k_dtype="mxfp4")`` -- the same score with the keys read
+  from a paged mxfp4 cache (nibble rows + E8M0 scale rows, the gather's layout),
+  as the fp8/fp4 logits kernel xkernels issue #27 names ("Unknown": the
+  indexer forward uses an fp8-q x fp4-k MQA-logits kernel) computes it; per
+  comment 2 ("Caveats / deferred") the packing is an encoding detail, so the
+  definition is the score over the dequantised keys.
 
 Parity pins for each function are in tests/test_oracle_pins.py.
 """
@@ -68,12 +74,15 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
 
 def dequantize(data: np.ndarray, scale, dtype: str) -> np.ndarray:
     """Storage -> float64 values.  E4M3 rows are multiplied by their fp32 row scale
-    (exactly, in float64); bf16 has no scale."""
+    (exactly, in float64); bf16 has no scale; mxfp4 rows are [.., D/2] nibble bytes
+    with [.., D/32] E8M0 scale bytes (see mxfp4_dequant)."""
     if dtype == "bf16":
         return bf16_to_f64(data)
     if dtype == "e4m3":
         v = e4m3_to_f64(data)
         return v * np.asarray(scale, dtype=np.float64)[..., None]
+    if dtype == "mxfp4":
+        return mxfp4_dequant(data, scale)
     raise ValueError(dtype)
 
 
@@ -98,11 +107,13 @@ def sequence_key_rows(b: int, L: int, block_table, block_size: int, num_rows: in
 
 def indexer_logits(q, q_scale, dtype: str, weights, k_data, k_scale, block_table,
                    block_size: int, B: int, next_n: int, context_lens, causal: bool,
-                   rows=None, width=None) -> np.ndarray:
+                   rows=None, width=None, k_dtype=None) -> np.ndarray:
     """Indexer score for the query rows ``rows`` (default: all T = B * next_n).
 
-    Returns float64 [len(rows), width] with width = max context length by
-    default; entries at masked or out-of-range keys are -inf.
+    ``dtype`` is the storage of q (and of the keys unless ``k_dtype`` says
+    otherwise: "mxfp4" keys are k_data = nibble rows [rows, D/2] with k_scale =
+    E8M0 rows [rows, D/32]).  Returns float64 [len(rows), width] with width = max
+    context length by default; entries at masked or out-of-range keys are -inf.
     """
     context_lens = np.asarray(context_lens, dtype=np.int64)
     T = B * next_n
@@ -117,7 +128,7 @@ def indexer_logits(q, q_scale, dtype: str, weights, k_data, k_scale, block_table
         if b not in key_cache:
             kr = sequence_key_rows(b, L, block_table, block_size, k_data.shape[0])
             ks = None if k_scale is None else np.asarray(k_scale)[kr]
-            key_cache = {b: dequantize(np.asarray(k_data)[kr], ks, dtype)}  # [L, D]
+            key_cache = {b: dequantize(np.asarray(k_data)[kr], ks, k_dtype or dtype)}  # [L, D]
         k = key_cache[b]
         qs = None if q_scale is None else np.asarray(q_scale)[t]
         qt = dequantize(np.asarray(q)[t], qs, dtype)                      # [H, D]

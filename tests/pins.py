@@ -347,6 +347,42 @@ def check_logits_e4m3(orc, seed=6):
     assert np.array_equal(got_p, got)
 
 
+def check_logits_mxfp4_keys(orc, seed=9):
+    """Keys read from a paged mxfp4 cache (the fp8-q x fp4-k form of the score, xkernels
+    issue #27): a hand-worked case, then the same score as over the bf16 patterns of the
+    dequantised keys."""
+    H, Dm = 2, 128
+    nib = np.full((3, Dm // 2), 0x21, np.uint8)   # every byte: even element code 1 (0.5), odd code 2 (1.0)
+    sc = np.array([[127] * 4, [128] * 4, [0xFF] * 4], np.uint8)   # scale 1, 2, and 0xFF -> 0
+    # block size 2, table [1, 0]: keys 0, 1 are pool rows 2, 3; key 2 is pool row 0
+    pool_n = np.stack([nib[2], nib[2], nib[0], nib[1]])
+    pool_s = np.stack([sc[2], sc[2], sc[0], sc[1]])
+    table = np.array([[1, 0]], np.int32)
+    qc = np.zeros((1, H, Dm), np.uint8)
+    qc[0, 0, 0::2] = 0x38                          # head 0: 1.0 on the even dims; head 1: 0
+    qs = np.ones((1, H), np.float32)
+    w = np.array([[1.0, 5.0]])
+    got = orc.indexer_logits(qc, qs, "e4m3", w, pool_n, pool_s, table, 2, 1, 1, np.array([3]), False,
+                             k_dtype="mxfp4")
+    assert np.array_equal(got, [[32.0, 64.0, 0.0]]), got   # 64 x 0.5, x 2, x 0
+    # random cache, scales in the normal range (so every dequantised key is exact in bf16)
+    r = np.random.default_rng(seed)
+    B, n, bs, nblk = 2, 3, 4, 6
+    lens = np.array([13, 7])
+    pool_n = r.integers(0, 256, (nblk * bs, Dm // 2)).astype(np.uint8)
+    pool_s = r.integers(120, 135, (nblk * bs, Dm // 32)).astype(np.uint8)
+    table = np.array([[5, 0, 3, 1], [2, 4, -1, -1]], np.int32)
+    qc = r.integers(0, 256, (B * n, H, Dm)).astype(np.uint8)
+    qc[(qc & 0x7F) == 0x7F] = 0x30                 # no NaN codes
+    qs = (r.random((B * n, H)) + 0.5).astype(np.float32)
+    w = r.random((B * n, H))
+    got = orc.indexer_logits(qc, qs, "e4m3", w, pool_n, pool_s, table, bs, B, n, lens, True, k_dtype="mxfp4")
+    kb = f64_to_bf16_exact(orc.mxfp4_dequant(pool_n, pool_s))
+    want = orc.indexer_logits(qc, qs, "e4m3", w, kb, None, table, bs, B, n, lens, True, k_dtype="bf16")
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.isfinite(got[0]), np.arange(13) <= 13 - 3)   # causal window, row 0
+
+
 # --------------------------------------------------------------------------- top-k
 
 def check_topk_hand(orc):
@@ -393,5 +429,6 @@ ALL_CHECKS = [
     check_bf16_decode, check_e4m3_decode, check_bf16_rounding, check_e8m0, check_e2m1,
     check_mxfp4_hand_rows, check_mxfp4_gather_hand, check_gather_invariant,
     check_logits_hand, check_logits_plain_matmul, check_logits_special,
-    check_logits_invariances, check_logits_e4m3, check_topk_hand, check_topk_bruteforce,
+    check_logits_invariances, check_logits_e4m3, check_logits_mxfp4_keys, check_topk_hand,
+    check_topk_bruteforce,
 ]

@@ -37,6 +37,10 @@ MUTANTS = {
     "padded_not_zero": ("live = sel >= 0", "live = sel >= -1"),
     "gather_seq_row": ("[b[live], pos // block_size]", "[0 * b[live], pos // block_size]"),
     "gather_offset": ("off = pos % block_size", "off = pos // block_size % block_size"),
+    "key_dtype_ignored": ("dequantize(np.asarray(k_data)[kr], ks, k_dtype or dtype)",
+                          "dequantize(np.asarray(k_data)[kr], ks, dtype)"),
+    "mxfp4_key_scale_ignored": ("return mxfp4_dequant(data, scale)",
+                                "return mxfp4_dequant(data, np.full_like(scale, 127))"),
 }
 
 
