@@ -125,6 +125,12 @@ def test_host_side_rejections_launch_nothing(lib):
         == dsa.DSA_ERR_INVALID_ARG
     assert _status(dsa.mxfp4_paged_gather, FAKE, FAKE, 8, 0, 128, FAKE, 8, FAKE, 1, 1, 4, FAKE, s) \
         == dsa.DSA_ERR_INVALID_ARG
+    # a batch whose work-plan line (key tiles + per-item costs of every query group) would
+    # not fit the plan's 32-bit positions is refused, not wrapped around
+    huge = dsa.make_queries(1000, 1, FAKE, 2**31 - 1, True)
+    assert dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, huge, 512) == 0
+    assert _status(dsa.dsa_indexer_logits_topk, FAKE, None, dsa.DSA_BF16, FAKE, 64, 128, pkeys, huge, 512, FAKE,
+                   None, FAKE, 1 << 40, s) == dsa.DSA_ERR_UNSUPPORTED
     # empty problems are valid no-ops
     assert _status(dsa.mxfp4_paged_gather, None, None, 0, 64, 128, None, 0, None, 0, 1, 512, None, s) == dsa.DSA_OK
     assert dsa.dsa_launch_count() == before
