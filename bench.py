@@ -2,9 +2,12 @@
 
 One step = the whole path over one batch: the fused indexer score + top-k
 (dsa_indexer_logits_topk) followed by the paged mxfp4 gather of the selected rows
-(mxfp4_paged_gather).  Default workload: the Flash decode batch (64 sequences, one
-query token each, context lengths uniform in [4096, 65536], paged bf16 keys,
-top-512, gather of 512 rows per query).
+(mxfp4_paged_gather).  Headline workload (`value`, `roofline`, `e2e`): the FP8
+long-context chunked prefill, the largest configuration that fits one GPU (8192 E4M3
+queries at positions 57344..65535 over 65536 E4M3 keys, causal, top-1024, then the
+gather of all 8,388,608 selected rows).  The same JSON line carries one sub-record per
+other configuration (tiny, Flash decode, Pro decode MTP, 16K prefill) with its fused
+and gather times and its own roofline fraction, each from its own timed loop.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -32,31 +35,35 @@ if ROOT not in sys.path:
 METRIC = "indexer query-tokens/s (logits+top-k), gather GB/s; % of roofline, 1×GB300"
 UNIT = "query-tokens/s"
 L2_BYTES = 129 * 2**20
+HEADLINE = "fp8_chunked"
 
 WORKLOADS = {
+    "tiny": dict(desc="1 seq, 64 queries at 1984..2047 over 2048 contiguous bf16 keys, causal, top-512, "
+                      "mxfp4 gather of 512 rows/query (5% padded)", seed=1, bound="tensor"),
     "flash_decode": dict(desc="64 seq x 1 query, L~U[4096,65536], paged bf16 keys bs=64, top-512, "
-                              "mxfp4 gather of 512 rows/query", seed=2),
+                              "mxfp4 gather of 512 rows/query", seed=2, bound="hbm"),
     "pro_mtp": dict(desc="32 seq x 2 queries (causal), L~U[32768,131072], paged bf16 keys bs=64, "
-                         "top-1024, mxfp4 gather of 1024 rows/query", seed=3),
+                         "top-1024, mxfp4 gather of 1024 rows/query (2% padded)", seed=3, bound="hbm"),
     "prefill": dict(desc="1 seq, T=K=16384, causal, contiguous bf16 keys, fused top-512 (no gather)",
-                    seed=4),
+                    seed=4, bound="tensor"),
     "fp8_chunked": dict(desc="1 seq, 8192 E4M3 queries at 57344..65535 over 65536 E4M3 keys, causal, "
-                             "top-1024, mxfp4 gather of every selection", seed=5),
+                             "top-1024, mxfp4 gather of every selection", seed=5, bound="tensor"),
 }
 
 
 def make_workload(name: str, seed: int, batch: int = 0):
     """The named workload; `batch` > 0 shrinks it for profiler captures: the sequence
-    count of a decode batch, or the tokens T = K of the prefill."""
+    count of a decode batch, the tokens T = K of the prefill, or the query rows of the
+    FP8 chunked prefill (the last `batch` positions before 65536)."""
     from deepseek_v4_sparse_dsa_gb300 import synth
-    fn = {"flash_decode": synth.make_flash_decode, "pro_mtp": synth.make_pro_mtp,
+    fn = {"tiny": synth.make_tiny, "flash_decode": synth.make_flash_decode, "pro_mtp": synth.make_pro_mtp,
           "prefill": synth.make_prefill, "fp8_chunked": synth.make_fp8_chunked}[name]
     if batch > 0:
-        if name == "prefill":
+        if name in ("prefill", "fp8_chunked"):
             return fn(seed=seed, T=batch)
-        if name not in ("flash_decode", "pro_mtp"):
-            raise SystemExit("--batch applies to the decode and prefill workloads only")
-        return fn(seed=seed, B=batch)
+        if name in ("flash_decode", "pro_mtp"):
+            return fn(seed=seed, B=batch)
+        raise SystemExit("--batch does not apply to the tiny workload")
     return fn(seed=seed)
 
 
@@ -73,15 +80,17 @@ def load_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("common.cuh", "indexer.cu", "topk.cu", "gather.cu"):
-        with open(os.path.join(ROOT, "deepseek_v4_sparse_dsa_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "deepseek_v4_sparse_dsa_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the fused call from a committed ncu summary, if it was
-    taken on the current kernel sources."""
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if it
+    was taken on the current kernel sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -108,6 +117,47 @@ def algorithmic_work(wl):
     gather_rows = T * k
     gather_bytes = gather_rows * (68 + 256) + gather_rows * 4
     return dict(fused_bytes=fused_bytes, flops=flops, gather_bytes=gather_bytes)
+
+
+def roofline_peak(bound: str, dtype: str, peaks):
+    """Peak of the fused call's bound: measured HBM copy bandwidth, or the measured
+    sustained bf16 dense rate (times 2 for E4M3, the nominal fp8 : bf16 ratio)."""
+    if bound == "hbm":
+        return peaks["hbm_gbs"], "GB/s"
+    return peaks["bf16_tflops_sustained"] * (2.0 if dtype == "e4m3" else 1.0), "TFLOP/s"
+
+
+def roofline(bound: str, wl, work, fused_ms: float, peaks):
+    peak, unit = roofline_peak(bound, wl.dtype, peaks)
+    if bound == "hbm":
+        achieved = work["fused_bytes"] / (fused_ms * 1e-3) / 1e9
+    else:
+        achieved = work["flops"] / (fused_ms * 1e-3) / 1e12
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "peak_source": f"{peaks['source']}: " + ("hbm_gbs" if bound == "hbm" else
+                                                     "bf16_tflops_sustained" + (" x 2 (fp8)" if wl.dtype == "e4m3"
+                                                                                else ""))}
+
+
+def l2_note(wl, work) -> str:
+    """How the timed steps avoid re-reading the previous step's data from the 129 MB L2."""
+    if work["fused_bytes"] - wl.T * wl.topk * 8 > L2_BYTES:     # inputs only, not the selection
+        return "inputs larger than L2"
+    out = wl.T * wl.topk * 256 if wl.kv_fp4 is not None else 0
+    if out > L2_BYTES:
+        return f"L2 flushed every step by the gather's {out / 2**30:.1f} GiB output write"
+    return "inputs fit in L2, not flushed (latency-bound parity case)"
+
+
+def config_of(name: str, wl, batch: int, world: int):
+    """The `config` object of the JSON line (identical for both arms)."""
+    info = WORKLOADS[name]
+    work = algorithmic_work(wl)
+    return {"workload": name + (f"_b{batch}" if batch else ""), "desc": info["desc"], "B": wl.B,
+            "next_n": wl.next_n, "topk": wl.topk, "dtype": wl.dtype, "sum_context": int(wl.context_lens.sum()),
+            "seed": info["seed"],
+            "l2": l2_note(wl, work),
+            "parallelism": f"replicas x{world}"}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -167,30 +217,118 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our arm
 
+class Runner:
+    """One workload resident on the device and its step (fused call, then the gather)."""
+
+    def __init__(self, wl, dev, stream):
+        import torch
+
+        from deepseek_v4_sparse_dsa_gb300 import dsa
+        from deepseek_v4_sparse_dsa_gb300.device import DeviceBatch
+        self.torch, self.dsa = torch, dsa
+        self.wl, self.dev, self.stream = wl, dev, stream
+        self.db = DeviceBatch.from_workload(wl, dev)
+        T, k = wl.T, wl.topk
+        self.has_gather = wl.kv_fp4 is not None
+        self.ws = self.db.workspace(dsa.DSA_OP_LOGITS_TOPK, k)
+        self.idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.gout = torch.empty((T, k, 128), dtype=torch.int16, device=dev) if self.has_gather else None
+        # Configurations with padded slots gather a copy of the selection with their seeded
+        # fraction of slots set to -1 (made once from the first fused result, outside any
+        # timed region; the selection is the same at every step).
+        self.sel = self.idx
+        if self.has_gather and wl.gather_pad_frac > 0:
+            from deepseek_v4_sparse_dsa_gb300 import synth
+            m = synth.pad_sel_pos(np.zeros((T, k), np.int32), wl.gather_pad_frac, wl.seed) < 0
+            self.fused()
+            torch.cuda.synchronize(dev)
+            self.sel = self.idx.clone().masked_fill_(torch.from_numpy(m).to(dev), -1)
+
+    def fused(self):
+        self.db.logits_topk(self.wl.topk, ws=self.ws, out_idx=self.idx, with_values=False, stream=self.stream)
+
+    def gather(self):
+        if self.has_gather:
+            self.db.gather(self.sel, out=self.gout, stream=self.stream)
+
+    def step(self):
+        self.fused()
+        self.gather()
+
+    def timed(self, steps: int, warm_s: float):
+        """Mean device ms of the fused call and of the gather over `steps` steps (CUDA
+        events on the launching stream), after a warm loop of about `warm_s` seconds;
+        also the whole region's ms per step and the library's launches inside it."""
+        torch, dev = self.torch, self.dev
+        for _ in range(3):
+            self.step()
+        t_end = time.time() + warm_s
+        while time.time() < t_end:
+            self.step()
+            torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        launches0 = self.dsa.dsa_launch_count()
+        t0.record(self.stream)
+        for i in range(steps):
+            ev[i][0].record(self.stream)
+            self.fused()
+            ev[i][1].record(self.stream)
+            self.gather()
+            ev[i][2].record(self.stream)
+        t1.record(self.stream)
+        torch.cuda.synchronize(dev)
+        launches = self.dsa.dsa_launch_count() - launches0
+        assert self.dsa.dsa_device_error(self.stream) == 0
+        fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        gather_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) if self.has_gather else 0.0
+        return fused_ms, gather_ms, t0.elapsed_time(t1) / steps, launches
+
+
+def sub_record(name: str, dev, stream, peaks, seconds: float):
+    """Fused and gather times of one more configuration, with its roofline fraction."""
+    info = WORKLOADS[name]
+    wl = make_workload(name, info["seed"])
+    r = Runner(wl, dev, stream)
+    fused_ms, gather_ms, _, _ = r.timed(3, 0.2)
+    steps = int(min(400, max(10, seconds * 1e3 / max(fused_ms + gather_ms, 1e-3))))
+    fused_ms, gather_ms, step_ms, launches = r.timed(steps, 0.3)
+    work = algorithmic_work(wl)
+    rec = {"workload": name, "desc": info["desc"], "T": wl.T, "topk": wl.topk, "dtype": wl.dtype,
+           "steps": steps, "ms_per_step": step_ms, "fused_ms": fused_ms, "gather_ms": gather_ms,
+           "indexer_qtok_s": wl.T / (fused_ms * 1e-3), "value": wl.T / (step_ms * 1e-3),
+           "work": work, "roofline": roofline(info["bound"], wl, work, fused_ms, peaks),
+           "gpu_launches": int(launches),
+           "l2": config_of(name, wl, 0, 1)["l2"]}
+    if r.has_gather:
+        gbps = work["gather_bytes"] / (gather_ms * 1e-3) / 1e9
+        rec["gather_gbps"] = gbps
+        rec["gather_frac_hbm"] = gbps / peaks["hbm_gbs"]
+    del r
+    import torch
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args, rank, world):
     import torch
 
     from deepseek_v4_sparse_dsa_gb300 import dsa
-    from deepseek_v4_sparse_dsa_gb300.device import DeviceBatch
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     dsa.load()
     info = WORKLOADS[args.workload]
     wl = make_workload(args.workload, info["seed"] + rank, args.batch)
-    db = DeviceBatch.from_workload(wl, dev)
     stream = torch.cuda.current_stream(dev)
     T, k = wl.T, wl.topk
-    has_gather = wl.kv_fp4 is not None
-    ws = db.workspace(dsa.DSA_OP_LOGITS_TOPK, k)
-    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-    gout = torch.empty((T, k, 128), dtype=torch.int16, device=dev) if has_gather else None
+    run = Runner(wl, dev, stream)
+    db = run.db
     work = algorithmic_work(wl)
-
-    def step():
-        db.logits_topk(k, ws=ws, out_idx=idx, with_values=False, stream=stream)
-        if has_gather:
-            db.gather(idx, out=gout, stream=stream)
+    peaks = load_peaks()
 
     def barrier():
         if world > 1:
@@ -200,34 +338,10 @@ def run_ours(args, rank, world):
     sampler = ClockSampler(dev.index)
     sampler.start()
     for _ in range(args.warmup):
-        step()
-    # keep the GPU busy for ~1 s before the timed region so clocks settle and get sampled
-    t_end = time.time() + 1.0
-    while time.time() < t_end:
-        step()
-        torch.cuda.synchronize(dev)
+        run.step()
     barrier()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    launches0 = dsa.dsa_launch_count()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        db.logits_topk(k, ws=ws, out_idx=idx, with_values=False, stream=stream)
-        ev[i][1].record(stream)
-        if has_gather:
-            db.gather(idx, out=gout, stream=stream)
-        ev[i][2].record(stream)
-    t1.record(stream)
+    fused_ms, gather_ms, ms_local, launches = run.timed(args.steps, 1.0)
     barrier()
-    launches = dsa.dsa_launch_count() - launches0
-    clocks = sampler.stop()
-    assert dsa.dsa_device_error(stream) == 0
-    total_ms = t0.elapsed_time(t1)
-    fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    gather_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev) if has_gather else 0.0
 
     # end to end through the public API: pinned host inputs in, results back to pinned host
     h_q = db.q.cpu().pin_memory()
@@ -236,9 +350,9 @@ def run_ours(args, rank, world):
     h_lens = db.context_lens.cpu().pin_memory()
     h_bt = db.block_table.cpu().pin_memory() if db.block_table is not None else None
     h_idx = torch.empty((T, k), dtype=torch.int32).pin_memory()
-    h_out = torch.empty((T, k, 128), dtype=torch.int16).pin_memory() if has_gather else None
+    h_out = torch.empty((T, k, 128), dtype=torch.int16).pin_memory() if run.has_gather else None
     h2d = sum(x.numel() * x.element_size() for x in (h_q, h_w, h_qs, h_lens, h_bt) if x is not None)
-    d2h = h_idx.numel() * 4 + (h_out.numel() * 2 if has_gather else 0)
+    d2h = h_idx.numel() * 4 + (h_out.numel() * 2 if run.has_gather else 0)
 
     def e2e_step():
         db.q.copy_(h_q, non_blocking=True)
@@ -248,64 +362,68 @@ def run_ours(args, rank, world):
         db.context_lens.copy_(h_lens, non_blocking=True)
         if h_bt is not None:
             db.block_table.copy_(h_bt, non_blocking=True)
-        step()
-        h_idx.copy_(idx, non_blocking=True)
-        if has_gather:
-            h_out.copy_(gout, non_blocking=True)
+        run.step()
+        h_idx.copy_(run.idx, non_blocking=True)
+        if run.has_gather:
+            h_out.copy_(run.gout, non_blocking=True)
 
-    for _ in range(max(3, args.warmup)):
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(3):
         e2e_step()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(e2e_steps):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    local = torch.tensor([total_ms / args.steps, e2e_ms], dtype=torch.float64, device=dev)
+    local = torch.tensor([ms_local, e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
         torch.distributed.all_reduce(local, op=torch.distributed.ReduceOp.MAX)
     ms_step, e2e_ms = float(local[0]), float(local[1])
+
+    subs = []
+    if rank == 0 and world == 1 and not args.batch and args.sub:
+        del run, db
+        torch.cuda.empty_cache()
+        for name in WORKLOADS:
+            if name != args.workload:
+                subs.append(sub_record(name, dev, stream, peaks, args.sub_seconds))
+    clocks = sampler.stop()
     if rank != 0:
         return None
 
-    peaks = load_peaks()
-    bound = "tensor" if args.workload in ("prefill", "fp8_chunked") else "hbm"
-    if bound == "hbm":
-        achieved = work["fused_bytes"] / (fused_ms * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
-    else:
-        achieved = work["flops"] / (fused_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"] * (2.0 if wl.dtype == "e4m3" else 1.0)
-        unit = "TFLOP/s"
     out = {
         "metric": METRIC, "value": T * world / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if wl.dtype == "e4m3" else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded SplitMix64 generator; no dataset or weights)",
-        "config": {"workload": args.workload + (f"_b{wl.B}" if args.batch else ""), "desc": info["desc"], "B": wl.B, "next_n": wl.next_n,
-                   "topk": k, "sum_context": int(wl.context_lens.sum()), "seed": info["seed"],
-                   "l2": "inputs larger than L2" if work["fused_bytes"] > L2_BYTES else "L2 not flushed",
-                   "parallelism": f"replicas x{world}"},
+        "config": config_of(args.workload, wl, args.batch, world),
         "indexer_qtok_s": T / (fused_ms * 1e-3),
         "fused_ms": fused_ms,
         "gather_ms": gather_ms,
-        "gather_gbps": (work["gather_bytes"] / (gather_ms * 1e-3) / 1e9) if has_gather else None,
+        "work": work,
+        "gather_gbps": (work["gather_bytes"] / (gather_ms * 1e-3) / 1e9) if run_has_gather(wl) else None,
         "gather_frac_hbm": (work["gather_bytes"] / (gather_ms * 1e-3) / 1e9 / peaks["hbm_gbs"])
-        if has_gather else None,
-        "roofline": {"kernel": "dsa_indexer_logits_topk (indexer_kernel + merge_kernel)", "bound": bound,
-                     "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "peak_source": peaks["source"], "traffic": recorded_traffic(args.workload)},
+        if run_has_gather(wl) else None,
+        "roofline": dict(kernel="dsa_indexer_logits_topk (plan_kernel + indexer_kernel + merge_kernel)",
+                         **roofline(info["bound"], wl, work, fused_ms, peaks),
+                         traffic=recorded_traffic(args.workload)),
         "gpu_launches": int(launches),
         "clocks": clocks,
         "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": e2e_steps},
     }
+    if subs:
+        out["configs"] = subs
     return out, wl
+
+
+def run_has_gather(wl) -> bool:
+    return wl.kv_fp4 is not None
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -362,8 +480,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.T * statistics.mean(per_step),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded SplitMix64 generator; no dataset or weights)",
-        "config": {"workload": args.workload + (f"_b{wl.B}" if args.batch else ""), "desc": info["desc"], "B": wl.B, "next_n": wl.next_n,
-                   "topk": wl.topk},
+        "config": config_of(args.workload, wl, args.batch, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -373,12 +490,15 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="flash_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch", type=int, default=0,
-                    help="sequences of a decode workload, tokens of the prefill (0: the workload's own size)")
+                    help="sequences of a decode workload, query rows of a prefill (0: the workload's own size)")
+    ap.add_argument("--no-sub", dest="sub", action="store_false",
+                    help="skip the sub-records of the other configurations")
+    ap.add_argument("--sub-seconds", type=float, default=0.5, help="timed seconds per sub-record")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

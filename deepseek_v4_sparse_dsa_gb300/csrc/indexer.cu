@@ -756,8 +756,8 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
           group_sync<NT>();
 #pragma unroll 1
           for (int q = 0; q < NQ; ++q) {
-            const uint32_t cn = es->cnt[q];
-            if (cn > (uint32_t)(cap - 128 * EG * CI)) {
+            const uint32_t cn = min(es->cnt[q], (uint32_t)cap);   // (a count past cap only after
+            if (cn > (uint32_t)(cap - 128 * EG * CI)) {              //  a flagged overflow)
               // cut back to a superset of the top-k; exactly only if the histogram
               // cannot free enough room
               uint64_t* buf = ebuf + (size_t)q * cap;
@@ -851,7 +851,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         group_sync<NT>();
 #pragma unroll 1
         for (int q = 0; q < NQ; ++q) {
-          uint32_t cn = es->cnt[q];
+          uint32_t cn = min(es->cnt[q], (uint32_t)cap);
           uint64_t* buf = ebuf + (size_t)q * cap;
           if (cn > (uint32_t)SN) {
             engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, (uint32_t)SN, es->bins, &es->esc, et);
@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         group_sync<NT>();
         for (int q = ew; q < NQ; q += 4 * EG) {
           uint64_t* buf = ebuf + (size_t)q * cap;
-          const int cn = (int)es->cnt[q];
+          const int cn = min((int)es->cnt[q], cap);
           const int64_t t = it.t0 + q;
           const bool real = q < it.nreal;
           int32_t* oi = p.out_idx + t * p.topk;
@@ -881,7 +881,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         // slot; the merge kernel ranks the group's lists
         group_sync<NT>();
         for (int q = 0; q < it.nreal; ++q) {
-          const int cn = (int)es->cnt[q];
+          const int cn = min((int)es->cnt[q], cap);
           const size_t l = (size_t)it.slot * NQ + q;
           const uint64_t* buf = ebuf + (size_t)q * cap;
           for (int s = et; s < cn; s += NT) p.partial[l * cap + s] = buf[s];

@@ -248,6 +248,10 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
       const ulonglong2 x = out2[f];
       r += (x.x > key) + (x.y > key);
     }
+    if (r >= topk) {                            // only if the lists held equal keys (stale lists
+      raise_error(DSA_DEVERR_OVERFLOW | (33u << 8));   // after an abandoned call): never write
+      continue;                                 // past the row
+    }
     out_idx[t * topk + r] = index_of_key(key);
     if (out_val) out_val[t * topk + r] = value_of_key(key);
   }

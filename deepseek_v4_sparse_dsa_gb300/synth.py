@@ -124,14 +124,27 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 def normal_bf16(rng: Rng, shape, stream: str) -> np.ndarray:
     out = np.empty(shape, dtype=np.uint16)
     flat = out.reshape(-1)
-    tmp = np.empty(max(1, min(flat.size, 2 * _CHUNK)), dtype=np.float32)
-    # Draw in slices so multi-GB key pools never hold a float64 copy.
-    step = tmp.size
-    for s0 in range(0, flat.size, step):
+    # Draw in slices so multi-GB key pools never hold a float64 copy.  Every slice has
+    # its own named stream, so the slices are independent and are drawn by a few
+    # threads at once (numpy releases the GIL in the transcendental functions); the
+    # values do not depend on the thread count.
+    step = max(1, min(flat.size, 2 * _CHUNK))
+    starts = list(range(0, flat.size, step))
+
+    def draw(s0):
         m = min(step, flat.size - s0)
-        buf = tmp[:m]
+        buf = np.empty(m, dtype=np.float32)
         rng.normal_into(buf, f"{stream}@{s0}")
         flat[s0:s0 + m] = f32_to_bf16_bits(buf)
+
+    if len(starts) <= 1:
+        for s0 in starts:
+            draw(s0)
+    else:
+        import concurrent.futures as cf
+        import os
+        with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1, len(starts))) as ex:
+            list(ex.map(draw, starts))
     return out
 
 

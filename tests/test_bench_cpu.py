@@ -53,7 +53,29 @@ def test_e4m3_key_scales_counted():
 
 
 def test_workloads_and_metric_are_named():
-    assert set(bench.WORKLOADS) == {"flash_decode", "pro_mtp", "prefill", "fp8_chunked"}
+    assert set(bench.WORKLOADS) == {"tiny", "flash_decode", "pro_mtp", "prefill", "fp8_chunked"}
+    assert bench.HEADLINE == "fp8_chunked"       # the largest configuration that fits one GPU
     assert bench.UNIT == "query-tokens/s"
     peaks = bench.load_peaks()
     assert peaks["hbm_gbs"] > 0 and peaks["bf16_tflops"] > 0 and peaks["source"] in ("measured", "fallback")
+
+
+def test_roofline_fraction_recomputes_from_the_record():
+    # a record's frac is its algorithmic work / its own ms / the peak it names
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1500.0, "source": "measured"}
+    wl = _shape_only(1, 8192, [65536], 1024, dtype="e4m3", gather=True)
+    w = bench.algorithmic_work(wl)
+    r = bench.roofline("tensor", wl, w, 4.0, peaks)
+    assert r["peak"] == 3000.0 and r["unit"] == "TFLOP/s"
+    assert abs(r["frac"] - w["flops"] / 4e-3 / 1e12 / 3000.0) < 1e-12
+    wl2 = _shape_only(4, 1, [5000, 6000, 7000, 8000], 512)
+    w2 = bench.algorithmic_work(wl2)
+    r2 = bench.roofline("hbm", wl2, w2, 0.01, peaks)
+    assert r2["unit"] == "GB/s" and abs(r2["frac"] - w2["fused_bytes"] / 1e-5 / 1e9 / 6000.0) < 1e-12
+
+
+def test_config_is_shared_by_both_arms():
+    wl = _shape_only(1, 8192, [65536], 1024, dtype="e4m3", gather=True)
+    c = bench.config_of("fp8_chunked", wl, 0, 1)
+    assert c["workload"] == "fp8_chunked" and c["topk"] == 1024 and c["dtype"] == "e4m3"
+    assert "gather" in c["l2"]                   # the 2 GiB output write flushes L2 every step
