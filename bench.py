@@ -451,10 +451,10 @@ def oracle_sample(wl, budget_s: float, min_rows: int = 1):
 
 
 def cpu_cores() -> int:
-    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
-        if os.environ.get(var):
-            return int(os.environ[var])
-    return os.cpu_count() or 1
+    """Worker threads the C++ oracle runs on (every hardware thread unless
+    DSA_ORACLE_THREADS says otherwise)."""
+    from oracle import dsa_oracle as orc
+    return orc.threads_used()
 
 
 def run_reference(args, rank, world):

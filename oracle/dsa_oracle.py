@@ -1,240 +1,252 @@
-"""CPU oracle for the DeepSeek-V4 DSA indexer hot path -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle of the DeepSeek-V4 DSA indexer hot path -- TEST INFRASTRUCTURE ONLY.
 
-Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
-this module.  The library never calls it and shares no code with it: no
-kernels, headers, helpers, tables or constants.  It takes plain numpy arrays
-(raw bf16 bits, E4M3 codes, mxfp4 bytes) and decodes them itself.
+The oracle itself is plain, slow C++ (oracle/dsa_oracle.cpp: scalar float64 loops in
+the order the problem states each step, std::thread over independent rows).  This
+module only builds that file with the host C++ compiler (once, into oracle/_build/),
+loads it with ctypes, and marshals numpy arrays in and out: it does no arithmetic of
+its own.  Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+import it; the CUDA library never does, and shares no code with it.
 
-Every function is the plain definition, written out, in float64:
+Functions (same names and arguments as the float64 numpy cross-check in
+dsa_oracle_np.py):
 
-* ``indexer_logits`` -- the DSA indexer score of xkernels issue #27
-  ("DSA indexer + attention: validate/provide gfx942 forward path", comment 2
-  "What shipped"): logits[t, j] = sum_h weights[t, h] * relu(q[t, h, :] . k[j, :]),
-  with q [T, H, D], one shared MQA key k [K, D], per-head weights and an
-  optional per-query causal window.  The causal window is read as: query i of
-  sequence b sits at absolute position p = L_b - next_n + i and sees key j iff
-  j <= p (non-causal: j < L_b).  Masked keys get -inf (the same comment shows
-  a -inf literal as the masked value).  One library matmul per query forms the
-  [H, L] dot products; ReLU, the weighted head sum and the mask follow the
-  formula term by term.
-* ``topk_select`` -- the per-query top-k (top-512 Flash / top-1024 Pro, xkernels
-  issue #27 "Context") under the deterministic tie rule: larger value first,
-  then smaller index (the "canonical top-512 sort" / top-k tie-break overlays
-  of README "DeepSeek V4 Flash on a single AMD MI300X", overlay table).  -0.0
-  and +0.0 are one value; -inf is never selected; short rows pad with -1.
-* ``e2m1_value`` / ``e8m0_scale`` / ``mxfp4_paged_gather`` -- the paged mxfp4
-  gather of xkernels issue #28 ("DeepSeek-V4 serving support -- tracking",
-  comment 2 "What it does"): E2M1 nibbles, one E8M0 scale 2^(b-127) per 32
-  elements with 0xFF meaning 0, positions read through a block table,
-  dequantised to bf16, padded slots (sel_pos < 0) -> zero row.  The E2M1 value
-  set {0, 0.5, 1, 1.5, 2, 3, 4, 6} is the OCP Microscaling v1.0 definition; the
-  oracle decodes by table (the GPU decodes arithmetically).  The low nibble of
-  byte i holds element 2i.
-* ``e4m3_to_f64`` -- OCP E4M3 (bias 7, no infinities, S.1111.111 = NaN,
-  subnormals m * 2^-9), the byte format README "DeepSeek V4 Flash on a single
-  AMD MI300X" ("FP8 format") contrasts with AMD's FNUZ variant.
-* ``indexer_logits(..., k_dtype="mxfp4")`` -- the same score with the keys read
-  from a paged mxfp4 cache (nibble rows + E8M0 scale rows, the gather's layout),
-  as the fp8/fp4 logits kernel xkernels issue #27 names ("Unknown": the
-  indexer forward uses an fp8-q x fp4-k MQA-logits kernel) computes it; per
-  comment 2 ("Caveats / deferred") the packing is an encoding detail, so the
-  definition is the score over the dequantised keys.
+* ``indexer_logits`` -- the indexer score of xkernels issue #27 "DSA indexer +
+  attention: validate/provide gfx942 forward path", comment 2 "What shipped";
+* ``topk_select`` -- the per-query top-k under the canonical tie rule (README
+  "DeepSeek V4 Flash on a single AMD MI300X", overlay table);
+* ``mxfp4_paged_gather``, ``mxfp4_dequant``, ``e2m1_value``, ``e8m0_scale``,
+  ``f64_to_bf16_bits`` -- the paged mxfp4 gather of xkernels issue #28
+  "DeepSeek-V4 serving support -- tracking", comment 2 "What it does";
+* ``bf16_to_f64``, ``e4m3_to_f64`` -- the storage decoders.
 
-Parity pins for each function are in tests/test_oracle_pins.py.
+The worker count is ``DSA_ORACLE_THREADS`` (default: every hardware thread).
 """
 from __future__ import annotations
 
+import ctypes
+import os
+import subprocess
+import threading
+from ctypes import POINTER, c_double, c_int, c_int32, c_int64, c_uint8, c_uint16, c_void_p
+
 import numpy as np
 
-NEG_INF = float("-inf")
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "dsa_oracle.cpp")
+LIB = os.path.join(HERE, "_build", "libdsa_oracle.so")
+CXXFLAGS = ["-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-ffp-contract=off"]
 
-# ----------------------------------------------------------------------------- decoding
-
-def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
-    """bf16 is the upper half of an IEEE binary32: widen the bits, reinterpret."""
-    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    with np.errstate(invalid="ignore"):
-        return u.view(np.float32).astype(np.float64)
+_KIND = {"bf16": 0, "e4m3": 1, "mxfp4": 2}
+_lock = threading.RLock()
 
 
-def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
-    """OCP E4M3: sign bit 7, exponent bits 6..3 (bias 7), mantissa bits 2..0.
-
-    e == 0: (-1)^s * (m / 8) * 2^-6 (subnormal); e == 15 and m == 7: NaN;
-    otherwise (-1)^s * (1 + m / 8) * 2^(e - 7).
-    """
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
-    s = (c >> 7) & 1
-    e = (c >> 3) & 0xF
-    m = c & 7
-    mag = np.where(e == 0, (m / 8.0) * 2.0**-6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
-    val = np.where(s == 1, -mag, mag)
-    return np.where((e == 15) & (m == 7), np.nan, val)
-
-
-def dequantize(data: np.ndarray, scale, dtype: str) -> np.ndarray:
-    """Storage -> float64 values.  E4M3 rows are multiplied by their fp32 row scale
-    (exactly, in float64); bf16 has no scale; mxfp4 rows are [.., D/2] nibble bytes
-    with [.., D/32] E8M0 scale bytes (see mxfp4_dequant)."""
-    if dtype == "bf16":
-        return bf16_to_f64(data)
-    if dtype == "e4m3":
-        v = e4m3_to_f64(data)
-        return v * np.asarray(scale, dtype=np.float64)[..., None]
-    if dtype == "mxfp4":
-        return mxfp4_dequant(data, scale)
-    raise ValueError(dtype)
-
-
-# ----------------------------------------------------------------------------- logits
-
-def sequence_key_rows(b: int, L: int, block_table, block_size: int, num_rows: int) -> np.ndarray:
-    """Physical row of each logical key j < L of sequence b.
-
-    Paged: row = block_table[b, j // block_size] * block_size + j % block_size.
-    Contiguous (no block table, one sequence): row = j.
-    """
-    j = np.arange(L, dtype=np.int64)
-    if block_table is None:
-        assert b == 0 and L <= num_rows
-        return j
-    blocks = np.asarray(block_table)[b, j // block_size].astype(np.int64)
-    assert (blocks >= 0).all()
-    rows = blocks * block_size + j % block_size
-    assert (rows < num_rows).all()
-    return rows
-
-
-def indexer_logits(q, q_scale, dtype: str, weights, k_data, k_scale, block_table,
-                   block_size: int, B: int, next_n: int, context_lens, causal: bool,
-                   rows=None, width=None, k_dtype=None) -> np.ndarray:
-    """Indexer score for the query rows ``rows`` (default: all T = B * next_n).
-
-    ``dtype`` is the storage of q (and of the keys unless ``k_dtype`` says
-    otherwise: "mxfp4" keys are k_data = nibble rows [rows, D/2] with k_scale =
-    E8M0 rows [rows, D/32]).  Returns float64 [len(rows), width] with width = max
-    context length by default; entries at masked or out-of-range keys are -inf.
-    """
-    context_lens = np.asarray(context_lens, dtype=np.int64)
-    T = B * next_n
-    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
-    width = int(context_lens.max()) if width is None else int(width)
-    w = np.asarray(weights, dtype=np.float64)
-    out = np.full((rows.size, width), NEG_INF, dtype=np.float64)
-    key_cache = {}
-    for r, t in enumerate(rows):
-        b, i = divmod(int(t), next_n)
-        L = int(context_lens[b])
-        if b not in key_cache:
-            kr = sequence_key_rows(b, L, block_table, block_size, k_data.shape[0])
-            ks = None if k_scale is None else np.asarray(k_scale)[kr]
-            key_cache = {b: dequantize(np.asarray(k_data)[kr], ks, k_dtype or dtype)}  # [L, D]
-        k = key_cache[b]
-        qs = None if q_scale is None else np.asarray(q_scale)[t]
-        qt = dequantize(np.asarray(q)[t], qs, dtype)                      # [H, D]
-        visible = (L - next_n + i + 1) if causal else L
-        visible = max(0, min(visible, L))
-        s = qt @ k[:visible].T                                          # [H, visible]
-        relu = np.maximum(s, 0.0)
-        out[r, :visible] = w[t] @ relu                                  # sum over heads
+def build(source: str = SOURCE, out: str = LIB, opt: str = "-O2", force: bool = False) -> str:
+    """Compiles the oracle into a shared library (no-op when it is up to date)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(source):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cxx = os.environ.get("CXX", "g++")
+    tmp = f"{out}.{os.getpid()}.tmp"
+    flags = [opt if f == "-O2" else f for f in CXXFLAGS]
+    r = subprocess.run([cxx, *flags, source, "-o", tmp], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle build failed:\n{r.stderr[-4000:]}")
+    os.replace(tmp, out)
     return out
 
 
-# ----------------------------------------------------------------------------- top-k
-
-def topk_select(logits: np.ndarray, k: int):
-    """Top-k per row under (value descending, index ascending); -inf never selected.
-
-    Returns (idx int32 [R, k], val float64 [R, k]); slots past the number of
-    finite candidates hold -1 / -inf.  NaN logits are not part of the problem
-    (ReLU and finite weights cannot produce them) and are rejected.
-    """
-    x = np.atleast_2d(np.asarray(logits))
-    assert not np.isnan(x).any(), "NaN logits are outside the problem's domain"
-    R = x.shape[0]
-    idx = np.full((R, k), -1, dtype=np.int32)
-    val = np.full((R, k), NEG_INF, dtype=np.float64)
-    for r in range(R):
-        row = x[r] + 0.0          # canonical zero: -0.0 + 0.0 == +0.0
-        cand = np.nonzero(row != NEG_INF)[0]
-        v = row[cand]
-        order = np.lexsort((cand, -v))   # primary: value desc; secondary: index asc
-        take = order[:k]
-        idx[r, :take.size] = cand[take]
-        val[r, :take.size] = v[take]
-    return idx, val
+def threads() -> int:
+    return int(os.environ.get("DSA_ORACLE_THREADS", "0"))
 
 
-# ----------------------------------------------------------------------------- mxfp4
-
-_E2M1_MAGNITUDE = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
-
-
-def e2m1_value(nibble: np.ndarray) -> np.ndarray:
-    """E2M1 nibble s|e1 e0|m -> value, by the OCP MX magnitude table and sign bit 3."""
-    n = np.asarray(nibble, dtype=np.int64) & 0xF
-    mag = np.asarray(_E2M1_MAGNITUDE, dtype=np.float64)[n & 7]
-    return np.where((n & 8) != 0, -mag, mag)
+def _p(a, ctype):
+    return a.ctypes.data_as(POINTER(ctype))
 
 
-def e8m0_scale(b: np.ndarray) -> np.ndarray:
-    """E8M0 group scale: 2^(b-127); the byte 0xFF means a scale of 0."""
-    b = np.asarray(b, dtype=np.int64)
-    return np.where(b == 0xFF, 0.0, np.ldexp(1.0, (b - 127).astype(np.int32)))
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
 
 
-def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round to bf16, nearest-even, returning bit patterns.
+class Oracle:
+    """The compiled oracle at `lib` (built from SOURCE when `lib` is None)."""
 
-    Goes through binary32 first; every value this oracle rounds (an E2M1 value
-    times a power of two) has at most two significant bits, so that step is
-    exact (or overflows to inf, as the bf16 rounding would).
-    """
-    with np.errstate(over="ignore"):
-        f = np.asarray(x, dtype=np.float64).astype(np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    keep = (u >> np.uint64(16)) & np.uint64(1)
-    r = ((u + np.uint64(0x7FFF) + keep) >> np.uint64(16)).astype(np.uint16)
-    nan = np.isnan(f)
-    r[nan] = np.uint16(0x7FC0)
-    return r
+    def __init__(self, lib: str | None = None):
+        if lib is None:
+            with _lock:
+                lib = build()
+                try:
+                    self.lib = ctypes.CDLL(lib)
+                except OSError:                  # a stale library built for another machine
+                    self.lib = ctypes.CDLL(build(force=True))
+        else:
+            self.lib = ctypes.CDLL(lib)
+        L = self.lib
+        L.orc_threads_used.restype = c_int
+        L.orc_threads_used.argtypes = [c_int]
+        for name, ctype in (("orc_bf16", c_uint16), ("orc_e4m3", c_uint8), ("orc_e2m1", c_uint8),
+                            ("orc_e8m0", c_uint8)):
+            fn = getattr(L, name)
+            fn.restype = None
+            fn.argtypes = [POINTER(ctype), c_int64, POINTER(c_double)]
+        L.orc_bf16_round.restype = None
+        L.orc_bf16_round.argtypes = [POINTER(c_double), c_int64, POINTER(c_uint16)]
+        L.orc_mxfp4_dequant.restype = None
+        L.orc_mxfp4_dequant.argtypes = [POINTER(c_uint8), POINTER(c_uint8), c_int64, c_int, POINTER(c_double)]
+        L.orc_indexer_logits.restype = c_int
+        L.orc_indexer_logits.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_void_p, c_void_p, c_int,
+                                         c_int64, c_void_p, c_int64, c_int, c_int, c_int, c_void_p, c_int, c_void_p,
+                                         c_int64, c_int64, POINTER(c_double), c_int]
+        L.orc_topk.restype = c_int
+        L.orc_topk.argtypes = [POINTER(c_double), c_int64, c_int64, c_int, POINTER(c_int32), POINTER(c_double), c_int]
+        L.orc_mxfp4_gather.restype = c_int
+        L.orc_mxfp4_gather.argtypes = [POINTER(c_uint8), POINTER(c_uint8), c_int64, c_int, c_int, POINTER(c_int32),
+                                       c_int64, POINTER(c_int32), c_int64, c_int, c_int, POINTER(c_uint16), c_int]
+
+    # ------------------------------------------------------------------ decoders
+    def _map(self, fn, x, dtype, ctype):
+        a = _c(x, dtype)
+        out = np.empty(a.shape, dtype=np.float64)
+        fn(_p(a, ctype), a.size, _p(out, c_double))
+        return out
+
+    def bf16_to_f64(self, bits):
+        return self._map(self.lib.orc_bf16, bits, np.uint16, c_uint16)
+
+    def e4m3_to_f64(self, codes):
+        return self._map(self.lib.orc_e4m3, codes, np.uint8, c_uint8)
+
+    def e2m1_value(self, nibble):
+        return self._map(self.lib.orc_e2m1, np.asarray(nibble).astype(np.int64) & 0xF, np.uint8, c_uint8)
+
+    def e8m0_scale(self, b):
+        return self._map(self.lib.orc_e8m0, np.asarray(b).astype(np.int64) & 0xFF, np.uint8, c_uint8)
+
+    def f64_to_bf16_bits(self, x):
+        a = _c(x, np.float64)
+        out = np.empty(a.shape, dtype=np.uint16)
+        self.lib.orc_bf16_round(_p(a, c_double), a.size, _p(out, c_uint16))
+        return out
+
+    def mxfp4_dequant(self, fp4_rows, scale_rows):
+        nib = _c(fp4_rows, np.uint8)
+        sc = _c(scale_rows, np.uint8)
+        N, half = nib.shape
+        assert sc.shape == (N, 2 * half // 32)
+        out = np.empty((N, 2 * half), dtype=np.float64)
+        self.lib.orc_mxfp4_dequant(_p(nib, c_uint8), _p(sc, c_uint8), N, 2 * half, _p(out, c_double))
+        return out
+
+    # ------------------------------------------------------------------ score
+    def indexer_logits(self, q, q_scale, dtype: str, weights, k_data, k_scale, block_table, block_size: int,
+                       B: int, next_n: int, context_lens, causal: bool, rows=None, width=None, k_dtype=None):
+        """Indexer score for the query rows ``rows`` (default: all T = B * next_n) as
+        float64 [len(rows), width] (width = the longest context by default); -inf at
+        masked keys.  ``dtype`` is the storage of q, and of the keys unless ``k_dtype``
+        says otherwise ("mxfp4" keys: k_data = nibble rows [rows, D/2], k_scale = E8M0
+        rows [rows, D/32])."""
+        q = _c(q, np.uint16 if dtype == "bf16" else np.uint8)
+        T, H, Dm = q.shape
+        kd = k_dtype or dtype
+        k = _c(k_data, np.uint16 if kd == "bf16" else np.uint8)
+        ks = None
+        if kd == "e4m3":
+            ks = _c(k_scale, np.float64)
+        elif kd == "mxfp4":
+            ks = _c(k_scale, np.uint8)
+        qs = _c(q_scale, np.float64) if dtype == "e4m3" else None
+        w = _c(weights, np.float64)
+        lens = _c(context_lens, np.int32)
+        tab = None if block_table is None else _c(block_table, np.int32)
+        rows = np.arange(B * next_n, dtype=np.int64) if rows is None else _c(rows, np.int64)
+        width = int(lens.max()) if width is None else int(width)
+        out = np.empty((rows.size, width), dtype=np.float64)
+        rc = self.lib.orc_indexer_logits(
+            q.ctypes.data, None if qs is None else qs.ctypes.data, _KIND[dtype], w.ctypes.data, H, Dm,
+            k.ctypes.data, None if ks is None else ks.ctypes.data, _KIND[kd], k.shape[0],
+            None if tab is None else tab.ctypes.data, 0 if tab is None else tab.shape[1], int(block_size), int(B),
+            int(next_n), lens.ctypes.data, 1 if causal else 0, rows.ctypes.data, rows.size, width,
+            _p(out, c_double), threads())
+        assert rc == 0, "a visible key maps outside the key pool"
+        return out
+
+    # ------------------------------------------------------------------ top-k
+    def topk_select(self, logits, k: int):
+        """(idx int32 [R, k], val float64 [R, k]) per row under (value desc, index asc);
+        -inf never selected; -1 / -inf past the candidates.  NaN logits are rejected."""
+        x = _c(np.atleast_2d(np.asarray(logits, dtype=np.float64)), np.float64)
+        R, K = x.shape
+        idx = np.empty((R, k), dtype=np.int32)
+        val = np.empty((R, k), dtype=np.float64)
+        rc = self.lib.orc_topk(_p(x, c_double), R, K, int(k), _p(idx, c_int32), _p(val, c_double), threads())
+        assert rc == 0, "NaN logits are outside the problem's domain"
+        return idx, val
+
+    # ------------------------------------------------------------------ gather
+    def mxfp4_paged_gather(self, kv_fp4, kv_scale, block_table, sel_pos, B: int, next_n: int, block_size: int):
+        """out[t, s, :] = bf16(dequant(cache row of sel_pos[t, s])), zeros where sel_pos < 0."""
+        nib = _c(kv_fp4, np.uint8)
+        sc = _c(kv_scale, np.uint8)
+        tab = _c(block_table, np.int32)
+        sel = _c(sel_pos, np.int32)
+        T, K = sel.shape
+        Dm = 2 * nib.shape[-1]
+        out = np.empty((T, K, Dm), dtype=np.uint16)
+        rc = self.lib.orc_mxfp4_gather(_p(nib, c_uint8), _p(sc, c_uint8), nib.shape[0], int(block_size), Dm,
+                                       _p(tab, c_int32), tab.shape[1], _p(sel, c_int32), T, int(next_n), K,
+                                       _p(out, c_uint16), threads())
+        assert rc == 0, "a selected position maps outside the block table or the cache"
+        return out
+
+    def threads_used(self) -> int:
+        return int(self.lib.orc_threads_used(threads()))
 
 
-def mxfp4_dequant(fp4_rows: np.ndarray, scale_rows: np.ndarray) -> np.ndarray:
-    """[N, D/2] nibble bytes + [N, D/32] E8M0 bytes -> float64 [N, D].
-
-    Element e is nibble (e & 1) of byte e // 2 (low nibble first) times the
-    scale of its group e // 32.
-    """
-    fp4_rows = np.asarray(fp4_rows, dtype=np.uint8)
-    N, half = fp4_rows.shape
-    Dm = 2 * half
-    nib = np.empty((N, Dm), dtype=np.uint8)
-    nib[:, 0::2] = fp4_rows & 0xF
-    nib[:, 1::2] = fp4_rows >> 4
-    vals = e2m1_value(nib)
-    sc = e8m0_scale(np.asarray(scale_rows, dtype=np.uint8))       # [N, D/32]
-    return vals * np.repeat(sc, 32, axis=1)
+_default = None
 
 
-def mxfp4_paged_gather(kv_fp4, kv_scale, block_table, sel_pos, B: int, next_n: int,
-                       block_size: int) -> np.ndarray:
-    """out[t, s, :] = bf16(dequant(cache row of sel_pos[t, s])) or zeros when sel_pos < 0.
+def _get() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle()
+    return _default
 
-    Sequence of row t is b = t // next_n; the cache row of logical position pos is
-    (block_table[b, pos // block_size], pos % block_size).
-    """
-    kv_fp4 = np.asarray(kv_fp4, dtype=np.uint8)
-    kv_scale = np.asarray(kv_scale, dtype=np.uint8)
-    sel = np.asarray(sel_pos, dtype=np.int64)
-    T, K = sel.shape
-    Dm = 2 * kv_fp4.shape[-1]
-    out = np.zeros((T, K, Dm), dtype=np.uint16)
-    b = np.repeat(np.arange(B), next_n)[:, None].repeat(K, axis=1)
-    live = sel >= 0
-    pos = sel[live]
-    blk = np.asarray(block_table, dtype=np.int64)[b[live], pos // block_size]
-    off = pos % block_size
-    vals = mxfp4_dequant(kv_fp4[blk, off], kv_scale[blk, off])
-    out[live] = f64_to_bf16_bits(vals)
-    return out
+
+def indexer_logits(*a, **kw):
+    return _get().indexer_logits(*a, **kw)
+
+
+def topk_select(*a, **kw):
+    return _get().topk_select(*a, **kw)
+
+
+def mxfp4_paged_gather(*a, **kw):
+    return _get().mxfp4_paged_gather(*a, **kw)
+
+
+def mxfp4_dequant(*a, **kw):
+    return _get().mxfp4_dequant(*a, **kw)
+
+
+def e2m1_value(*a, **kw):
+    return _get().e2m1_value(*a, **kw)
+
+
+def e8m0_scale(*a, **kw):
+    return _get().e8m0_scale(*a, **kw)
+
+
+def f64_to_bf16_bits(*a, **kw):
+    return _get().f64_to_bf16_bits(*a, **kw)
+
+
+def bf16_to_f64(*a, **kw):
+    return _get().bf16_to_f64(*a, **kw)
+
+
+def e4m3_to_f64(*a, **kw):
+    return _get().e4m3_to_f64(*a, **kw)
+
+
+def threads_used() -> int:
+    return _get().threads_used()

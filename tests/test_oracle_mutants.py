@@ -1,61 +1,75 @@
-"""Plant plausible mistakes in copies of the oracle (CPU only) and require that
-every one of them fails at least one pin.  This is evidence that the pins in
-pins.py constrain each part of the oracle, not only that the oracle passes them."""
+"""Plant plausible mistakes in copies of the C++ oracle (CPU only) and require that
+every one of them fails at least one pin.  This is evidence that the pins in pins.py
+constrain each part of the oracle, not only that the oracle passes them.  Each mutant is
+the oracle's source with one edit, compiled on its own."""
+import concurrent.futures as cf
 import os
-import types
+import tempfile
 
 import pytest
 
 import pins
-
-ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                          "oracle", "dsa_oracle.py")
+from oracle import dsa_oracle
 
 MUTANTS = {
-    "relu_dropped": ("relu = np.maximum(s, 0.0)", "relu = s"),
-    "relu_after_weighting": ("out[r, :visible] = w[t] @ relu",
-                             "out[r, :visible] = np.maximum(w[t] @ s, 0.0)"),
-    "head_dropped": ("out[r, :visible] = w[t] @ relu", "out[r, :visible] = w[t][:-1] @ relu[:-1]"),
+    "relu_dropped": ("const double relu = s > 0.0 ? s : 0.0;", "const double relu = s;"),
+    "relu_after_weighting": ("*dst = logit + 0.0;     // -0.0 + 0.0 == +0.0",
+                             "*dst = 0.0;\n      { double z = 0.0; for (int h = 0; h < H; ++h) { double s = 0.0;"
+                             " for (int d = 0; d < D; ++d) s += qv[static_cast<size_t>(h) * D + d] * kv[d];"
+                             " z += weights[t * H + h] * s; } *dst = (z > 0.0 ? z : 0.0) + 0.0; }"),
+    "head_dropped": ("for (int h = 0; h < H; ++h) {\n        double s = 0.0;",
+                     "for (int h = 0; h < H - 1; ++h) {\n        double s = 0.0;"),
     "causal_off_by_one": ("(L - next_n + i + 1)", "(L - next_n + i)"),
-    "page_offset": ("blocks * block_size + j % block_size", "blocks * block_size + j // block_size"),
-    "seq_index": ("b, i = divmod(int(t), next_n)", "i, b = divmod(int(t), next_n)"),
-    "k_scale_rows": ("np.asarray(k_scale)[kr]", "np.asarray(k_scale)[:L]"),
-    "row_scale_dropped": ("return v * np.asarray(scale, dtype=np.float64)[..., None]", "return v"),
-    "e4m3_bias": ("np.exp2((e - 7)", "np.exp2((e - 8)"),
-    "e4m3_subnormal": ("(m / 8.0) * 2.0**-6", "(m / 8.0) * 2.0**-7"),
-    "tie_order": ("np.lexsort((cand, -v))", "np.lexsort((-cand, -v))"),
-    "neg_inf_selected": ("cand = np.nonzero(row != NEG_INF)[0]", "cand = np.arange(row.size)"),
-    "no_zero_canon": ("row = x[r] + 0.0", "row = np.where(np.signbit(x[r]) & (x[r] == 0), -1e-300, x[r])"),
-    "nibble_order": ("nib[:, 0::2] = fp4_rows & 0xF\n    nib[:, 1::2] = fp4_rows >> 4",
-                     "nib[:, 0::2] = fp4_rows >> 4\n    nib[:, 1::2] = fp4_rows & 0xF"),
-    "e2m1_table": ("(0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)", "(0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 3.0, 3.5)"),
-    "e2m1_sign": ("np.where((n & 8) != 0, -mag, mag)", "np.where((n & 4) != 0, -mag, mag)"),
-    "e8m0_ff": ("np.where(b == 0xFF, 0.0,", "np.where(b == 0x100, 0.0,"),
-    "e8m0_bias": ("(b - 127).astype(np.int32)", "(b - 128).astype(np.int32)"),
-    "scale_group": ("np.repeat(sc, 32, axis=1)", "np.tile(sc, (1, 32))"),
-    "bf16_truncate": ("(u + np.uint64(0x7FFF) + keep)", "(u)"),
-    "padded_not_zero": ("live = sel >= 0", "live = sel >= -1"),
-    "gather_seq_row": ("[b[live], pos // block_size]", "[0 * b[live], pos // block_size]"),
-    "gather_offset": ("off = pos % block_size", "off = pos // block_size % block_size"),
-    "key_dtype_ignored": ("dequantize(np.asarray(k_data)[kr], ks, k_dtype or dtype)",
-                          "dequantize(np.asarray(k_data)[kr], ks, dtype)"),
-    "mxfp4_key_scale_ignored": ("return mxfp4_dequant(data, scale)",
-                                "return mxfp4_dequant(data, np.full_like(scale, 127))"),
+    "page_offset": ("row = blk * block_size + j % block_size;", "row = blk * block_size + j / block_size;"),
+    "seq_index": ("const int64_t b = t / next_n, i = t % next_n;", "const int64_t b = t % next_n, i = t / next_n;"),
+    "k_scale_rows": ("static_cast<const double*>(k_scale)[row];", "static_cast<const double*>(k_scale)[j];"),
+    "q_scale_dropped": ("* q_scale[t * H + h];", ";"),
+    "e4m3_bias": ("std::ldexp(1.0, e - 7)", "std::ldexp(1.0, e - 8)"),
+    "e4m3_subnormal": ("(m / 8.0) * std::ldexp(1.0, -6)", "(m / 8.0) * std::ldexp(1.0, -7)"),
+    "bf16_shift": ("static_cast<uint32_t>(bits) << 16;", "static_cast<uint32_t>(bits) << 15;"),
+    "tie_order": ("return a.second < b.second;", "return a.second > b.second;"),
+    "neg_inf_selected": ("if (v == kNegInf || std::isnan(v)) continue;", "if (std::isnan(v)) continue;"),
+    "no_zero_canon": ("cand.emplace_back(v + 0.0, j);",
+                      "cand.emplace_back(std::signbit(v) && v == 0.0 ? -1e-300 : v, j);"),
+    "short_row_not_padded": ("        idx[r * k + s] = -1;\n", "        idx[r * k + s] = 0;\n"),
+    "nibble_order": ("(e % 2 == 0) ? (byte & 0xF) : (byte >> 4)", "(e % 2 == 0) ? (byte >> 4) : (byte & 0xF)"),
+    "e2m1_table": ("{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 3.0, 3.5}"),
+    "e2m1_sign": ("return (nibble & 8) ? -mag : mag;", "return (nibble & 4) ? -mag : mag;"),
+    "e8m0_ff": ("b == 0xFF ? 0.0 :", "b == 0x100 ? 0.0 :"),
+    "e8m0_bias": ("static_cast<int>(b) - 127", "static_cast<int>(b) - 128"),
+    "scale_group": ("scale_row[e / 32]", "scale_row[e % 4]"),
+    "bf16_truncate": ("(static_cast<uint64_t>(u) + 0x7FFFu + lsb) >> 16", "static_cast<uint64_t>(u) >> 16"),
+    "padded_not_zero": ("if (pos < 0) {", "if (pos < -1) {"),
+    "gather_seq_row": ("const int64_t blk = col < bt_stride ? block_table[b * bt_stride + col] : -1;",
+                       "const int64_t blk = col < bt_stride ? block_table[0 * b * bt_stride + col] : -1;"),
+    "gather_offset": ("const int64_t row = blk * block_size + pos % block_size;",
+                      "const int64_t row = blk * block_size + pos / block_size % block_size;"),
+    "key_kind_ignored": ("} else if (k_kind == kE4M3) {", "} else if (k_kind != kBF16) {"),
+    "mxfp4_key_scale_row": ("static_cast<const uint8_t*>(k_scale) + row * (D / 32);",
+                            "static_cast<const uint8_t*>(k_scale) + 0 * row * (D / 32);"),
 }
 
 
-def _mutant(name):
-    src = open(ORACLE_SRC).read()
-    old, new = MUTANTS[name]
-    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
-    mod = types.ModuleType(f"oracle_mutant_{name}")
-    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
-    return mod
+@pytest.fixture(scope="module")
+def mutant_libs():
+    src = open(dsa_oracle.SOURCE).read()
+    tmp = tempfile.mkdtemp(prefix="oracle_mutants_")
+
+    def make(name):
+        old, new = MUTANTS[name]
+        assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+        path = os.path.join(tmp, f"{name}.cpp")
+        with open(path, "w") as f:
+            f.write(src.replace(old, new))
+        return name, dsa_oracle.build(path, os.path.join(tmp, f"lib{name}.so"), opt="-O1")
+
+    with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        return dict(ex.map(make, sorted(MUTANTS)))
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_mutant_is_caught(name):
-    mod = _mutant(name)
+def test_mutant_is_caught(name, mutant_libs):
+    mod = dsa_oracle.Oracle(mutant_libs[name])
     failed = []
     for check in pins.ALL_CHECKS:
         try:
