@@ -75,17 +75,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits until the phase with the given parity has completed.  Gives up after
 // `limit_ns` (or as soon as *abort becomes non-zero) and returns false; the caller
-// then abandons its work.  Never spins forever.
+// then abandons its work.  Never spins forever.  (try_wait itself may suspend the
+// thread for a while before it reports an incomplete phase, so the clock and the
+// abort flag are read after every failed attempt.)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns,
                                           const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
