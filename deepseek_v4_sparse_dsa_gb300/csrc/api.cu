@@ -171,13 +171,14 @@ const char* dsa_status_string(dsa_status status) {
 
 int dsa_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
-  unsigned int w = 0, total = 0;
-  if (tu_gather_read_clear_error(&w) != cudaSuccess) return -1;
-  total |= w;
-  if (tu_indexer_read_clear_error(&w) != cudaSuccess) return -1;
-  total |= w;
-  if (tu_topk_read_clear_error(&w) != cudaSuccess) return -1;
-  total |= w;
+  unsigned int total = 0;
+  int n = 0;
+  const TuWords* tus = all_tu_words(&n);
+  for (int i = 0; i < n; ++i) {
+    unsigned int w = 0;
+    if (tus[i].read_clear(&w) != cudaSuccess) return -1;
+    total |= w;
+  }
   return (int)total;
 }
 
@@ -185,9 +186,10 @@ uint64_t dsa_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 dsa_status dsa_set_wait_limit_ns(uint64_t ns) {
   const unsigned long long v = ns;
-  if (tu_gather_set_wait_limit(v) != cudaSuccess) return DSA_ERR_CUDA;
-  if (tu_indexer_set_wait_limit(v) != cudaSuccess) return DSA_ERR_CUDA;
-  if (tu_topk_set_wait_limit(v) != cudaSuccess) return DSA_ERR_CUDA;
+  int n = 0;
+  const TuWords* tus = all_tu_words(&n);
+  for (int i = 0; i < n; ++i)
+    if (tus[i].set_limit(v) != cudaSuccess) return DSA_ERR_CUDA;
   return DSA_OK;
 }
 

@@ -100,6 +100,24 @@ cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_
 
 DSA_DECLARE_TU_ERROR_ACCESSORS(gather)
 DSA_DECLARE_TU_ERROR_ACCESSORS(indexer)
+DSA_DECLARE_TU_ERROR_ACCESSORS(indexer_bf16_topk)
+DSA_DECLARE_TU_ERROR_ACCESSORS(indexer_bf16_logits)
+DSA_DECLARE_TU_ERROR_ACCESSORS(indexer_fp8_topk)
+DSA_DECLARE_TU_ERROR_ACCESSORS(indexer_fp8_logits)
 DSA_DECLARE_TU_ERROR_ACCESSORS(topk)
+
+// Every translation unit's accessors, for dsa_device_error / dsa_set_wait_limit_ns.
+struct TuWords {
+  cudaError_t (*read_clear)(unsigned int*);
+  cudaError_t (*set_limit)(unsigned long long);
+};
+#define DSA_TU_WORDS(name) TuWords{tu_##name##_read_clear_error, tu_##name##_set_wait_limit}
+inline const TuWords* all_tu_words(int* n) {
+  static const TuWords w[] = {DSA_TU_WORDS(gather), DSA_TU_WORDS(indexer), DSA_TU_WORDS(indexer_bf16_topk),
+                              DSA_TU_WORDS(indexer_bf16_logits), DSA_TU_WORDS(indexer_fp8_topk),
+                              DSA_TU_WORDS(indexer_fp8_logits), DSA_TU_WORDS(topk)};
+  *n = (int)(sizeof(w) / sizeof(w[0]));
+  return w;
+}
 
 }  // namespace dsa
