@@ -32,7 +32,29 @@
 //    arithmetically); the low nibble of byte i holds element 2i.
 //  * orc_e4m3 -- OCP E4M3 (bias 7, no infinities, S.1111.111 = NaN, subnormals
 //    m * 2^-9), the byte format README "DeepSeek V4 Flash on a single AMD MI300X"
-//    ("FP8 format") contrasts with AMD's FNUZ variant.
+//    ("FP8 format") contrasts with AMD's FNUZ variant; orc_e4m3_encode rounds to it
+//    (nearest, ties to the even code, saturating at +-448 = the FP8_MAX the OCP path
+//    uses, vllm PR #1 "Sparse-MLA bring-up on MI300X", "Root cause story" item 1).
+//  * orc_q_rope_quant -- the indexer-Q producer ahead of the score (vllm PR #1, "Root
+//    cause story" item 3: a fused RoPE + per-row FP8 quantisation of the indexer query
+//    whose bytes the fp8 MQA-logits reader consumes).  Readings: RoPE rotates the
+//    interleaved pairs (2i, 2i+1) of the first rope_dim dims of every head by the angle
+//    whose cos / sin the caller's table holds for the token's position; the other dims
+//    pass through; each (token, head) row is then quantised with scale = rowmax / 448
+//    (1 for an all-zero row), code = E4M3(value / scale).  Arithmetic in fp32, each
+//    product and sum rounded on its own (no fused multiply-add), because the codes are
+//    integers decided by that arithmetic.
+//  * orc_k_hadamard_mxfp4 -- the indexer-key compressor's write into the paged FP4
+//    cache (ROCm/ATOM issue #707, "CSA": "CSA Indexer Compressor (head_dim=128,
+//    Hadamard, FP4)"), read as: rotate each 128-dim key by the orthonormal
+//    Walsh-Hadamard matrix (Sylvester order, entries +-1/sqrt(128)), then encode it in
+//    the gather's mxfp4 layout by the OCP MX v1.0 conversion: per 32-element group
+//    the shared exponent is floor(log2(amax)) - 2 (2 = the largest E2M1 exponent), the
+//    E8M0 byte that exponent + 127 (clamped to 0..254; an all-zero group gets byte 0),
+//    each element E2M1(value / 2^exponent) rounded to nearest, ties to the even code,
+//    saturating at 6; low nibble = even element; written to the pool row its slot
+//    names (slot < 0: skipped).  The rotation is computed in float64 and rounded to
+//    fp32, the precision in which the codes are decided.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -98,6 +120,48 @@ double mxfp4_element(const uint8_t* nib_row, const uint8_t* scale_row, int e) {
   const uint8_t byte = nib_row[e / 2];
   const uint8_t nibble = (e % 2 == 0) ? (byte & 0xF) : (byte >> 4);
   return e2m1_value(nibble) * e8m0_value(scale_row[e / 32]);
+}
+
+// Nearest E4M3 code of a finite fp32 value: ties to the code with the even mantissa,
+// magnitudes beyond 448 saturate to 448.  Found by rounding the value on the grid of
+// its binade (subnormal spacing 2^-9 below 2^-6), then looking the rounded value up
+// among the 256 codes.
+uint8_t e4m3_encode(float xf) {
+  const double x = static_cast<double>(xf);
+  double a = std::fabs(x);
+  if (a > 448.0) a = 448.0;
+  double step;
+  if (a < std::ldexp(1.0, -6)) {
+    step = std::ldexp(1.0, -9);
+  } else {
+    int e;
+    std::frexp(a, &e);                      // a = f * 2^e, f in [0.5, 1)
+    step = std::ldexp(1.0, (e - 1) - 3);    // 3 mantissa bits below the leading one
+  }
+  const double q = a / step;                // exact: step is a power of two
+  double r = std::floor(q);
+  const double frac = q - r;
+  if (frac > 0.5 || (frac == 0.5 && std::fmod(r, 2.0) != 0.0)) r += 1.0;
+  const double v = r * step;                // <= 448: a <= 448 = 14 * 32 lies on the grid
+  const bool neg = std::signbit(x);
+  for (int c = 0; c < 128; ++c) {           // codes 0x00..0x7F are the non-negative values
+    if (c == 0x7F) continue;                 // NaN
+    if (e4m3_value(static_cast<uint8_t>(c)) == v) return static_cast<uint8_t>(neg ? (c | 0x80) : c);
+  }
+  return 0x7F;                               // not reached for finite inputs
+}
+
+// Nearest E2M1 code of a double value: ties to the code with the even mantissa bit,
+// magnitudes beyond 6 saturate to 6.
+uint8_t e2m1_encode(double x) {
+  double a = std::fabs(x);
+  if (a > 6.0) a = 6.0;
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const double dc = std::fabs(kE2M1Magnitude[c] - a), db = std::fabs(kE2M1Magnitude[best] - a);
+    if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+  }
+  return static_cast<uint8_t>(best | (std::signbit(x) && best != 0 ? 8 : 0));
 }
 
 // ------------------------------------------------------------------ threads
@@ -308,6 +372,103 @@ int orc_mxfp4_gather(const uint8_t* kv_fp4, const uint8_t* kv_scale, int64_t num
       const int64_t row = blk * block_size + pos % block_size;
       for (int e = 0; e < D; ++e)
         dst[e] = bf16_bits_of(mxfp4_element(kv_fp4 + row * (D / 2), kv_scale + row * (D / 32), e));
+    }
+  });
+  return bad.load() ? -1 : 0;
+}
+
+void orc_e2m1_encode(const double* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e2m1_encode(x[i]);
+}
+
+void orc_e4m3_encode(const float* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_encode(x[i]);
+}
+
+// q [T, H, D] bf16 bits, positions [T], cos_sin [max_pos, rope_dim] fp32 (per position:
+// rope_dim / 2 cosines, then rope_dim / 2 sines) -> codes [T, H, D] E4M3, scale [T, H] fp32.
+// Returns -1 if a position lies outside the table.
+int orc_q_rope_quant(const uint16_t* q, const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                     int rope_dim, int64_t T, int H, int D, uint8_t* codes, float* scale, int threads) {
+  std::atomic<int> bad{0};
+  parallel_for(T * H, threads, [&](int64_t row) {
+    const int64_t t = row / H;
+    const int64_t pos = positions[t];
+    if (pos < 0 || pos >= max_pos) {
+      bad.store(1);
+      for (int d = 0; d < D; ++d) codes[row * D + d] = 0;
+      scale[row] = 0.0f;
+      return;
+    }
+    std::vector<float> y(D);
+    for (int d = 0; d < D; ++d) y[d] = static_cast<float>(bf16_value(q[row * D + d]));
+    const int half = rope_dim / 2;
+    for (int i = 0; i < half; ++i) {
+      const float x0 = y[2 * i], x1 = y[2 * i + 1];
+      const float c = cos_sin[pos * rope_dim + i], s = cos_sin[pos * rope_dim + half + i];
+      const float p0 = x0 * c, p1 = x1 * s, p2 = x0 * s, p3 = x1 * c;
+      y[2 * i] = p0 - p1;
+      y[2 * i + 1] = p2 + p3;
+    }
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) amax = std::max(amax, std::fabs(y[d]));
+    const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+    scale[row] = sc;
+    for (int d = 0; d < D; ++d) codes[row * D + d] = e4m3_encode(y[d] / sc);
+  });
+  return bad.load() ? -1 : 0;
+}
+
+// k [N, D] bf16 bits, slot [N] (pool row or < 0) -> kv_fp4 [num_rows, D/2],
+// kv_scale [num_rows, D/32] at the slots' rows.  D must be a power of two.
+// Returns -1 if a slot lies outside the pool.
+int orc_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot, int64_t N, int D, uint8_t* kv_fp4,
+                         uint8_t* kv_scale, int64_t num_rows, int threads) {
+  std::atomic<int> bad{0};
+  const double norm = 1.0 / std::sqrt(static_cast<double>(D));
+  parallel_for(N, threads, [&](int64_t n) {
+    const int64_t row = slot[n];
+    if (row < 0) return;
+    if (row >= num_rows) {
+      bad.store(1);
+      return;
+    }
+    std::vector<double> x(D);
+    std::vector<float> y(D);
+    for (int d = 0; d < D; ++d) x[d] = bf16_value(k[n * D + d]);
+    // y_i = sum_j H[i][j] x_j / sqrt(D), H[i][j] = (-1)^popcount(i & j) (Sylvester order)
+    for (int i = 0; i < D; ++i) {
+      double acc = 0.0;
+      for (int j = 0; j < D; ++j) {
+        const int sign = __builtin_popcount(static_cast<unsigned>(i & j)) & 1;
+        acc += sign ? -x[j] : x[j];
+      }
+      y[i] = static_cast<float>(acc * norm);
+    }
+    for (int g = 0; g < D / 32; ++g) {
+      float amax = 0.0f;
+      for (int e = 0; e < 32; ++e) amax = std::max(amax, std::fabs(y[g * 32 + e]));
+      int sexp = 0;                                  // shared exponent
+      uint8_t byte = 0;
+      if (amax > 0.0f) {
+        int e2;
+        std::frexp(static_cast<double>(amax), &e2);  // amax = f * 2^e2, f in [0.5, 1)
+        sexp = (e2 - 1) - 2;                         // floor(log2(amax)) - 2
+        int b = sexp + 127;
+        if (b < 0) b = 0;
+        if (b > 254) b = 254;
+        byte = static_cast<uint8_t>(b);
+        sexp = b - 127;
+      }
+      kv_scale[row * (D / 32) + g] = byte;
+      for (int e = 0; e < 32; e += 2) {
+        uint8_t lo = 0, hi = 0;
+        if (amax > 0.0f) {
+          lo = e2m1_encode(std::ldexp(static_cast<double>(y[g * 32 + e]), -sexp));
+          hi = e2m1_encode(std::ldexp(static_cast<double>(y[g * 32 + e + 1]), -sexp));
+        }
+        kv_fp4[row * (D / 2) + (g * 32 + e) / 2] = static_cast<uint8_t>(lo | (hi << 4));
+      }
     }
   });
   return bad.load() ? -1 : 0;

@@ -27,7 +27,7 @@ import ctypes
 import os
 import subprocess
 import threading
-from ctypes import POINTER, c_double, c_int, c_int32, c_int64, c_uint8, c_uint16, c_void_p
+from ctypes import POINTER, c_double, c_float, c_int, c_int32, c_int64, c_uint8, c_uint16, c_void_p
 
 import numpy as np
 
@@ -98,6 +98,16 @@ class Oracle:
                                          c_int64, c_int64, POINTER(c_double), c_int]
         L.orc_topk.restype = c_int
         L.orc_topk.argtypes = [POINTER(c_double), c_int64, c_int64, c_int, POINTER(c_int32), POINTER(c_double), c_int]
+        L.orc_e2m1_encode.restype = None
+        L.orc_e2m1_encode.argtypes = [POINTER(c_double), c_int64, POINTER(c_uint8)]
+        L.orc_e4m3_encode.restype = None
+        L.orc_e4m3_encode.argtypes = [POINTER(c_float), c_int64, POINTER(c_uint8)]
+        L.orc_q_rope_quant.restype = c_int
+        L.orc_q_rope_quant.argtypes = [POINTER(c_uint16), POINTER(c_int32), POINTER(c_float), c_int64, c_int, c_int64,
+                                       c_int, c_int, POINTER(c_uint8), POINTER(c_float), c_int]
+        L.orc_k_hadamard_mxfp4.restype = c_int
+        L.orc_k_hadamard_mxfp4.argtypes = [POINTER(c_uint16), POINTER(c_int64), c_int64, c_int, POINTER(c_uint8),
+                                           POINTER(c_uint8), c_int64, c_int]
         L.orc_mxfp4_gather.restype = c_int
         L.orc_mxfp4_gather.argtypes = [POINTER(c_uint8), POINTER(c_uint8), c_int64, c_int, c_int, POINTER(c_int32),
                                        c_int64, POINTER(c_int32), c_int64, c_int, c_int, POINTER(c_uint16), c_int]
@@ -197,6 +207,51 @@ class Oracle:
         assert rc == 0, "a selected position maps outside the block table or the cache"
         return out
 
+    # ------------------------------------------------------------------ producers
+    def e2m1_encode(self, x):
+        """Nearest E2M1 codes (nibbles) of values (ties to the even code, saturating at 6)."""
+        a = _c(x, np.float64)
+        out = np.empty(a.shape, dtype=np.uint8)
+        self.lib.orc_e2m1_encode(_p(a, c_double), a.size, _p(out, c_uint8))
+        return out
+
+    def e4m3_encode(self, x):
+        """Nearest OCP E4M3 codes of fp32 values (ties to even, saturating at +-448)."""
+        a = _c(x, np.float32)
+        out = np.empty(a.shape, dtype=np.uint8)
+        self.lib.orc_e4m3_encode(_p(a, c_float), a.size, _p(out, c_uint8))
+        return out
+
+    def q_rope_quant(self, q, positions, cos_sin, rope_dim: int):
+        """Indexer-Q producer: RoPE on the interleaved pairs of the first rope_dim dims of
+        every head (cos / sin from the table row of the token's position), then per-row
+        E4M3 quantisation.  q [T, H, D] bf16 bits -> (codes [T, H, D] uint8, scale [T, H])."""
+        qb = _c(q, np.uint16)
+        T, H, Dm = qb.shape
+        pos = _c(positions, np.int32)
+        cs = _c(cos_sin, np.float32)
+        codes = np.empty((T, H, Dm), dtype=np.uint8)
+        scale = np.empty((T, H), dtype=np.float32)
+        rc = self.lib.orc_q_rope_quant(_p(qb, c_uint16), _p(pos, c_int32), _p(cs, c_float), cs.shape[0],
+                                       int(rope_dim), T, H, Dm, _p(codes, c_uint8), _p(scale, c_float), threads())
+        assert rc == 0, "a position lies outside the cos / sin table"
+        return codes, scale
+
+    def k_hadamard_mxfp4(self, k, slot, kv_fp4, kv_scale):
+        """Indexer-key compressor write: Hadamard rotation + mxfp4 encoding of the keys
+        k [N, D] (bf16 bits) into copies of the pools kv_fp4 [blocks, bs, D/2] and
+        kv_scale [blocks, bs, D/32] at pool rows `slot` (< 0: skipped); returns them."""
+        kb = _c(k, np.uint16)
+        N, Dm = kb.shape
+        sl = _c(slot, np.int64)
+        fp4 = np.array(kv_fp4, dtype=np.uint8, copy=True, order="C")
+        sc = np.array(kv_scale, dtype=np.uint8, copy=True, order="C")
+        rows = fp4.size // (Dm // 2)
+        rc = self.lib.orc_k_hadamard_mxfp4(_p(kb, c_uint16), _p(sl, c_int64), N, Dm, _p(fp4, c_uint8),
+                                           _p(sc, c_uint8), rows, threads())
+        assert rc == 0, "a slot lies outside the pool"
+        return fp4, sc
+
     def threads_used(self) -> int:
         return int(self.lib.orc_threads_used(threads()))
 
@@ -250,3 +305,19 @@ def e4m3_to_f64(*a, **kw):
 
 def threads_used() -> int:
     return _get().threads_used()
+
+
+def e4m3_encode(*a, **kw):
+    return _get().e4m3_encode(*a, **kw)
+
+
+def q_rope_quant(*a, **kw):
+    return _get().q_rope_quant(*a, **kw)
+
+
+def k_hadamard_mxfp4(*a, **kw):
+    return _get().k_hadamard_mxfp4(*a, **kw)
+
+
+def e2m1_encode(*a, **kw):
+    return _get().e2m1_encode(*a, **kw)

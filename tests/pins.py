@@ -425,10 +425,140 @@ def check_topk_bruteforce(orc, seed=8):
         assert np.array_equal(val[0][live], row[idx[0][live]])
 
 
+# --------------------------------------------------------------------------- producers
+
+def check_e4m3_encode(orc):
+    """Nearest-even, saturating E4M3 rounding == torch's float32 -> float8_e4m3fn after a
+    clamp to +-448, on random values, binade edges, subnormals, ties and signed zeros."""
+    import torch
+    r = np.random.default_rng(10)
+    x = np.concatenate([
+        (r.standard_normal(20000) * np.exp2(r.integers(-12, 10, 20000))).astype(np.float32),
+        np.float32([0.0, -0.0, 448, 449, 464, 480, -1e9, 2**-9, 2**-10, 3 * 2**-11, -3 * 2**-11, 1e-30,
+                    -1e-30, 1.0625, 1.1875, 17.0, 19.0, 2**-6, 15 * 2**-10]),
+    ])
+    ref = torch.from_numpy(np.clip(x, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = orc.e4m3_encode(x)
+    assert np.array_equal(got, ref), (x[got != ref][:5], got[got != ref][:5], ref[got != ref][:5])
+    # decode(encode(v)) == v for every finite code value
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    vals = orc.e4m3_to_f64(codes).astype(np.float32)
+    assert np.array_equal(orc.e4m3_to_f64(orc.e4m3_encode(vals)), vals.astype(np.float64))
+
+
+def check_e2m1_encode(orc):
+    """OCP E2M1 rounding: nearest grid value, ties to the even code, saturation at 6."""
+    x = np.array([0.0, 0.1, 0.25, 0.26, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 5.1, 7.0, 100.0, -0.3, -2.5, -6.5])
+    want = [0, 0, 0, 1, 2, 2, 4, 4, 6, 6, 7, 7, 7, 9, 12, 15]
+    assert list(orc.e2m1_encode(x)) == want
+
+
+def _rope_table(max_pos, rope_dim, base=10000.0):
+    """cos / sin of pos * base^(-2i / rope_dim), float64 rounded to fp32, laid out per
+    position as rope_dim / 2 cosines then rope_dim / 2 sines (the standard table)."""
+    i = np.arange(rope_dim // 2, dtype=np.float64)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * base ** (-2.0 * i / rope_dim)[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def check_q_rope_quant(orc, seed=11):
+    from deepseek_v4_sparse_dsa_gb300 import synth
+    r = np.random.default_rng(seed)
+    T, H, Dm, R = 5, 3, 128, 64
+    qf = r.standard_normal((T, H, Dm)).astype(np.float32)
+    qb = (qf.view(np.uint32) >> 16).astype(np.uint16)          # bf16 patterns (truncation)
+    qv = orc.bf16_to_f64(qb).astype(np.float32)
+    pos = np.array([0, 3, 1, 4, 2], np.int32)
+    # identity rotation (cos 1, sin 0): the per-row quantisation of the config generator
+    ident = np.concatenate([np.ones((6, R // 2)), np.zeros((6, R // 2))], axis=1).astype(np.float32)
+    codes, scale = orc.q_rope_quant(qb, pos, ident, R)
+    want_c, want_s = synth.quantize_e4m3_rows(qv)
+    assert np.array_equal(codes, want_c) and np.array_equal(scale, want_s)
+    # a quarter turn (cos 0, sin 1): (x0, x1) -> (-x1, x0) on the first R dims, exactly
+    quarter = np.concatenate([np.zeros((6, R // 2)), np.ones((6, R // 2))], axis=1).astype(np.float32)
+    codes, scale = orc.q_rope_quant(qb, pos, quarter, R)
+    rot = qv.copy()
+    rot[..., 0:R:2] = -qv[..., 1:R:2]
+    rot[..., 1:R:2] = qv[..., 0:R:2]
+    want_c, want_s = synth.quantize_e4m3_rows(rot)
+    assert np.array_equal(codes, want_c) and np.array_equal(scale, want_s)
+    # hand case: head 0 of token 0 = e_0 rotated by 90 degrees -> e_1 -> code 448 = 0x7E at dim 1
+    one = np.zeros((1, 1, Dm), np.uint16)
+    one[0, 0, 0] = 0x3F80                            # 1.0
+    codes, scale = orc.q_rope_quant(one, np.array([2], np.int32), quarter, R)
+    assert scale[0, 0] == np.float32(1.0) / np.float32(448.0)
+    assert codes[0, 0, 1] == 0x7E and not np.delete(codes[0, 0], 1).any()
+    # a real RoPE table: the dequantised result is the exact rotation to within E4M3
+    # rounding (half a step, 2^-4 relative) of each element
+    tab = _rope_table(8, R)
+    codes, scale = orc.q_rope_quant(qb, pos, tab, R)
+    deq = orc.e4m3_to_f64(codes) * scale[..., None]
+    exact = qv.astype(np.float64).copy()
+    c = tab[pos][:, None, :R // 2].astype(np.float64)
+    sn = tab[pos][:, None, R // 2:].astype(np.float64)
+    x0, x1 = qv[..., 0:R:2].astype(np.float64), qv[..., 1:R:2].astype(np.float64)
+    exact[..., 0:R:2] = x0 * c - x1 * sn
+    exact[..., 1:R:2] = x0 * sn + x1 * c
+    step = np.maximum(np.abs(exact), 2.0**-6 * scale[..., None]) * 2.0**-4 + 1e-6 * np.abs(exact)
+    assert np.all(np.abs(deq - exact) <= step)
+    # dims past rope_dim pass through: their codes are the plain quantisation of the input
+    # at the row's scale (torch's float8 conversion)
+    import torch
+    y = np.clip(qv[..., R:] / scale[..., None], -448, 448).astype(np.float32)
+    want = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes[..., R:], want)
+
+
+def _hadamard(Dm):
+    Hm = np.array([[1.0]])
+    while Hm.shape[0] < Dm:
+        Hm = np.block([[Hm, Hm], [Hm, -Hm]])
+    return Hm
+
+
+def check_k_hadamard_mxfp4(orc, seed=12):
+    Dm, bs, nblk = 128, 4, 3
+    pool = np.full((nblk, bs, Dm // 2), 0xAA, np.uint8)
+    psc = np.full((nblk, bs, Dm // 32), 0x55, np.uint8)
+    # hand case: a one-hot key e_j -> column j of H / sqrt(128): every entry +-2^-3.5;
+    # amax 0.0884 -> shared exponent floor(log2) - 2 = -6 (byte 121); 0.0884 * 2^6 = 5.66
+    # rounds to 6.0 (code 7); signs (-1)^popcount(i & j)
+    j = 5
+    k = np.zeros((1, Dm), np.uint16)
+    k[0, j] = 0x3F80
+    fp4, sc = orc.k_hadamard_mxfp4(k, np.array([1 * bs + 2]), pool, psc)
+    assert (sc[1, 2] == 121).all()
+    want = np.where(np.array([bin(i & j).count("1") % 2 for i in range(Dm)]) == 1, 0xF, 0x7)
+    assert np.array_equal(fp4[1, 2] & 0xF, want[0::2]) and np.array_equal(fp4[1, 2] >> 4, want[1::2])
+    # other rows untouched; a negative slot writes nothing
+    mask = np.ones((nblk, bs), bool)
+    mask[1, 2] = False
+    assert (fp4[mask] == 0xAA).all() and (sc[mask] == 0x55).all()
+    fp4b, scb = orc.k_hadamard_mxfp4(k, np.array([-1]), pool, psc)
+    assert np.array_equal(fp4b, pool) and np.array_equal(scb, psc)
+    # random keys: decoding the written rows gives H x / sqrt(128) to within half an
+    # E2M1 step at the group's scale (the step is 0.5, 1 or 2 units of 2^exponent)
+    r = np.random.default_rng(seed)
+    N = 6
+    k = f64_to_bf16_exact(r.integers(-64, 65, (N, Dm)) / 16.0)
+    slots = r.permutation(nblk * bs)[:N]
+    fp4, sc = orc.k_hadamard_mxfp4(k, slots, pool, psc)
+    y = orc.bf16_to_f64(k) @ _hadamard(Dm).T / np.sqrt(Dm)
+    deq = orc.mxfp4_dequant(fp4.reshape(-1, Dm // 2)[slots], sc.reshape(-1, Dm // 32)[slots])
+    g = y.reshape(N, Dm // 32, 32)
+    amax = np.abs(g).max(axis=2, keepdims=True)
+    e = np.floor(np.log2(amax)) - 2
+    assert np.array_equal(sc.reshape(-1, Dm // 32)[slots], (e[..., 0] + 127).astype(np.uint8))
+    v = np.abs(g) / 2.0**e
+    half_step = np.where(v < 2, 0.25, np.where(v < 4, 0.5, 1.0)) * 2.0**e
+    err = np.abs(deq.reshape(N, Dm // 32, 32) - g)
+    assert np.all(err <= half_step * (1 + 1e-6) + np.where(v > 6, np.abs(g) - 6 * 2.0**e, 0))
+
+
 ALL_CHECKS = [
     check_bf16_decode, check_e4m3_decode, check_bf16_rounding, check_e8m0, check_e2m1,
     check_mxfp4_hand_rows, check_mxfp4_gather_hand, check_gather_invariant,
     check_logits_hand, check_logits_plain_matmul, check_logits_special,
     check_logits_invariances, check_logits_e4m3, check_logits_mxfp4_keys, check_topk_hand,
-    check_topk_bruteforce,
+    check_topk_bruteforce, check_e4m3_encode, check_e2m1_encode, check_q_rope_quant, check_k_hadamard_mxfp4,
 ]

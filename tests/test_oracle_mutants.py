@@ -45,6 +45,18 @@ MUTANTS = {
     "gather_offset": ("const int64_t row = blk * block_size + pos % block_size;",
                       "const int64_t row = blk * block_size + pos / block_size % block_size;"),
     "key_kind_ignored": ("} else if (k_kind == kE4M3) {", "} else if (k_kind != kBF16) {"),
+    "e4m3_ties_up": ("if (frac > 0.5 || (frac == 0.5 && std::fmod(r, 2.0) != 0.0)) r += 1.0;",
+                     "if (frac >= 0.5) r += 1.0;"),
+    "e4m3_no_saturation": ("  if (a > 448.0) a = 448.0;\n  double step;", "  double step;"),
+    "e4m3_subnormal_step": ("step = std::ldexp(1.0, -9);", "step = std::ldexp(1.0, -10);"),
+    "rope_pairs_split": ("const float x0 = y[2 * i], x1 = y[2 * i + 1];", "const float x0 = y[i], x1 = y[i + half];"),
+    "rope_sin_sign": ("y[2 * i] = p0 - p1;", "y[2 * i] = p0 + p1;"),
+    "q_fp8_max_fnuz": ("amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
+    "hadamard_sign": ("__builtin_popcount(static_cast<unsigned>(i & j)) & 1", "__builtin_popcount(static_cast<unsigned>(i | j)) & 1"),
+    "hadamard_unnormalised": ("y[i] = static_cast<float>(acc * norm);", "y[i] = static_cast<float>(acc);"),
+    "mx_shared_exp": ("sexp = (e2 - 1) - 2;", "sexp = (e2 - 1) - 1;"),
+    "e2m1_ties_odd": ("if (dc < db || (dc == db && (c & 1) == 0)) best = c;", "if (dc <= db) best = c;"),
+    "writer_nibble_order": ("static_cast<uint8_t>(lo | (hi << 4));", "static_cast<uint8_t>(hi | (lo << 4));"),
     "mxfp4_key_scale_row": ("static_cast<const uint8_t*>(k_scale) + row * (D / 32);",
                             "static_cast<const uint8_t*>(k_scale) + 0 * row * (D / 32);"),
 }
