@@ -148,6 +148,31 @@ dsa_status mxfp4_paged_gather(const uint8_t* kv_fp4, const uint8_t* kv_scale, in
                                          static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status dsa_indexer_q_rope_quant(const uint16_t* q, const int32_t* positions, const float* cos_sin,
+                                    int64_t max_pos, int rope_dim, int T, int H, int D, uint8_t* q_fp8,
+                                    float* q_scale, void* stream) {
+  if (D != 128) return DSA_ERR_UNSUPPORTED;
+  if (T < 0 || H < 1 || max_pos < 0) return DSA_ERR_INVALID_ARG;
+  if (rope_dim < 0 || rope_dim > D || rope_dim % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if ((int64_t)T * H == 0) return DSA_OK;
+  if (q == nullptr || positions == nullptr || q_fp8 == nullptr || q_scale == nullptr) return DSA_ERR_INVALID_ARG;
+  if (rope_dim > 0 && (cos_sin == nullptr || !aligned(cos_sin, 8))) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 8) || !aligned(q_fp8, 4) || !aligned(q_scale, 4)) return DSA_ERR_INVALID_ARG;
+  return cuda_status(launch_q_rope_quant(q, positions, cos_sin, max_pos, rope_dim, T, H, q_fp8, q_scale,
+                                         device_sm_count(), static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_indexer_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot_mapping, int64_t N, int D,
+                                        uint8_t* kv_fp4, uint8_t* kv_scale, int64_t num_rows, void* stream) {
+  if (D != 128) return DSA_ERR_UNSUPPORTED;
+  if (N < 0 || num_rows < 0) return DSA_ERR_INVALID_ARG;
+  if (N == 0) return DSA_OK;
+  if (k == nullptr || slot_mapping == nullptr || kv_fp4 == nullptr || kv_scale == nullptr) return DSA_ERR_INVALID_ARG;
+  if (!aligned(k, 8) || !aligned(kv_fp4, 2) || !aligned(kv_scale, 4)) return DSA_ERR_INVALID_ARG;
+  return cuda_status(launch_k_hadamard_mxfp4(k, slot_mapping, N, kv_fp4, kv_scale, num_rows, device_sm_count(),
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 size_t dsa_workspace_bytes(dsa_op op, dsa_dtype dtype, dsa_queries qs, int topk) {
   if (check_queries(qs) != DSA_OK || topk < 1 || topk > 2048) return 0;
   if (op == DSA_OP_TOPK) return plan_topk(qs, topk).ws_bytes;

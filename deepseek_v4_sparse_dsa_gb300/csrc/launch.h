@@ -82,6 +82,13 @@ cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_
                                 const int32_t* table, int64_t bt_stride, const int32_t* sel, int next_n,
                                 int topk, int64_t rows, uint16_t* out, int num_sms, cudaStream_t stream);
 
+// ------------------------------------------------------------------ producers (producer.cu)
+cudaError_t launch_q_rope_quant(const uint16_t* q, const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                                int rope_dim, int64_t T, int H, uint8_t* codes, float* scale, int num_sms,
+                                cudaStream_t stream);
+cudaError_t launch_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot, int64_t n, uint8_t* fp4, uint8_t* scale,
+                                    int64_t num_rows, int num_sms, cudaStream_t stream);
+
 // ------------------------------------------------------------------ per-TU device words
 #define DSA_DECLARE_TU_ERROR_ACCESSORS(name)                                        \
   cudaError_t tu_##name##_read_clear_error(unsigned int* out);                      \
@@ -105,6 +112,7 @@ DSA_DECLARE_TU_ERROR_ACCESSORS(indexer_bf16_logits)
 DSA_DECLARE_TU_ERROR_ACCESSORS(indexer_fp8_topk)
 DSA_DECLARE_TU_ERROR_ACCESSORS(indexer_fp8_logits)
 DSA_DECLARE_TU_ERROR_ACCESSORS(topk)
+DSA_DECLARE_TU_ERROR_ACCESSORS(producer)
 
 // Every translation unit's accessors, for dsa_device_error / dsa_set_wait_limit_ns.
 struct TuWords {
@@ -115,7 +123,7 @@ struct TuWords {
 inline const TuWords* all_tu_words(int* n) {
   static const TuWords w[] = {DSA_TU_WORDS(gather), DSA_TU_WORDS(indexer), DSA_TU_WORDS(indexer_bf16_topk),
                               DSA_TU_WORDS(indexer_bf16_logits), DSA_TU_WORDS(indexer_fp8_topk),
-                              DSA_TU_WORDS(indexer_fp8_logits), DSA_TU_WORDS(topk)};
+                              DSA_TU_WORDS(indexer_fp8_logits), DSA_TU_WORDS(topk), DSA_TU_WORDS(producer)};
   *n = (int)(sizeof(w) / sizeof(w[0]));
   return w;
 }

@@ -74,6 +74,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                     dsa_queries, c_int, c_void_p, c_void_p, c_void_p]),
         "mxfp4_paged_gather": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_int, c_void_p, c_int64,
                                        c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
+        "dsa_indexer_q_rope_quant": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int, c_int, c_int,
+                                             c_void_p, c_void_p, c_void_p]),
+        "dsa_indexer_k_hadamard_mxfp4": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_void_p, c_void_p, c_int64,
+                                                 c_void_p]),
         "dsa_workspace_bytes": (c_size_t, [c_int, c_int, dsa_queries, c_int]),
         "dsa_status_string": (ctypes.c_char_p, [c_int]),
         "dsa_device_error": (c_int, [c_void_p]),
@@ -156,6 +160,18 @@ def mxfp4_paged_gather(kv_fp4, kv_scale, num_blocks, block_size, D, block_table,
     _check(load().mxfp4_paged_gather(_ptr(kv_fp4), _ptr(kv_scale), int(num_blocks), int(block_size), int(D),
                                      _ptr(block_table), int(bt_stride), _ptr(sel_pos), int(B), int(next_n),
                                      int(topk), _ptr(out), _stream(stream)), "mxfp4_paged_gather")
+
+
+def dsa_indexer_q_rope_quant(q, positions, cos_sin, max_pos, rope_dim, T, H, D, q_fp8, q_scale, stream=None):
+    _check(load().dsa_indexer_q_rope_quant(_ptr(q), _ptr(positions), _ptr(cos_sin), int(max_pos), int(rope_dim),
+                                           int(T), int(H), int(D), _ptr(q_fp8), _ptr(q_scale), _stream(stream)),
+           "dsa_indexer_q_rope_quant")
+
+
+def dsa_indexer_k_hadamard_mxfp4(k, slot_mapping, N, D, kv_fp4, kv_scale, num_rows, stream=None):
+    _check(load().dsa_indexer_k_hadamard_mxfp4(_ptr(k), _ptr(slot_mapping), int(N), int(D), _ptr(kv_fp4),
+                                               _ptr(kv_scale), int(num_rows), _stream(stream)),
+           "dsa_indexer_k_hadamard_mxfp4")
 
 
 def dsa_workspace_bytes(op, dtype, qs, topk) -> int:

@@ -178,6 +178,53 @@ dsa_status mxfp4_paged_gather(const uint8_t* kv_fp4, const uint8_t* kv_scale, in
                               uint16_t* out, void* stream);
 
 /*
+ * dsa_indexer_q_rope_quant -- the indexer-query producer ahead of the score (vllm PR #1
+ * "Sparse-MLA bring-up on MI300X", "Root cause story" item 3: a fused RoPE + FP8
+ * quantisation of the indexer query whose bytes the fp8 MQA-logits reader consumes;
+ * FP8_MAX = 448 on the OCP path).  For every (token t, head h) row of q:
+ *   1. RoPE: for i < rope_dim / 2 the pair (x[2i], x[2i+1]) becomes
+ *      (x0 c - x1 s, x0 s + x1 c) with c = cos_sin[p * rope_dim + i],
+ *      s = cos_sin[p * rope_dim + rope_dim / 2 + i], p = positions[t]; dims >= rope_dim
+ *      pass through (this library's reading: interleaved pairs, a caller-built table);
+ *   2. q_scale[t, h] = max_d |y[d]| / 448 (1 for an all-zero row);
+ *   3. q_fp8[t, h, d] = E4M3(y[d] / q_scale[t, h]), nearest even, saturating at +-448.
+ * All arithmetic in fp32, each product and sum rounded on its own.  The output is the
+ * (q, q_scale) pair dsa_indexer_logits* take with dtype DSA_E4M3.
+ *  q        [T, H, D] bf16 bit patterns, 8-byte aligned.
+ *  positions [T] int32; a position outside [0, max_pos) gives a zero row (codes 0,
+ *           scale 0) and sets DSA_DEVERR_INDEX.
+ *  cos_sin  [max_pos, rope_dim] fp32 (rope_dim / 2 cosines, then rope_dim / 2 sines per
+ *           position), 8-byte aligned; may be NULL when rope_dim == 0.
+ *  q_fp8    [T, H, D] E4M3 codes (4-byte aligned); q_scale [T, H] fp32.
+ * D must be 128 (DSA_ERR_UNSUPPORTED otherwise); rope_dim a multiple of 4, <= D.
+ */
+dsa_status dsa_indexer_q_rope_quant(const uint16_t* q, const int32_t* positions, const float* cos_sin,
+                                    int64_t max_pos, int rope_dim, int T, int H, int D, uint8_t* q_fp8,
+                                    float* q_scale, void* stream);
+
+/*
+ * dsa_indexer_k_hadamard_mxfp4 -- the indexer-key compressor's write into the paged FP4
+ * cache (ROCm/ATOM issue #707, "CSA": "CSA Indexer Compressor (head_dim=128, Hadamard,
+ * FP4)").  For every key n with pool row r = slot_mapping[n] >= 0:
+ *   y = H k[n] / sqrt(128), H the Sylvester-ordered Walsh-Hadamard matrix
+ *       (H[i][j] = (-1)^popcount(i & j)), in fp32;
+ *   per 32-element group g: kv_scale[r, g] = E8M0 byte floor(log2(amax_g)) - 2 + 127
+ *       (clamped to >= 0; 0 for an all-zero group), and each element is the nearest E2M1
+ *       code of y / 2^(byte - 127) (ties to the even code, saturating at 6; zero results
+ *       are +0), packed two per byte of kv_fp4[r], low nibble = even element
+ *       (the OCP MX v1.0 conversion, in the layout mxfp4_paged_gather reads).
+ *  k            [N, D] bf16 bit patterns, 8-byte aligned.
+ *  slot_mapping [N] int64 pool rows (block * block_size + offset); < 0: key skipped;
+ *               >= num_rows: skipped and DSA_DEVERR_INDEX set.
+ *  kv_fp4       [num_rows, D/2] bytes; kv_scale [num_rows, D/32] bytes (4-byte aligned).
+ * D must be 128.  The transform is summed by butterflies in fp32: a code can differ
+ * from the one of the exactly rounded rotation only where that value lies within a few
+ * fp32 ulps of an E2M1 rounding boundary.
+ */
+dsa_status dsa_indexer_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot_mapping, int64_t N, int D,
+                                        uint8_t* kv_fp4, uint8_t* kv_scale, int64_t num_rows, void* stream);
+
+/*
  * dsa_indexer_logits_topk_noalloc -- dsa_indexer_logits_topk for callers that cannot
  * allocate device memory: a process whose device memory is all reserved at start-up
  * and handed out by its own pool, or a latency-critical loop that cannot afford

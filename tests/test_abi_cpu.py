@@ -131,6 +131,22 @@ def test_host_side_rejections_launch_nothing(lib):
     assert dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, huge, 512) == 0
     assert _status(dsa.dsa_indexer_logits_topk, FAKE, None, dsa.DSA_BF16, FAKE, 64, 128, pkeys, huge, 512, FAKE,
                    None, FAKE, 1 << 40, s) == dsa.DSA_ERR_UNSUPPORTED
+    # producers: head dim, RoPE width, misalignment, empty batches
+    assert _status(dsa.dsa_indexer_q_rope_quant, FAKE, FAKE, FAKE, 100, 64, 4, 64, 64, FAKE, FAKE, s) \
+        == dsa.DSA_ERR_UNSUPPORTED
+    for rope in (-4, 66, 132):
+        assert _status(dsa.dsa_indexer_q_rope_quant, FAKE, FAKE, FAKE, 100, rope, 4, 64, 128, FAKE, FAKE, s) \
+            == dsa.DSA_ERR_INVALID_ARG
+    assert _status(dsa.dsa_indexer_q_rope_quant, FAKE + 4, FAKE, FAKE, 100, 64, 4, 64, 128, FAKE, FAKE, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    assert _status(dsa.dsa_indexer_q_rope_quant, FAKE, FAKE, None, 100, 64, 4, 64, 128, FAKE, FAKE, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    assert _status(dsa.dsa_indexer_q_rope_quant, None, None, None, 0, 0, 0, 64, 128, None, None, s) == dsa.DSA_OK
+    assert _status(dsa.dsa_indexer_k_hadamard_mxfp4, FAKE, FAKE, 10, 64, FAKE, FAKE, 100, s) \
+        == dsa.DSA_ERR_UNSUPPORTED
+    assert _status(dsa.dsa_indexer_k_hadamard_mxfp4, FAKE, FAKE, 10, 128, FAKE, FAKE + 2, 100, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    assert _status(dsa.dsa_indexer_k_hadamard_mxfp4, None, None, 0, 128, None, None, 0, s) == dsa.DSA_OK
     # empty problems are valid no-ops
     assert _status(dsa.mxfp4_paged_gather, None, None, 0, 64, 128, None, 0, None, 0, 1, 512, None, s) == dsa.DSA_OK
     assert dsa.dsa_launch_count() == before
