@@ -604,6 +604,131 @@ __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k
   return (uint64_t)tord << 32;
 }
 
+// Exact cut-back: keeps exactly the k largest of the (distinct, nonzero) keys of buf[0, n),
+// packed to the front (*cnt = k), and returns the k-th largest key, the row's new
+// threshold.  One 512-bin histogram of the value images (as in engine_cut_approx) finds
+// the bin holding the k-th key; the few keys in that bin are sorted by one warp to
+// name the k-th key exactly; only when that bin holds more than 64 keys (values packed
+// closely, e.g. ties) does the exact radix select over the whole buffer decide.
+// Returns 0 (buffer untouched) when there are at most k keys.  `bins` holds 512 words of
+// shared scratch; needs n <= NT * MAXPER.
+template <int KPL>
+__device__ __forceinline__ void warp_sort_regs(uint64_t (&x)[KPL]);
+
+template <int NT, int MAXPER>
+__device__ uint64_t engine_cut_exact(uint64_t* buf, uint32_t* cnt, int n, int k, uint32_t* bins, EngineScratch* sc,
+                                     int tid, int bar = 1) {
+  constexpr int NW = NT / 32;
+  constexpr int BPT = kCutBins / NT;
+  static_assert(kCutBins % NT == 0 && NW <= 16, "group size");
+  const int lane = tid & 31, w = tid >> 5;
+  uint64_t keep[MAXPER];
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u, nz = 0u;
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i) {
+    const int e = tid + i * NT;
+    keep[i] = (e < n) ? buf[e] : 0ull;
+    if (keep[i]) {
+      const uint32_t o = (uint32_t)(keep[i] >> 32);
+      lo = min(lo, o);
+      hi = max(hi, o);
+      ++nz;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+    nz += __shfl_xor_sync(0xFFFFFFFFu, nz, o);
+  }
+  uint32_t* wred = sc->hist;                        // [0, 3 * NW): per-warp lo, hi, count
+  if (lane == 0) {
+    wred[w] = lo;
+    wred[NW + w] = hi;
+    wred[2 * NW + w] = nz;
+  }
+  for (int i = tid; i < kCutBins; i += NT) bins[i] = 0u;
+  group_sync<NT>(bar);
+  lo = 0xFFFFFFFFu;
+  hi = 0u;
+  nz = 0u;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    lo = min(lo, wred[i]);
+    hi = max(hi, wred[NW + i]);
+    nz += wred[2 * NW + i];
+  }
+  if (nz <= (uint32_t)k) {
+    group_sync<NT>(bar);                               // wred is read before it is reused
+    return 0ull;
+  }
+  const uint64_t span = (uint64_t)(hi - lo) + 1u;
+  const uint32_t mul = (uint32_t)min(((uint64_t)kCutBins << 32) / span, (uint64_t)0xFFFFFFFFu);
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i)
+    if (keep[i]) atomicAdd(&bins[cut_bin((uint32_t)(keep[i] >> 32), lo, mul)], 1u);
+  group_sync<NT>(bar);
+  // bin b holding the k-th key from the top, and the count of keys in the bins above it
+  uint32_t c[BPT], sum = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    c[i] = bins[kCutBins - 1 - tid * BPT - i];
+    sum += c[i];
+  }
+  uint32_t incl = sum;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t* wsum = sc->hist + 3 * NW;               // [3 * NW, 4 * NW): per-warp totals
+  if (lane == 31) wsum[w] = incl;
+  group_sync<NT>(bar);
+  uint32_t before = 0;
+  for (int i = 0; i < w; ++i) before += wsum[i];
+  uint32_t above = before + incl - sum;
+  if (above < (uint32_t)k && (uint32_t)k <= above + sum) {
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      if (above < (uint32_t)k && (uint32_t)k <= above + c[i]) {
+        sc->pick[0] = (uint32_t)(kCutBins - 1 - tid * BPT - i);
+        sc->pick[1] = above;                        // keys in the bins above b
+        sc->pick[2] = c[i];                         // keys in bin b
+      }
+      above += c[i];
+    }
+  }
+  group_sync<NT>(bar);
+  const uint32_t b = sc->pick[0], abv = sc->pick[1], inb = sc->pick[2];
+  uint64_t thr;
+  if (inb <= 64u) {
+    // the keys of bin b into a short list (bins is free again), sorted by warp 0
+    uint64_t* list = reinterpret_cast<uint64_t*>(bins);
+    if (tid == 0) sc->pick[3] = 0u;
+    if (tid < 64) list[tid] = 0ull;
+    group_sync<NT>(bar);
+#pragma unroll
+    for (int i = 0; i < MAXPER; ++i) {
+      if (keep[i] && cut_bin((uint32_t)(keep[i] >> 32), lo, mul) == b) {
+        const uint32_t at = atomicAdd(&sc->pick[3], 1u);
+        if (at < 64u) list[at] = keep[i];
+      }
+    }
+    group_sync<NT>(bar);
+    if (w == 0) {
+      uint64_t x[2] = {list[lane], list[32 + lane]};
+      warp_sort_regs<2>(x);                         // descending: element e = r * 32 + lane
+      const uint32_t need = (uint32_t)k - abv;      // 1 <= need <= inb
+      const uint32_t e = need - 1u;
+      if (lane == (int)(e & 31u)) list[64] = x[e >> 5];
+    }
+    group_sync<NT>(bar);
+    thr = list[64];
+  } else {
+    thr = engine_select<NT>(buf, n, k, sc, tid, bar);
+  }
+  engine_scatter<NT, MAXPER, false>(buf, cnt, keep, thr, 0u, 0u, 0u, sc, tid, bar);
+  return thr;
+}
+
 // Keeps the keys >= thr of buf[0, n), packed to the front; *cnt becomes their
 // number.  Holds the keys in registers meanwhile: needs n <= NT * MAXPER.  The caller
 // has passed a group barrier since buf and n were last written.
