@@ -3,13 +3,12 @@
 // paged cache of E2M1 nibbles (low nibble = even element) with one E8M0 scale per 32
 // elements (2^(b-127), 0xFF -> 0), dequantised to bf16; padded slots give zero rows.
 //
-// HBM-bound: 68 bytes read and 256 bytes written per live row.  A warp owns R rows per
-// step (32, or 16 / 8 when the batch is small, so every SM gets warps).  Each lane
-// resolves one row's source (sel_pos -> block table -> cache row); the warp then moves
-// the rows two at a time, 16 lanes per row: a lane loads 4 nibble bytes (8 elements)
-// and their scale byte and writes 16 bytes, so every store instruction writes two whole
-// 256-byte rows.  The next step's positions and block-table entries are fetched while
-// the current rows are in flight.
+// HBM-bound: 68 bytes read and 256 bytes written per live row.  A warp owns 32 rows per
+// step.  Each lane resolves one row's source (sel_pos -> block table -> cache row); the
+// warp then moves the rows two at a time, 16 lanes per row: a lane loads 4 nibble bytes
+// (8 elements) and their scale byte and writes 16 bytes, so every store instruction
+// writes two whole 256-byte rows.  The next step's positions and block-table entries
+// are fetched while the current rows are in flight.
 #include "common.cuh"
 #include "launch.h"
 
@@ -108,13 +107,7 @@ __device__ __forceinline__ int64_t gather_source(const GatherArgs& g, int64_t r,
   return -1;
 }
 
-// R rows per warp step (8, 16 or 32): lanes 0..R-1 resolve one row each, then the warp
-// moves them two at a time, up to 8 pairs per batch of loads.  Small batches use R = 8
-// so that enough warps (rows in flight) cover every SM.
-template <int R>
 __global__ void __launch_bounds__(256) mxfp4_gather_kernel(const GatherArgs g) {
-  constexpr int KP = (R / 2) < 8 ? (R / 2) : 8;   // row pairs per batch of loads
-  constexpr int NB = (R / 2) / KP;                // batches per step
   __shared__ uint2 lut[256];
   lut[threadIdx.x] = lut_entry(threadIdx.x);
   __syncthreads();
@@ -124,23 +117,23 @@ __global__ void __launch_bounds__(256) mxfp4_gather_kernel(const GatherArgs g) {
   const int64_t step = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int sub = (int)(lane >> 4);    // row within a pair
   const int part = (int)(lane & 15u);  // elements 8 * part .. 8 * part + 7
-  int64_t r0 = warp * R;
+  int64_t r0 = warp * 32;
   int64_t src_next = -1;
-  if (r0 < g.rows && lane < (uint32_t)R) {
+  if (r0 < g.rows) {
     const int64_t r = r0 + lane;
     src_next = gather_source(g, r, r < g.rows ? __ldg(g.sel + r) : -1);
   }
-  for (; r0 < g.rows; r0 += step * R) {
+  for (; r0 < g.rows; r0 += step * 32) {
     const int64_t src = src_next;
-    const int64_t r1 = r0 + step * R + lane;
-    const int32_t pos_next = (lane < (uint32_t)R && r1 < g.rows) ? __ldg(g.sel + r1) : -1;   // in flight meanwhile
+    const int64_t r1 = r0 + step * 32 + lane;
+    const int32_t pos_next = r1 < g.rows ? __ldg(g.sel + r1) : -1;   // in flight meanwhile
 #pragma unroll
-    for (int h = 0; h < NB; ++h) {
-      uint32_t w[KP], sb[KP];
-      int64_t srow[KP];
+    for (int h = 0; h < 2; ++h) {
+      uint32_t w[8], sb[8];
+      int64_t srow[8];
 #pragma unroll
-      for (int k = 0; k < KP; ++k) {
-        srow[k] = __shfl_sync(0xFFFFFFFFu, src, h * 2 * KP + 2 * k + sub);
+      for (int k = 0; k < 8; ++k) {
+        srow[k] = __shfl_sync(0xFFFFFFFFu, src, h * 16 + 2 * k + sub);
         w[k] = 0u;
         sb[k] = 255u;
         if (srow[k] >= 0) {
@@ -148,10 +141,10 @@ __global__ void __launch_bounds__(256) mxfp4_gather_kernel(const GatherArgs g) {
           sb[k] = __ldg(g.scale + srow[k] * 4 + (part >> 2));
         }
       }
-      if (h == 0) src_next = lane < (uint32_t)R ? gather_source(g, r1, pos_next) : -1;
+      if (h == 0) src_next = gather_source(g, r1, pos_next);
 #pragma unroll
-      for (int k = 0; k < KP; ++k) {
-        const int64_t row = r0 + h * 2 * KP + 2 * k + sub;
+      for (int k = 0; k < 8; ++k) {
+        const int64_t row = r0 + h * 16 + 2 * k + sub;
         if (row >= g.rows) continue;
         const uint4 v = srow[k] >= 0 ? decode8(w[k], sb[k], lut) : make_uint4(0u, 0u, 0u, 0u);
         st_stream(reinterpret_cast<uint4*>(g.out + row * 128) + part, v);
@@ -165,12 +158,9 @@ cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_
                                 int topk, int64_t rows, uint16_t* out, int num_sms, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   GatherArgs g{fp4, scale, num_blocks, bs, table, bt_stride, sel, (int64_t)next_n * topk, rows, out};
-  const int64_t cap = (int64_t)num_sms * 8;   // resident blocks of 256 threads per SM
-  // rows per warp step: 32 when that still gives every resident warp work, fewer otherwise
-  int R = 32;
-  while (R > 8 && (rows + R - 1) / R < cap * 8) R >>= 1;
-  const int64_t warps_needed = (rows + R - 1) / R;
+  const int64_t warps_needed = (rows + 31) / 32;
   const int64_t blocks_needed = (warps_needed + 7) / 8;
+  const int64_t cap = (int64_t)num_sms * 4;   // resident blocks of 256 threads per SM
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(blocks_needed < cap ? blocks_needed : cap));
   cfg.blockDim = dim3(256);
@@ -180,10 +170,7 @@ cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e;
-  if (R == 32) e = cudaLaunchKernelEx(&cfg, mxfp4_gather_kernel<32>, g);
-  else if (R == 16) e = cudaLaunchKernelEx(&cfg, mxfp4_gather_kernel<16>, g);
-  else e = cudaLaunchKernelEx(&cfg, mxfp4_gather_kernel<8>, g);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, mxfp4_gather_kernel, g);
   note_launch();
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -198,14 +198,15 @@ constexpr size_t kSmemLimit = 232448;   // max dynamic shared memory per CTA (22
 constexpr size_t kSmemHalf = 115712;    // two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
 constexpr int64_t kSplitUnits = 1216;   // logits mode: fewer query groups than this: split key chunks
 
-size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap) {
+size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap, int ring = 0) {
   const size_t elt = fp8 ? 1 : 2;
   size_t s = 1024;                                    // alignment slack
   s += (size_t)nq * 64 * 128 * elt;                  // Q tile
   s += (size_t)stages * 128 * 128 * elt;             // key ring
-  s += (size_t)(2 * stages + 16) * 8;                // barriers
+  s += (size_t)(2 * stages + 16 + 2 * ring) * 8;     // barriers
   s += sizeof(EpiSmem<4>) + 16;
   if (topk) s += (size_t)nq * cap * 8;
+  s += (size_t)ring * nq * 128 * 4;                  // score ring (selector mode)
   return s;
 }
 
@@ -252,6 +253,26 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
   if (pl.ctas_per_sm == 1 && pl.nq >= 2) pl.eg = 2;   // one CTA per SM: two groups take turns
   if (tk && (pl.cap < topk + 256 || pl.cap < pl.pow2)) pl.ok = false;
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
+  // Selector mode for four-row items: one head-sum group + one selector group, a score
+  // ring of 16 (E4M3) / 8 (bf16) tiles between them, 4 / 3 key stages, and the largest
+  // candidate buffers that still fit (the bigger the buffer, the rarer the cut-backs).
+  pl.sel = false;
+  pl.ring = 0;
+  if (tk && pl.nq == 4) {
+    const int ring = fp8 ? 16 : 8, st = fp8 ? 4 : 3;
+    const size_t fixed = smem_bytes(fp8, 4, st, true, 0, ring);
+    int cap = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / (4 * 8)) / 256 * 256 : 0;
+    if (cap > 128 * kSelMaxPer) cap = 128 * kSelMaxPer;
+    if (cap >= topk + 512 && cap >= pl.pow2) {
+      pl.sel = true;
+      pl.ring = ring;
+      pl.stages = st;
+      pl.cap = cap;
+      pl.eg = 1;
+      pl.ctas_per_sm = 1;
+      pl.smem = smem_bytes(fp8, 4, st, true, cap, ring);
+    }
+  }
   // as many accumulator buffers (up to 4) as TMEM holds for the CTAs sharing an SM, so
   // the MMAs can run ahead of an epilogue busy cutting its candidates back
   pl.nbuf_log2 = 2;
@@ -327,6 +348,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   prm.chunk = pl.chunk;
   prm.stages = pl.stages;
   prm.nbuf_log2 = pl.nbuf_log2;
+  prm.ring = pl.ring;
   prm.logits = a.logits;
   prm.ld = a.ld;
   prm.topk = a.topk;

@@ -31,6 +31,9 @@ struct IndexerPlan {
   int64_t items;     // logits mode: work items; top-k mode: query groups
   size_t ws_bytes;   // workspace bytes (top-k mode)
   size_t prefix_off, ufirst_off, split_off, order_off, partial_off, meta_off;   // byte offsets in ws
+  bool sel;          // top-k mode, four query rows per item: head-sum warps hand the scores
+                     // to separate selector warps through a ring of `ring` tiles
+  int ring;          // selector mode: score-ring slots
   bool ok;           // false: shape does not fit this build
 };
 
