@@ -604,30 +604,29 @@ __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k
   return (uint64_t)tord << 32;
 }
 
-// Exact cut-back: keeps exactly the k largest of the (distinct, nonzero) keys of buf[0, n),
-// packed to the front (*cnt = k), and returns the k-th largest key, the row's new
-// threshold.  One 512-bin histogram of the value images (as in engine_cut_approx) finds
-// the bin holding the k-th key; the few keys in that bin are sorted by one warp to
-// name the k-th key exactly; only when that bin holds more than 64 keys (values packed
-// closely, e.g. ties) does the exact radix select over the whole buffer decide.
-// Returns 0 (buffer untouched) when there are at most k keys.  `bins` holds 512 words of
-// shared scratch; needs n <= NT * MAXPER.
+// Exact cut-back of a candidate set held in registers: keep[] holds every candidate of
+// the set (distinct nonzero keys; zero = empty) spread over the group's threads.  The k
+// largest (all of them when there are at most k) are written to the front of buf, *cnt
+// becomes their number, and the k-th largest key (1 when all are kept) is returned: the
+// set's new threshold.  One 512-bin histogram of the value images finds the bin holding
+// the k-th key; the few keys in that bin are sorted by one warp to name the k-th key
+// exactly; only when the bin holds more than 64 keys (values packed closely, e.g. ties)
+// does the exact radix select over the (compacted) set decide.  `bins` holds 512 words of
+// shared scratch; buf must have room for every candidate (the writes may overwrite any
+// of the slots the candidates came from: they are all in keep[] already).
 template <int KPL>
 __device__ __forceinline__ void warp_sort_regs(uint64_t (&x)[KPL]);
 
 template <int NT, int MAXPER>
-__device__ uint64_t engine_cut_exact(uint64_t* buf, uint32_t* cnt, int n, int k, uint32_t* bins, EngineScratch* sc,
-                                     int tid, int bar = 1) {
+__device__ uint64_t engine_cut_exact_keep(uint64_t* buf, uint32_t* cnt, const uint64_t (&keep)[MAXPER], int k,
+                                          uint32_t* bins, EngineScratch* sc, int tid, int bar = 1) {
   constexpr int NW = NT / 32;
   constexpr int BPT = kCutBins / NT;
   static_assert(kCutBins % NT == 0 && NW <= 16, "group size");
   const int lane = tid & 31, w = tid >> 5;
-  uint64_t keep[MAXPER];
   uint32_t lo = 0xFFFFFFFFu, hi = 0u, nz = 0u;
 #pragma unroll
   for (int i = 0; i < MAXPER; ++i) {
-    const int e = tid + i * NT;
-    keep[i] = (e < n) ? buf[e] : 0ull;
     if (keep[i]) {
       const uint32_t o = (uint32_t)(keep[i] >> 32);
       lo = min(lo, o);
@@ -657,9 +656,10 @@ __device__ uint64_t engine_cut_exact(uint64_t* buf, uint32_t* cnt, int n, int k,
     hi = max(hi, wred[NW + i]);
     nz += wred[2 * NW + i];
   }
-  if (nz <= (uint32_t)k) {
-    group_sync<NT>(bar);                               // wred is read before it is reused
-    return 0ull;
+  group_sync<NT>(bar);                              // wred is read before it is reused
+  if (nz <= (uint32_t)k) {                          // keep them all, compacted
+    engine_scatter<NT, MAXPER, false>(buf, cnt, keep, 1ull, 0u, 0u, 0u, sc, tid, bar);
+    return 1ull;
   }
   const uint64_t span = (uint64_t)(hi - lo) + 1u;
   const uint32_t mul = (uint32_t)min(((uint64_t)kCutBins << 32) / span, (uint64_t)0xFFFFFFFFu);
@@ -716,14 +716,15 @@ __device__ uint64_t engine_cut_exact(uint64_t* buf, uint32_t* cnt, int n, int k,
     if (w == 0) {
       uint64_t x[2] = {list[lane], list[32 + lane]};
       warp_sort_regs<2>(x);                         // descending: element e = r * 32 + lane
-      const uint32_t need = (uint32_t)k - abv;      // 1 <= need <= inb
-      const uint32_t e = need - 1u;
+      const uint32_t e = (uint32_t)k - abv - 1u;    // the (k - abv)-th largest of the bin
       if (lane == (int)(e & 31u)) list[64] = x[e >> 5];
     }
     group_sync<NT>(bar);
     thr = list[64];
   } else {
-    thr = engine_select<NT>(buf, n, k, sc, tid, bar);
+    // compact the set to the front of buf, then the exact radix select over it
+    engine_scatter<NT, MAXPER, false>(buf, cnt, keep, 1ull, 0u, 0u, 0u, sc, tid, bar);
+    thr = engine_select<NT>(buf, (int)nz, k, sc, tid, bar);
   }
   engine_scatter<NT, MAXPER, false>(buf, cnt, keep, thr, 0u, 0u, 0u, sc, tid, bar);
   return thr;
@@ -837,6 +838,112 @@ __device__ __forceinline__ void warp_sort_regs(uint64_t (&x)[KPL]) {
         }
       }
     }
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// mxfp4 decode (E2M1 nibbles, low nibble first, times an E8M0 group scale 2^(b-127),
+// 0xFF -> 0), shared by the gather and the FP4-key score (xkernels issue #28
+// "DeepSeek-V4 serving support -- tracking", comment 2 "What it does").
+// ---------------------------------------------------------------------------------
+// bf16 bit pattern of E2M1 nibble n times 2^(b-127), b != 0xFF, exact except overflow.
+// Nonzero magnitudes are (2 + M) * 2^X with (M, X) = (0,-2), (0,-1), (1,-1), (0,0), (1,0),
+// (0,1), (1,1) for codes 1..7; the bf16 exponent field is E = X + b + 1 = e + b - 1 for
+// code = 2e + m (e >= 1) and b - 1 for code 1.
+__device__ __forceinline__ uint32_t e2m1_bf16_general(uint32_t n, int b) {
+  const uint32_t s = (n & 8u) << 12;
+  const uint32_t c = n & 7u;
+  if (c == 0u || b == 255) return s;
+  const int e = (int)(c >> 1);
+  const uint32_t M = (c > 1u) ? (c & 1u) : 0u;
+  const int E = b - 1 + e;
+  if (E >= 255) return s | 0x7F80u;                           // beyond bf16 range -> inf
+  if (E >= 1) return s | ((uint32_t)E << 7) | (M << 6);        // normal
+  return s | ((2u + M) << (E + 5));                            // subnormal (E = 0 or -1)
+}
+
+// Fast form for 2 <= b <= 252 (every code lands in the normal range):
+// bits = ((b-1) << 7) + (code << 6), minus 64 for code 1; code 0 -> signed zero.
+__device__ __forceinline__ uint32_t e2m1_bf16_fast(uint32_t n, uint32_t base) {
+  const uint32_t s = (n & 8u) << 12;
+  const uint32_t c = n & 7u;
+  const uint32_t v = base + (c << 6) - (c == 1u ? 64u : 0u);
+  return (c != 0u ? v : 0u) | s;
+}
+
+// Decode table: entry `byte` holds the bf16 pair of its two nibbles (low nibble in the
+// low half) at scale byte b = 2, and a mask of the nonzero halves.  For 2 <= b <= 252
+// the pair at scale b is entry + ((b - 2) << 7 in both halves, masked): that moves the
+// exponent field of each nonzero half (at most 0x7F40 with the sign clear, so no carry
+// crosses a half) and leaves signed zeros alone.
+__device__ __forceinline__ uint2 lut_entry(uint32_t byte) {
+  uint32_t v = 0, m = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t n = (byte >> (4 * h)) & 0xFu;
+    v |= e2m1_bf16_fast(n, 1u << 7) << (16 * h);
+    if (n & 7u) m |= 0xFFFFu << (16 * h);
+  }
+  return make_uint2(v, m);
+}
+
+// Eight elements (nibble bytes of w, low nibble first) times 2^(b-127) as bf16 pairs.
+__device__ __forceinline__ uint4 decode8(uint32_t w, uint32_t b, const uint2* lut) {
+  uint32_t o[4];
+  if (b >= 2u && b <= 252u) {
+    const uint32_t adj = ((b - 2u) << 7) * 0x10001u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint2 e = lut[(w >> (8 * k)) & 0xFFu];
+      o[k] = e.x + (adj & e.y);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t byte = (w >> (8 * k)) & 0xFFu;
+      o[k] = e2m1_bf16_general(byte & 0xFu, (int)b) | (e2m1_bf16_general(byte >> 4, (int)b) << 16);
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One warp: sorts the cn (<= 32 * KPL) keys at buf in registers and writes the first
+// k of them as the row's indices (and values), -1 / -inf past the candidates.
+template <int KPL>
+__device__ __forceinline__ void rank_row(const uint64_t* buf, int cn, int k, bool real, int32_t* out_idx,
+                                         float* out_val) {
+  const int lane = threadIdx.x & 31;
+  uint64_t x[KPL];
+#pragma unroll
+  for (int r = 0; r < KPL; ++r) {
+    const int e = r * 32 + lane;
+    x[r] = e < cn ? buf[e] : 0ull;
+  }
+  warp_sort_regs<KPL>(x);
+  if (!real) return;
+#pragma unroll
+  for (int r = 0; r < KPL; ++r) {
+    const int s = r * 32 + lane;
+    if (s < k) {
+      out_idx[s] = x[r] ? index_of_key(x[r]) : -1;
+      if (out_val) out_val[s] = x[r] ? value_of_key(x[r]) : -INFINITY;
+    }
+  }
+}
+
+// As rank_row for rows of more than 1024 keys: zero-pads buf to P, sorts it in shared
+// memory with one warp.
+__device__ __forceinline__ void rank_row_smem(uint64_t* buf, int cn, int P, int k, bool real, int32_t* out_idx,
+                                              float* out_val) {
+  const int lane = threadIdx.x & 31;
+  for (int e = cn + lane; e < P; e += 32) buf[e] = 0ull;
+  __syncwarp();
+  warp_sort(buf, P);
+  if (!real) return;
+  for (int s = lane; s < k; s += 32) {
+    const uint64_t key = buf[s];
+    out_idx[s] = key ? index_of_key(key) : -1;
+    if (out_val) out_val[s] = key ? value_of_key(key) : -INFINITY;
   }
 }
 

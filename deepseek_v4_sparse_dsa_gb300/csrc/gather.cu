@@ -14,67 +14,6 @@
 
 namespace dsa {
 
-// bf16 bit pattern of E2M1 nibble n times 2^(b-127), b != 0xFF, exact except overflow.
-// Nonzero magnitudes are (2 + M) * 2^X with (M, X) = (0,-2), (0,-1), (1,-1), (0,0), (1,0),
-// (0,1), (1,1) for codes 1..7; the bf16 exponent field is E = X + b + 1 = e + b - 1 for
-// code = 2e + m (e >= 1) and b - 1 for code 1.
-__device__ __forceinline__ uint32_t e2m1_bf16_general(uint32_t n, int b) {
-  const uint32_t s = (n & 8u) << 12;
-  const uint32_t c = n & 7u;
-  if (c == 0u || b == 255) return s;
-  const int e = (int)(c >> 1);
-  const uint32_t M = (c > 1u) ? (c & 1u) : 0u;
-  const int E = b - 1 + e;
-  if (E >= 255) return s | 0x7F80u;                           // beyond bf16 range -> inf
-  if (E >= 1) return s | ((uint32_t)E << 7) | (M << 6);        // normal
-  return s | ((2u + M) << (E + 5));                            // subnormal (E = 0 or -1)
-}
-
-// Fast form for 2 <= b <= 252 (every code lands in the normal range):
-// bits = ((b-1) << 7) + (code << 6), minus 64 for code 1; code 0 -> signed zero.
-__device__ __forceinline__ uint32_t e2m1_bf16_fast(uint32_t n, uint32_t base) {
-  const uint32_t s = (n & 8u) << 12;
-  const uint32_t c = n & 7u;
-  const uint32_t v = base + (c << 6) - (c == 1u ? 64u : 0u);
-  return (c != 0u ? v : 0u) | s;
-}
-
-// Decode table: entry `byte` holds the bf16 pair of its two nibbles (low nibble in the
-// low half) at scale byte b = 2, and a mask of the nonzero halves.  For 2 <= b <= 252
-// the pair at scale b is entry + ((b - 2) << 7 in both halves, masked): that moves the
-// exponent field of each nonzero half (at most 0x7F40 with the sign clear, so no carry
-// crosses a half) and leaves signed zeros alone.
-__device__ __forceinline__ uint2 lut_entry(uint32_t byte) {
-  uint32_t v = 0, m = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t n = (byte >> (4 * h)) & 0xFu;
-    v |= e2m1_bf16_fast(n, 1u << 7) << (16 * h);
-    if (n & 7u) m |= 0xFFFFu << (16 * h);
-  }
-  return make_uint2(v, m);
-}
-
-// Eight elements (nibble bytes of w, low nibble first) times 2^(b-127) as bf16 pairs.
-__device__ __forceinline__ uint4 decode8(uint32_t w, uint32_t b, const uint2* lut) {
-  uint32_t o[4];
-  if (b >= 2u && b <= 252u) {
-    const uint32_t adj = ((b - 2u) << 7) * 0x10001u;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint2 e = lut[(w >> (8 * k)) & 0xFFu];
-      o[k] = e.x + (adj & e.y);
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t byte = (w >> (8 * k)) & 0xFFu;
-      o[k] = e2m1_bf16_general(byte & 0xFu, (int)b) | (e2m1_bf16_general(byte >> 4, (int)b) << 16);
-    }
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)

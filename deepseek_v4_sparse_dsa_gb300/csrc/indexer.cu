@@ -36,7 +36,7 @@ __device__ __forceinline__ int group_tiles(const int32_t* context_lens, int u, i
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ context_lens, int B, int next_n,
                                                     int causal, int max_len, int nq, int ngroups, int slices,
                                                     int cost, int32_t* plan, int32_t* prefix, int32_t* ufirst,
-                                                    int32_t* split, int32_t* order) {
+                                                    int32_t* split, int32_t* order, uint8_t* gsplit) {
   grid_launch_dependents();                 // the indexer's set-up may overlap this kernel
   constexpr int kBuckets = 4096;
   __shared__ int s_warp[32];
@@ -95,7 +95,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     for (int u = tid; u < units; u += 1024) {
       const int a0 = prefix[u], a1 = prefix[u + 1];
       for (int r = (a0 + Q - 1) / Q; r < slices && (int64_t)r * Q < a1; ++r) ufirst[r] = u;
-      if (group_is_split(a0, a1, cost, Q)) {
+      const bool sp = group_is_split(a0, a1, cost, Q);
+      gsplit[u] = sp ? 1 : 0;
+      if (sp) {
         const int at = atomicAdd(&s_nsplit, 1);
         if (at < slices) split[at] = u;
       }
@@ -143,6 +145,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     for (int u = tid; u < units; u += 1024) {
       const int tiles = prefix[u + 1] - prefix[u] - cost;
       order[atomicAdd(&s_hist[kBuckets - 1 - tiles / per], 1)] = u;
+      gsplit[u] = 0;
     }
   }
   __syncthreads();
@@ -198,15 +201,14 @@ constexpr size_t kSmemLimit = 232448;   // max dynamic shared memory per CTA (22
 constexpr size_t kSmemHalf = 115712;    // two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
 constexpr int64_t kSplitUnits = 1216;   // logits mode: fewer query groups than this: split key chunks
 
-size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap, int ring = 0) {
+size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap) {
   const size_t elt = fp8 ? 1 : 2;
   size_t s = 1024;                                    // alignment slack
   s += (size_t)nq * 64 * 128 * elt;                  // Q tile
   s += (size_t)stages * 128 * 128 * elt;             // key ring
-  s += (size_t)(2 * stages + 16 + 2 * ring) * 8;     // barriers
+  s += (size_t)(2 * stages + 16) * 8;                // barriers
   s += sizeof(EpiSmem<4>) + 16;
   if (topk) s += (size_t)nq * cap * 8;
-  s += (size_t)ring * nq * 128 * 4;                  // score ring (selector mode)
   return s;
 }
 
@@ -251,28 +253,19 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
     }
   }
   if (pl.ctas_per_sm == 1 && pl.nq >= 2) pl.eg = 2;   // one CTA per SM: two groups take turns
-  if (tk && (pl.cap < topk + 256 || pl.cap < pl.pow2)) pl.ok = false;
-  pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
-  // Selector mode for four-row items: one head-sum group + one selector group, a score
-  // ring of 16 (E4M3) / 8 (bf16) tiles between them, 4 / 3 key stages, and the largest
-  // candidate buffers that still fit (the bigger the buffer, the rarer the cut-backs).
-  pl.sel = false;
-  pl.ring = 0;
-  if (tk && pl.nq == 4) {
-    const int ring = fp8 ? 16 : 8, st = fp8 ? 4 : 3;
-    const size_t fixed = smem_bytes(fp8, 4, st, true, 0, ring);
-    int cap = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / (4 * 8)) / 256 * 256 : 0;
-    if (cap > 128 * kSelMaxPer) cap = 128 * kSelMaxPer;
-    if (cap >= topk + 512 && cap >= pl.pow2) {
-      pl.sel = true;
-      pl.ring = ring;
-      pl.stages = st;
-      pl.cap = cap;
-      pl.eg = 1;
-      pl.ctas_per_sm = 1;
-      pl.smem = smem_bytes(fp8, 4, st, true, cap, ring);
-    }
+  // E4M3 four-row items have shared memory to spare: larger candidate buffers, rarer cuts
+  if (tk && fp8 && pl.nq == 4 && pl.ctas_per_sm == 1) {
+    while (pl.cap + 256 <= 256 * kMaxPer && smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap + 256) <= kSmemLimit)
+      pl.cap += 256;
   }
+  if (tk && (pl.cap < topk + 256 || pl.cap < pl.pow2)) pl.ok = false;
+  // each epilogue warp appends to its own region of a row's buffer, past the top-k slots;
+  // a region must hold a check interval of appends (32 keys per tile)
+  if (tk) {
+    pl.region = (pl.cap - topk) / (4 * pl.eg);
+    if (pl.region < 32 * (pl.eg == 1 ? 2 : 1) + 32) pl.ok = false;
+  }
+  pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
   // as many accumulator buffers (up to 4) as TMEM holds for the CTAs sharing an SM, so
   // the MMAs can run ahead of an epilogue busy cutting its candidates back
   pl.nbuf_log2 = 2;
@@ -315,6 +308,11 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
     off += (size_t)pl.slices * 2 * pl.nq * pl.cap * 8;
     pl.meta_off = off;
     off += (size_t)pl.slices * 2 * pl.nq * 16;
+    pl.gsplit_off = off;
+    off += (size_t)units;
+    off = (off + 15) / 16 * 16;
+    pl.stage_off = off;
+    if (pl.nq == 4) off += (size_t)qs.B * qs.next_n * topk * 8;   // four-row items: staged top-k
     pl.ws_bytes = off;
     pl.items = units;
   }
@@ -348,7 +346,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   prm.chunk = pl.chunk;
   prm.stages = pl.stages;
   prm.nbuf_log2 = pl.nbuf_log2;
-  prm.ring = pl.ring;
+  prm.region = pl.region;
   prm.logits = a.logits;
   prm.ld = a.ld;
   prm.topk = a.topk;
@@ -360,6 +358,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   int64_t grid = device_sm_count() * pl.ctas_per_sm;
   cudaError_t e;
   int32_t* split = nullptr;
+  uint8_t* gsplit = nullptr;
   if (tk) {
     char* ws = static_cast<char*>(a.ws);
     int32_t* plan = reinterpret_cast<int32_t*>(ws);
@@ -374,9 +373,12 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
     prm.work = reinterpret_cast<uint32_t*>(plan + 5);
     prm.partial = reinterpret_cast<uint64_t*>(ws + pl.partial_off);
     prm.partial_meta = reinterpret_cast<uint64_t*>(ws + pl.meta_off);
+    gsplit = reinterpret_cast<uint8_t*>(ws + pl.gsplit_off);
+    prm.stage = pl.nq == 4 ? reinterpret_cast<uint64_t*>(ws + pl.stage_off) : nullptr;
     grid = pl.slices;
     plan_kernel<<<1, 1024, 0, stream>>>(a.qs.context_lens, a.qs.B, a.qs.next_n, a.qs.causal, a.qs.max_context_len,
-                                        pl.nq, pl.ngroups, pl.slices, pl.cost, plan, prefix, ufirst, split, order);
+                                        pl.nq, pl.ngroups, pl.slices, pl.cost, plan, prefix, ufirst, split, order,
+                                        gsplit);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else if (grid > pl.items) {
@@ -390,8 +392,11 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
            : launch_indexer_bf16_logits(mq, mk, prm, pl, (int)grid, stream);
   if (e != cudaSuccess || !tk) return e;
   // groups cut by slice boundaries: rank their lists
-  return launch_merge(prm.partial, prm.partial_meta, pl.cap, prm.plan, prm.prefix, split, pl.slices, pl.nq, a.qs,
-                      a.topk, a.out_idx, a.out_val, stream);
+  e = launch_merge(prm.partial, prm.partial_meta, pl.cap, prm.plan, prm.prefix, split, pl.slices, pl.nq, a.qs,
+                   a.topk, a.out_idx, a.out_val, stream);
+  if (e != cudaSuccess || pl.nq != 4) return e;
+  // four-row items: sort the staged top-k of the unsplit rows
+  return launch_rank_stage(prm.stage, gsplit, pl.nq, pl.ngroups, a.qs, a.topk, a.out_idx, a.out_val, stream);
 }
 
 DSA_DEFINE_TU_ERROR_ACCESSORS(indexer)

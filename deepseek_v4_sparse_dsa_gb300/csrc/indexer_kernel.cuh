@@ -29,20 +29,12 @@
 //              warp refills); it runs ahead of the other roles across item boundaries
 //   warp 1     TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 2..  EG epilogue groups of 4 warps; global tile T uses TMEM buffer T % NB and
-//              epilogue group T % EG (selector mode: one group, then 4 selector warps)
+//              epilogue group T % EG
 // Epilogue: tcgen05.ld of each query's 64 head sums, fp32 ReLU * weight head sum in a
 // fixed order, then a store of the score row (logits mode) or an insert into a per-query
 // candidate buffer in shared memory (top-k mode) that a histogram cut brings back to a
 // superset of the top-k whenever it fills.  Unsplit groups get their rows ranked here,
 // one warp per row.
-//
-// Selector mode (top-k, four query rows per item: prefill-shaped work, where the
-// contraction is the bound): warps 2..5 only form the scores and put each tile's
-// [4][128] scores into a ring of shared-memory slots; warps 6..9 ("selectors") take the
-// tiles from the ring, keep the candidates at or above each row's threshold, cut a full
-// buffer back to exactly the row's top-k (the threshold becomes the k-th key, so later
-// tiles add few candidates), and rank and write the rows when the item ends.  The ring
-// lets a cut-back or the final ranking run while the tensor cores and the head sums go on.
 //
 // Every wait is bounded (see common.cuh); a timeout abandons the work, flags
 // DSA_DEVERR_TIMEOUT, waits for this CTA's own copies and MMAs, frees TMEM and returns.
@@ -80,11 +72,11 @@ struct IndexerParams {
   int32_t ngroups, nchunks, chunk;  // static schedule (logits mode)
   int32_t topk, cap, pow2, stages;
   int32_t nbuf_log2;        // log2 of the TMEM accumulator buffers (1 or 2)
-  int32_t ring;             // selector mode: score-ring slots between head sums and selectors
+  int32_t region;           // top-k mode: candidate slots per epilogue warp and row (see EpiSmem)
+  uint64_t* stage;          // four-row items: [T][topk] exact top-k keys of unsplit rows, unsorted
 };
 
 constexpr int kMaxPer = 10;        // candidate capacity per query <= 256 * kMaxPer
-constexpr int kSelMaxPer = 24;     // selector mode: candidate capacity per query <= 128 * kSelMaxPer
 
 struct ItemInfo {
   int32_t valid, b, g, L, nreal, vis_max;
@@ -105,9 +97,13 @@ struct EpiSmem {
   int abort;
   int stop;
   int last;
-  int sstop;                // selector mode: the selectors' own stop decision
   uint32_t cnt[4];
   uint64_t thr[4];
+  // Top-k mode, row q's candidate buffer (cap keys): slots [0, topk) hold the row's top-k
+  // after its last cut-back (bcnt[q] of them); epilogue warp w appends to its own region
+  // [topk + w * region, topk + (w + 1) * region), wcnt[q][w] keys so far (no atomics).
+  uint32_t bcnt[4];
+  uint32_t wcnt[4][8];
   EngineScratch esc;
   uint32_t bins[kCutBins];
 };
@@ -236,48 +232,8 @@ __device__ bool next_slice_item(const IndexerParams& p, int slice, int r0, int r
   return false;
 }
 
-// One warp: sorts the cn (<= 32 * KPL) keys at buf in registers and writes the first
-// k of them as the row's indices (and values), -1 / -inf past the candidates.
-template <int KPL>
-__device__ __forceinline__ void rank_row(const uint64_t* buf, int cn, int k, bool real, int32_t* out_idx,
-                                         float* out_val) {
-  const int lane = threadIdx.x & 31;
-  uint64_t x[KPL];
-#pragma unroll
-  for (int r = 0; r < KPL; ++r) {
-    const int e = r * 32 + lane;
-    x[r] = e < cn ? buf[e] : 0ull;
-  }
-  warp_sort_regs<KPL>(x);
-  if (!real) return;
-#pragma unroll
-  for (int r = 0; r < KPL; ++r) {
-    const int s = r * 32 + lane;
-    if (s < k) {
-      out_idx[s] = x[r] ? index_of_key(x[r]) : -1;
-      if (out_val) out_val[s] = x[r] ? value_of_key(x[r]) : -INFINITY;
-    }
-  }
-}
-
-// As rank_row for rows of more than 1024 keys: zero-pads buf to P, sorts it in shared
-// memory with one warp.
-__device__ __forceinline__ void rank_row_smem(uint64_t* buf, int cn, int P, int k, bool real, int32_t* out_idx,
-                                              float* out_val) {
-  const int lane = threadIdx.x & 31;
-  for (int e = cn + lane; e < P; e += 32) buf[e] = 0ull;
-  __syncwarp();
-  warp_sort(buf, P);
-  if (!real) return;
-  for (int s = lane; s < k; s += 32) {
-    const uint64_t key = buf[s];
-    out_idx[s] = key ? index_of_key(key) : -1;
-    if (out_val) out_val[s] = key ? value_of_key(key) : -INFINITY;
-  }
-}
-
-template <bool kFP8, int NQ, bool kTopk, int EG, bool kSel>
-__global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && !kSel) ? 2 : 1)
+template <bool kFP8, int NQ, bool kTopk, int EG>
+__global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const IndexerParams p) {
   constexpr int N = NQ * 64;                       // MMA N: (query, head) rows
@@ -300,14 +256,9 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
   uint8_t* k_s = smem + Q_BYTES;                         // S stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(k_s + (size_t)S * K_BYTES);
   // full[S] | empty[S] | tfull[4] | tempty[4] | qfull | qempty | ifull[2] | iempty[2] | mmadone | tmemfree
-  // | selector mode: sfull[RS] | sfree[RS]
-  const int RS = kSel ? p.ring : 0;
-  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 16 + 2 * RS);
+  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 16);
   uint64_t* ebuf = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(es) + sizeof(EpiSmem<NQ>) + 15) & ~uintptr_t(15));
-  // selector mode: the score ring, RS tiles of [NQ][128] scores
-  float* ring = reinterpret_cast<float*>(ebuf + (size_t)NQ * p.cap);
-  const uint32_t sfull0 = smem_u32(bars + 2 * S + 16), sfree0 = sfull0 + 8u * (uint32_t)RS;
 
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
   const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 4);
@@ -335,11 +286,7 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(ifull0 + 8 * a, 1);
-      mbar_init(iempty0 + 8 * a, 1 + 4 * EG + (kSel ? 4 : 0));   // MMA, epilogue (and selector) warps
-    }
-    for (int r = 0; r < RS; ++r) {
-      mbar_init(sfull0 + 8 * r, 4);           // the 4 head-sum warps that wrote the slot
-      mbar_init(sfree0 + 8 * r, 4);           // the 4 selector warps that read it
+      mbar_init(iempty0 + 8 * a, 1 + 4 * EG);
     }
     mbar_init(qfull, 1);
     mbar_init(qempty, 1);
@@ -566,12 +513,10 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
-  } else if (!kSel || warp < 2 + 4 * EG) {
+  } else {
     // ============================ epilogue ============================
     // EG groups of 4 warps take the tiles in turn (global tile T goes to group T % EG);
     // all NT threads share the per-row candidate buffers and cut them back together.
-    // Selector mode: the (single) group only forms the scores and hands each tile's
-    // [NQ][128] scores to the selector warps through the score ring.
     constexpr int NT = 128 * EG;
     constexpr int MAXPER = kMaxPer * 2 / EG;     // candidate slots per thread in a cut-back
     const int et = threadIdx.x - 64;             // 0..NT-1
@@ -581,6 +526,33 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
     const int row = quarter * 32 + lane;         // key row within the tile
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const int cap = p.cap;
+    constexpr int NEW = 4 * EG;                  // epilogue warps (one candidate region each)
+    constexpr bool kStage = kTopk && NQ == 4;    // unsplit rows go to the stage + rank kernel
+    // Cuts row q's candidates (its top-k slots and every warp's region) back to exactly
+    // the row's top-k, packed into [0, topk); raises the row's threshold to the k-th key;
+    // empties the regions.  Every epilogue thread calls it (group barriers inside).
+    auto cut_row = [&](int q) {
+      uint64_t* buf = ebuf + (size_t)q * cap;
+      const uint32_t bc = es->bcnt[q];
+      uint64_t keep[MAXPER];
+#pragma unroll
+      for (int i = 0; i < MAXPER; ++i) {
+        const int e = et + i * NT;
+        bool ok = false;
+        if (e < p.topk) {
+          ok = (uint32_t)e < bc;
+        } else if (e < cap) {
+          const int rel = e - p.topk, w = rel / p.region;
+          ok = w < NEW && (uint32_t)(rel - w * p.region) < es->wcnt[q][w];
+        }
+        keep[i] = ok ? buf[e] : 0ull;
+      }
+      group_sync<NT>();                          // everything is read before the writes
+      const uint64_t thr = engine_cut_exact_keep<NT, MAXPER>(buf, &es->bcnt[q], keep, p.topk, es->bins, &es->esc, et);
+      if (et < NEW) es->wcnt[q][et] = 0;
+      if (et == 0 && thr > es->thr[q]) es->thr[q] = thr;
+      group_sync<NT>();
+    };
     int T0 = 0;                                  // global index of the item's first tile
     for (int n = 0;; ++n) {
       const int slot = n & 1;
@@ -609,10 +581,14 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
         }
         es->w[slot][q][h] = w;
       }
-      if (kTopk && !kSel && et < NQ) {
-        es->cnt[et] = 0;
+      if (kTopk && et < NQ) {
+        es->bcnt[et] = 0;
         es->thr[et] = 0;
       }
+      if (kTopk && et < NQ * 8) es->wcnt[et >> 3][et & 7] = 0;
+      uint32_t cntw[NQ];                         // this warp's region fill per row (warp-uniform)
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) cntw[q] = 0;
       group_sync<NT>();
       const float* wq = &es->w[slot][0][0];
       const int niter = (it.ntiles + EG - 1) / EG;
@@ -633,24 +609,19 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
         // One group checks its buffers every CI tiles (one barrier per check), leaving
         // room for CI tiles of appends; two groups check at every tile.
         constexpr int CI = EG == 1 ? 2 : 1;
-        if (kTopk && !kSel && m % CI == 0) {
+        if (kTopk && m % CI == 0) {
           group_sync<NT>();
 #pragma unroll 1
           for (int q = 0; q < NQ; ++q) {
-            const uint32_t cn = min(es->cnt[q], (uint32_t)cap);   // (a count past cap only after
-            if (cn > (uint32_t)(cap - 128 * EG * CI)) {              //  a flagged overflow)
-              // cut back to a superset of the top-k; exactly only if the histogram
-              // cannot free enough room
-              uint64_t* buf = ebuf + (size_t)q * cap;
-              const uint32_t room = (uint32_t)min((cap + p.topk) / 2, cap - 256 * EG * CI);
-              uint64_t thr = engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, room, es->bins,
-                                                           &es->esc, et);
-              if (thr == 0ull) {
-                thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
-                engine_compact<NT, MAXPER>(buf, &es->cnt[q], (int)cn, thr, &es->esc, et);
-              }
-              if (et == 0 && thr > es->thr[q]) es->thr[q] = thr;
-              group_sync<NT>();
+            uint32_t fill = 0;
+            for (int w = 0; w < NEW; ++w) fill = max(fill, es->wcnt[q][w]);
+            if (fill > (uint32_t)(p.region - 32 * CI)) {
+              // some warp's region could overflow before the next check: cut the row back
+              // to exactly its top-k (the threshold becomes its k-th key)
+              cut_row(q);
+#pragma unroll
+              for (int qq = 0; qq < NQ; ++qq)
+                if (qq == q) cntw[qq] = 0;
             }
           }
         }
@@ -697,24 +668,7 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty0 + 8 * a);
 
-        if constexpr (kSel) {
-          // hand the tile's scores to the selectors: -inf for keys the rows do not see
-          const int rs = T % RS;
-          bool okr = (lane == 0) ? mbar_wait(sfree0 + 8 * rs, ((uint32_t)(T / RS) & 1u) ^ 1u, limit, abort_flag) : true;
-          okr = __shfl_sync(0xFFFFFFFFu, okr ? 1 : 0, 0) != 0;
-          if (!okr) {
-            if (lane == 0) {
-              raise_error(DSA_DEVERR_TIMEOUT);
-              *abort_flag = 1;
-            }
-            continue;
-          }
-          __syncwarp();                          // lane 0's acquire covers the whole warp
-#pragma unroll
-          for (int q = 0; q < NQ; ++q) ring[(size_t)(rs * NQ + q) * 128 + row] = (valid && j < it.vis[q]) ? v[q] : -INFINITY;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(sfull0 + 8 * rs);
-        } else if (!kTopk) {
+        if (!kTopk) {
           if (j < p.max_len) {
 #pragma unroll
             for (int q = 0; q < NQ; ++q)
@@ -722,14 +676,23 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
                 p.logits[(int64_t)(it.t0 + q) * p.ld + j] = (valid && j < it.vis[q]) ? v[q] : -INFINITY;
           }
         } else {
-          uint64_t key[NQ];
-          bool take[NQ];
+          // append to this warp's own region of each row: a ballot gives every key its
+          // slot, the fill count stays in registers (no shared atomics)
+          const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
           for (int q = 0; q < NQ; ++q) {
-            key[q] = rank_key(v[q], (uint32_t)j);
-            take[q] = valid && j < it.vis[q] && is_candidate(v[q]) && key[q] >= es->thr[q];
+            const uint64_t key = rank_key(v[q], (uint32_t)j);
+            const bool take = valid && j < it.vis[q] && is_candidate(v[q]) && key >= es->thr[q];
+            const uint32_t mb = __ballot_sync(0xFFFFFFFFu, take);
+            if (mb == 0u) continue;
+            if (take) {
+              const uint32_t at = cntw[q] + __popc(mb & below);
+              if (at < (uint32_t)p.region) ebuf[(size_t)q * cap + p.topk + ew * p.region + at] = key;
+              else raise_error(DSA_DEVERR_OVERFLOW | (10u << 8));
+            }
+            cntw[q] = min(cntw[q] + (uint32_t)__popc(mb), (uint32_t)p.region);
+            if (lane == 0) es->wcnt[q][ew] = cntw[q];
           }
-          engine_append_multi<NQ>(ebuf, (size_t)cap, es->cnt, key, take, (uint32_t)cap, 10u);
         }
       }
       T0 += it.ntiles;
@@ -740,54 +703,47 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
         const int f1 = min(it.ks + it.chunk, p.max_len);
         for (int q = 0; q < it.nreal; ++q)
           for (int jj = f0 + et; jj < f1; jj += NT) p.logits[(int64_t)(it.t0 + q) * p.ld + jj] = -INFINITY;
-      } else if (kSel) {
-        // the selectors finish the item
-      } else if (!it.split) {
-        // the whole group in one item: cut each row's candidates back to at most SN
-        // (histogram first, the exact radix select only if that is not enough), then one
-        // warp per row sorts them in registers and writes the first k
-        const int P = p.pow2;
-        const int SN = P <= 128 ? 256 : (P <= 512 ? 2 * P : P);   // keys sorted per row
+      } else {
+        // every row cut back to exactly its top-k (compacting the warp regions)
         group_sync<NT>();
 #pragma unroll 1
-        for (int q = 0; q < NQ; ++q) {
-          uint32_t cn = min(es->cnt[q], (uint32_t)cap);
-          uint64_t* buf = ebuf + (size_t)q * cap;
-          if (cn > (uint32_t)SN) {
-            engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, (uint32_t)SN, es->bins, &es->esc, et);
-            cn = es->cnt[q];
+        for (int q = 0; q < NQ; ++q) cut_row(q);
+        if (!it.split && kStage) {
+          // four-row items: the rows' top-k keys, unsorted, to the stage; the rank kernel
+          // sorts and writes them (the tensor cores go on with the next item meanwhile)
+          for (int q = 0; q < it.nreal; ++q) {
+            const int64_t t = it.t0 + q;
+            const int cn = (int)es->bcnt[q];
+            const uint64_t* buf = ebuf + (size_t)q * cap;
+            for (int s2 = et; s2 < p.topk; s2 += NT) p.stage[t * p.topk + s2] = s2 < cn ? buf[s2] : 0ull;
           }
-          if (cn > (uint32_t)SN) {
-            const uint64_t thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
-            engine_compact<NT, MAXPER>(buf, &es->cnt[q], (int)cn, thr, &es->esc, et);
+        } else if (!it.split) {
+          // one warp per row sorts its top-k in registers and writes them
+          const int P = p.pow2;
+          for (int q = ew; q < NQ; q += 4 * EG) {
+            const uint64_t* buf = ebuf + (size_t)q * cap;
+            const int cn = (int)es->bcnt[q];
+            const int64_t t = it.t0 + q;
+            const bool real = q < it.nreal;
+            int32_t* oi = p.out_idx + t * p.topk;
+            float* ov = p.out_val ? p.out_val + t * p.topk : nullptr;
+            if (P <= 256) rank_row<8>(buf, cn, p.topk, real, oi, ov);
+            else if (P <= 512) rank_row<16>(buf, cn, p.topk, real, oi, ov);
+            else if (P <= 1024) rank_row<32>(buf, cn, p.topk, real, oi, ov);
+            else rank_row_smem(ebuf + (size_t)q * cap, cn, P, p.topk, real, oi, ov);
           }
-        }
-        group_sync<NT>();
-        for (int q = ew; q < NQ; q += 4 * EG) {
-          uint64_t* buf = ebuf + (size_t)q * cap;
-          const int cn = min((int)es->cnt[q], cap);
-          const int64_t t = it.t0 + q;
-          const bool real = q < it.nreal;
-          int32_t* oi = p.out_idx + t * p.topk;
-          float* ov = p.out_val ? p.out_val + t * p.topk : nullptr;
-          if (SN == 256) rank_row<8>(buf, cn, p.topk, real, oi, ov);
-          else if (SN == 512) rank_row<16>(buf, cn, p.topk, real, oi, ov);
-          else if (SN == 1024) rank_row<32>(buf, cn, p.topk, real, oi, ov);
-          else rank_row_smem(buf, cn, P, p.topk, real, oi, ov);
-        }
-      } else {
-        // a piece of a split group: its candidates as they stand (unsorted, at least
-        // its top-k) with their count and the piece's threshold, in the slice's list
-        // slot; the merge kernel ranks the group's lists
-        group_sync<NT>();
-        for (int q = 0; q < it.nreal; ++q) {
-          const int cn = min((int)es->cnt[q], cap);
-          const size_t l = (size_t)it.slot * NQ + q;
-          const uint64_t* buf = ebuf + (size_t)q * cap;
-          for (int s = et; s < cn; s += NT) p.partial[l * cap + s] = buf[s];
-          if (et == 0) {
-            p.partial_meta[2 * l] = (uint64_t)cn;
-            p.partial_meta[2 * l + 1] = es->thr[q];
+        } else {
+          // a piece of a split group: its top-k, unsorted, with the piece's threshold, in
+          // the slice's list slot; the merge kernel ranks the group's lists
+          for (int q = 0; q < it.nreal; ++q) {
+            const int cn = (int)es->bcnt[q];
+            const size_t l = (size_t)it.slot * NQ + q;
+            const uint64_t* buf = ebuf + (size_t)q * cap;
+            for (int s2 = et; s2 < cn; s2 += NT) p.partial[l * cap + s2] = buf[s2];
+            if (et == 0) {
+              p.partial_meta[2 * l] = (uint64_t)cn;
+              p.partial_meta[2 * l + 1] = es->thr[q];
+            }
           }
         }
       }
@@ -799,121 +755,6 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(tmemfree);
-  } else if constexpr (kSel) {
-    // ============================ selectors ============================
-    // Four warps rank the scores the head-sum warps leave in the score ring, so cut-backs
-    // and the final ranking of a group's rows overlap the tensor-core work instead of
-    // holding it up.  Thread st owns key row st of every tile.  A row's candidate buffer
-    // is cut back to exactly its top-k (and the row's threshold raised to the k-th key)
-    // whenever the next tile could overflow it.
-    constexpr int NTS = 128;
-    constexpr int SBAR = 2;                      // the selectors' named barrier
-    const int st = threadIdx.x - (64 + 128 * EG);
-    const int sw = st >> 5;                      // selector warp 0..3
-    const int cap = p.cap;
-    int T0 = 0;
-    for (int n = 0;; ++n) {
-      const int slot = n & 1;
-      bool ok = (lane == 0) ? mbar_wait(ifull0 + 8 * slot, (uint32_t)(n >> 1) & 1u, limit, abort_flag) : true;
-      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-      if (!ok && lane == 0) {
-        raise_error(DSA_DEVERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-      group_sync<NTS>(SBAR);
-      if (st == 0) es->sstop = (*abort_flag != 0) || !es->info[slot].valid;
-      group_sync<NTS>(SBAR);
-      if (es->sstop) break;
-      const ItemInfo it = es->info[slot];
-      if (st < NQ) {
-        es->cnt[st] = 0;
-        es->thr[st] = 0;
-      }
-      for (int i = 0; i < it.ntiles; ++i) {
-        const int T = T0 + i;
-        const int rs = T % RS;
-        // room for this tile's appends (the counts are read after a barrier, so every
-        // selector takes the same branches)
-        group_sync<NTS>(SBAR);
-#pragma unroll 1
-        for (int q = 0; q < NQ; ++q) {
-          const uint32_t cn = min(es->cnt[q], (uint32_t)cap);
-          if (cn > (uint32_t)(cap - 128)) {
-            uint64_t* buf = ebuf + (size_t)q * cap;
-            const uint64_t thr =
-                engine_cut_exact<NTS, kSelMaxPer>(buf, &es->cnt[q], (int)cn, p.topk, es->bins, &es->esc, st, SBAR);
-            if (st == 0 && thr > es->thr[q]) es->thr[q] = thr;
-            group_sync<NTS>(SBAR);
-          }
-        }
-        bool okt = (lane == 0) ? mbar_wait(sfull0 + 8 * rs, (uint32_t)(T / RS) & 1u, limit, abort_flag) : true;
-        okt = __shfl_sync(0xFFFFFFFFu, okt ? 1 : 0, 0) != 0;
-        if (!okt) {
-          if (lane == 0) {
-            raise_error(DSA_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-          }
-          continue;
-        }
-        __syncwarp();                            // lane 0's acquire covers the whole warp
-        float v[NQ];
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) v[q] = ring[(size_t)(rs * NQ + q) * 128 + st];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sfree0 + 8 * rs);
-        const int j = it.ks + i * 128 + st;
-        uint64_t key[NQ];
-        bool take[NQ];
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-          key[q] = rank_key(v[q], (uint32_t)j);
-          take[q] = is_candidate(v[q]) && key[q] >= es->thr[q];
-        }
-        engine_append_multi<NQ>(ebuf, (size_t)cap, es->cnt, key, take, (uint32_t)cap, 11u);
-      }
-      T0 += it.ntiles;
-      group_sync<NTS>(SBAR);
-      if (!it.split) {
-        // each row cut to exactly its top-k, then sorted by one warp and written
-        const int P = p.pow2;
-#pragma unroll 1
-        for (int q = 0; q < NQ; ++q) {
-          const uint32_t cn = min(es->cnt[q], (uint32_t)cap);
-          if (cn > (uint32_t)p.topk) {
-            engine_cut_exact<NTS, kSelMaxPer>(ebuf + (size_t)q * cap, &es->cnt[q], (int)cn, p.topk, es->bins,
-                                              &es->esc, st, SBAR);
-            group_sync<NTS>(SBAR);
-          }
-        }
-        for (int q = sw; q < NQ; q += 4) {
-          uint64_t* buf = ebuf + (size_t)q * cap;
-          const int cn = min((int)es->cnt[q], p.topk);
-          const int64_t t = it.t0 + q;
-          const bool real = q < it.nreal;
-          int32_t* oi = p.out_idx + t * p.topk;
-          float* ov = p.out_val ? p.out_val + t * p.topk : nullptr;
-          if (P <= 256) rank_row<8>(buf, cn, p.topk, real, oi, ov);
-          else if (P <= 512) rank_row<16>(buf, cn, p.topk, real, oi, ov);
-          else if (P <= 1024) rank_row<32>(buf, cn, p.topk, real, oi, ov);
-          else rank_row_smem(buf, cn, P, p.topk, real, oi, ov);
-        }
-      } else {
-        // a piece of a split group: its candidates as they stand with the piece's
-        // threshold, in the slice's list slot (ranked by the merge kernel)
-        for (int q = 0; q < it.nreal; ++q) {
-          const int cn = min((int)es->cnt[q], cap);
-          const size_t l = (size_t)it.slot * NQ + q;
-          const uint64_t* buf = ebuf + (size_t)q * cap;
-          for (int s2 = st; s2 < cn; s2 += NTS) p.partial[l * cap + s2] = buf[s2];
-          if (st == 0) {
-            p.partial_meta[2 * l] = (uint64_t)cn;
-            p.partial_meta[2 * l + 1] = es->thr[q];
-          }
-        }
-      }
-      group_sync<NTS>(SBAR);
-      if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
-    }
   }
   // No CTA-wide barrier here: the warps leave as their roles end (warp 1 last frees
   // TMEM); shared memory stays valid until every thread of the CTA has exited.
@@ -923,15 +764,15 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kSel ? 128 : 0), (EG == 1 && 
 // Launch of one instantiation
 // =====================================================================================
 
-template <bool kFP8, int NQ, bool kTopk, int EG, bool kSel = false>
+template <bool kFP8, int NQ, bool kTopk, int EG>
 static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& prm,
                               const IndexerPlan& pl, int grid, cudaStream_t st) {
-  auto kern = indexer_kernel<kFP8, NQ, kTopk, EG, kSel>;
+  auto kern = indexer_kernel<kFP8, NQ, kTopk, EG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(64 + 128 * EG + (kSel ? 128 : 0));
+  cfg.blockDim = dim3(64 + 128 * EG);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -948,9 +789,6 @@ static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, cons
 template <bool kFP8, bool kTopk>
 static cudaError_t dispatch_nq(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& prm,
                                const IndexerPlan& pl, int grid, cudaStream_t st) {
-  if constexpr (kTopk) {
-    if (pl.sel) return launch_one<kFP8, 4, true, 1, true>(mq, mk, prm, pl, grid, st);
-  }
   switch (pl.nq * 2 + pl.eg) {
     case 3: return launch_one<kFP8, 1, kTopk, 1>(mq, mk, prm, pl, grid, st);
     case 5: return launch_one<kFP8, 2, kTopk, 1>(mq, mk, prm, pl, grid, st);
