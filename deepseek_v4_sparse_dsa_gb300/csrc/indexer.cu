@@ -36,7 +36,7 @@ __device__ __forceinline__ int group_tiles(const int32_t* context_lens, int u, i
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ context_lens, int B, int next_n,
                                                     int causal, int max_len, int nq, int ngroups, int slices,
                                                     int cost, int32_t* plan, int32_t* prefix, int32_t* ufirst,
-                                                    int32_t* split, int32_t* order, uint8_t* gsplit) {
+                                                    int32_t* split, int32_t* order) {
   grid_launch_dependents();                 // the indexer's set-up may overlap this kernel
   constexpr int kBuckets = 4096;
   __shared__ int s_warp[32];
@@ -95,9 +95,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     for (int u = tid; u < units; u += 1024) {
       const int a0 = prefix[u], a1 = prefix[u + 1];
       for (int r = (a0 + Q - 1) / Q; r < slices && (int64_t)r * Q < a1; ++r) ufirst[r] = u;
-      const bool sp = group_is_split(a0, a1, cost, Q);
-      gsplit[u] = sp ? 1 : 0;
-      if (sp) {
+      if (group_is_split(a0, a1, cost, Q)) {
         const int at = atomicAdd(&s_nsplit, 1);
         if (at < slices) split[at] = u;
       }
@@ -145,7 +143,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     for (int u = tid; u < units; u += 1024) {
       const int tiles = prefix[u + 1] - prefix[u] - cost;
       order[atomicAdd(&s_hist[kBuckets - 1 - tiles / per], 1)] = u;
-      gsplit[u] = 0;
     }
   }
   __syncthreads();
@@ -253,18 +250,7 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
     }
   }
   if (pl.ctas_per_sm == 1 && pl.nq >= 2) pl.eg = 2;   // one CTA per SM: two groups take turns
-  // E4M3 four-row items have shared memory to spare: larger candidate buffers, rarer cuts
-  if (tk && fp8 && pl.nq == 4 && pl.ctas_per_sm == 1) {
-    while (pl.cap + 256 <= 256 * kMaxPer && smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap + 256) <= kSmemLimit)
-      pl.cap += 256;
-  }
   if (tk && (pl.cap < topk + 256 || pl.cap < pl.pow2)) pl.ok = false;
-  // each epilogue warp appends to its own region of a row's buffer, past the top-k slots;
-  // a region must hold a check interval of appends (32 keys per tile)
-  if (tk) {
-    pl.region = (pl.cap - topk) / (4 * pl.eg);
-    if (pl.region < 32 * (pl.eg == 1 ? 2 : 1) + 32) pl.ok = false;
-  }
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
   // as many accumulator buffers (up to 4) as TMEM holds for the CTAs sharing an SM, so
   // the MMAs can run ahead of an epilogue busy cutting its candidates back
@@ -308,11 +294,6 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
     off += (size_t)pl.slices * 2 * pl.nq * pl.cap * 8;
     pl.meta_off = off;
     off += (size_t)pl.slices * 2 * pl.nq * 16;
-    pl.gsplit_off = off;
-    off += (size_t)units;
-    off = (off + 15) / 16 * 16;
-    pl.stage_off = off;
-    if (pl.nq == 4) off += (size_t)qs.B * qs.next_n * topk * 8;   // four-row items: staged top-k
     pl.ws_bytes = off;
     pl.items = units;
   }
@@ -346,7 +327,6 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   prm.chunk = pl.chunk;
   prm.stages = pl.stages;
   prm.nbuf_log2 = pl.nbuf_log2;
-  prm.region = pl.region;
   prm.logits = a.logits;
   prm.ld = a.ld;
   prm.topk = a.topk;
@@ -358,7 +338,6 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   int64_t grid = device_sm_count() * pl.ctas_per_sm;
   cudaError_t e;
   int32_t* split = nullptr;
-  uint8_t* gsplit = nullptr;
   if (tk) {
     char* ws = static_cast<char*>(a.ws);
     int32_t* plan = reinterpret_cast<int32_t*>(ws);
@@ -373,12 +352,9 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
     prm.work = reinterpret_cast<uint32_t*>(plan + 5);
     prm.partial = reinterpret_cast<uint64_t*>(ws + pl.partial_off);
     prm.partial_meta = reinterpret_cast<uint64_t*>(ws + pl.meta_off);
-    gsplit = reinterpret_cast<uint8_t*>(ws + pl.gsplit_off);
-    prm.stage = pl.nq == 4 ? reinterpret_cast<uint64_t*>(ws + pl.stage_off) : nullptr;
     grid = pl.slices;
     plan_kernel<<<1, 1024, 0, stream>>>(a.qs.context_lens, a.qs.B, a.qs.next_n, a.qs.causal, a.qs.max_context_len,
-                                        pl.nq, pl.ngroups, pl.slices, pl.cost, plan, prefix, ufirst, split, order,
-                                        gsplit);
+                                        pl.nq, pl.ngroups, pl.slices, pl.cost, plan, prefix, ufirst, split, order);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   } else if (grid > pl.items) {
@@ -392,11 +368,8 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
            : launch_indexer_bf16_logits(mq, mk, prm, pl, (int)grid, stream);
   if (e != cudaSuccess || !tk) return e;
   // groups cut by slice boundaries: rank their lists
-  e = launch_merge(prm.partial, prm.partial_meta, pl.cap, prm.plan, prm.prefix, split, pl.slices, pl.nq, a.qs,
-                   a.topk, a.out_idx, a.out_val, stream);
-  if (e != cudaSuccess || pl.nq != 4) return e;
-  // four-row items: sort the staged top-k of the unsplit rows
-  return launch_rank_stage(prm.stage, gsplit, pl.nq, pl.ngroups, a.qs, a.topk, a.out_idx, a.out_val, stream);
+  return launch_merge(prm.partial, prm.partial_meta, pl.cap, prm.plan, prm.prefix, split, pl.slices, pl.nq, a.qs,
+                      a.topk, a.out_idx, a.out_val, stream);
 }
 
 DSA_DEFINE_TU_ERROR_ACCESSORS(indexer)

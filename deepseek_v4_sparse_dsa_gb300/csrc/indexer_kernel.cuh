@@ -72,8 +72,6 @@ struct IndexerParams {
   int32_t ngroups, nchunks, chunk;  // static schedule (logits mode)
   int32_t topk, cap, pow2, stages;
   int32_t nbuf_log2;        // log2 of the TMEM accumulator buffers (1 or 2)
-  int32_t region;           // top-k mode: candidate slots per epilogue warp and row (see EpiSmem)
-  uint64_t* stage;          // four-row items: [T][topk] exact top-k keys of unsplit rows, unsorted
 };
 
 constexpr int kMaxPer = 10;        // candidate capacity per query <= 256 * kMaxPer
@@ -99,11 +97,6 @@ struct EpiSmem {
   int last;
   uint32_t cnt[4];
   uint64_t thr[4];
-  // Top-k mode, row q's candidate buffer (cap keys): slots [0, topk) hold the row's top-k
-  // after its last cut-back (bcnt[q] of them); epilogue warp w appends to its own region
-  // [topk + w * region, topk + (w + 1) * region), wcnt[q][w] keys so far (no atomics).
-  uint32_t bcnt[4];
-  uint32_t wcnt[4][8];
   EngineScratch esc;
   uint32_t bins[kCutBins];
 };
@@ -526,33 +519,6 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     const int row = quarter * 32 + lane;         // key row within the tile
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const int cap = p.cap;
-    constexpr int NEW = 4 * EG;                  // epilogue warps (one candidate region each)
-    constexpr bool kStage = kTopk && NQ == 4;    // unsplit rows go to the stage + rank kernel
-    // Cuts row q's candidates (its top-k slots and every warp's region) back to exactly
-    // the row's top-k, packed into [0, topk); raises the row's threshold to the k-th key;
-    // empties the regions.  Every epilogue thread calls it (group barriers inside).
-    auto cut_row = [&](int q) {
-      uint64_t* buf = ebuf + (size_t)q * cap;
-      const uint32_t bc = es->bcnt[q];
-      uint64_t keep[MAXPER];
-#pragma unroll
-      for (int i = 0; i < MAXPER; ++i) {
-        const int e = et + i * NT;
-        bool ok = false;
-        if (e < p.topk) {
-          ok = (uint32_t)e < bc;
-        } else if (e < cap) {
-          const int rel = e - p.topk, w = rel / p.region;
-          ok = w < NEW && (uint32_t)(rel - w * p.region) < es->wcnt[q][w];
-        }
-        keep[i] = ok ? buf[e] : 0ull;
-      }
-      group_sync<NT>();                          // everything is read before the writes
-      const uint64_t thr = engine_cut_exact_keep<NT, MAXPER>(buf, &es->bcnt[q], keep, p.topk, es->bins, &es->esc, et);
-      if (et < NEW) es->wcnt[q][et] = 0;
-      if (et == 0 && thr > es->thr[q]) es->thr[q] = thr;
-      group_sync<NT>();
-    };
     int T0 = 0;                                  // global index of the item's first tile
     for (int n = 0;; ++n) {
       const int slot = n & 1;
@@ -582,13 +548,9 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         es->w[slot][q][h] = w;
       }
       if (kTopk && et < NQ) {
-        es->bcnt[et] = 0;
+        es->cnt[et] = 0;
         es->thr[et] = 0;
       }
-      if (kTopk && et < NQ * 8) es->wcnt[et >> 3][et & 7] = 0;
-      uint32_t cntw[NQ];                         // this warp's region fill per row (warp-uniform)
-#pragma unroll
-      for (int q = 0; q < NQ; ++q) cntw[q] = 0;
       group_sync<NT>();
       const float* wq = &es->w[slot][0][0];
       const int niter = (it.ntiles + EG - 1) / EG;
@@ -613,15 +575,20 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
           group_sync<NT>();
 #pragma unroll 1
           for (int q = 0; q < NQ; ++q) {
-            uint32_t fill = 0;
-            for (int w = 0; w < NEW; ++w) fill = max(fill, es->wcnt[q][w]);
-            if (fill > (uint32_t)(p.region - 32 * CI)) {
-              // some warp's region could overflow before the next check: cut the row back
-              // to exactly its top-k (the threshold becomes its k-th key)
-              cut_row(q);
-#pragma unroll
-              for (int qq = 0; qq < NQ; ++qq)
-                if (qq == q) cntw[qq] = 0;
+            const uint32_t cn = min(es->cnt[q], (uint32_t)cap);   // (a count past cap only after
+            if (cn > (uint32_t)(cap - 128 * EG * CI)) {              //  a flagged overflow)
+              // cut back to a superset of the top-k; exactly only if the histogram
+              // cannot free enough room
+              uint64_t* buf = ebuf + (size_t)q * cap;
+              const uint32_t room = (uint32_t)min((cap + p.topk) / 2, cap - 256 * EG * CI);
+              uint64_t thr = engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, room, es->bins,
+                                                           &es->esc, et);
+              if (thr == 0ull) {
+                thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
+                engine_compact<NT, MAXPER>(buf, &es->cnt[q], (int)cn, thr, &es->esc, et);
+              }
+              if (et == 0 && thr > es->thr[q]) es->thr[q] = thr;
+              group_sync<NT>();
             }
           }
         }
@@ -676,23 +643,14 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
                 p.logits[(int64_t)(it.t0 + q) * p.ld + j] = (valid && j < it.vis[q]) ? v[q] : -INFINITY;
           }
         } else {
-          // append to this warp's own region of each row: a ballot gives every key its
-          // slot, the fill count stays in registers (no shared atomics)
-          const uint32_t below = (1u << lane) - 1u;
+          uint64_t key[NQ];
+          bool take[NQ];
 #pragma unroll
           for (int q = 0; q < NQ; ++q) {
-            const uint64_t key = rank_key(v[q], (uint32_t)j);
-            const bool take = valid && j < it.vis[q] && is_candidate(v[q]) && key >= es->thr[q];
-            const uint32_t mb = __ballot_sync(0xFFFFFFFFu, take);
-            if (mb == 0u) continue;
-            if (take) {
-              const uint32_t at = cntw[q] + __popc(mb & below);
-              if (at < (uint32_t)p.region) ebuf[(size_t)q * cap + p.topk + ew * p.region + at] = key;
-              else raise_error(DSA_DEVERR_OVERFLOW | (10u << 8));
-            }
-            cntw[q] = min(cntw[q] + (uint32_t)__popc(mb), (uint32_t)p.region);
-            if (lane == 0) es->wcnt[q][ew] = cntw[q];
+            key[q] = rank_key(v[q], (uint32_t)j);
+            take[q] = valid && j < it.vis[q] && is_candidate(v[q]) && key[q] >= es->thr[q];
           }
+          engine_append_multi<NQ>(ebuf, (size_t)cap, es->cnt, key, take, (uint32_t)cap, 10u);
         }
       }
       T0 += it.ntiles;
@@ -703,47 +661,52 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         const int f1 = min(it.ks + it.chunk, p.max_len);
         for (int q = 0; q < it.nreal; ++q)
           for (int jj = f0 + et; jj < f1; jj += NT) p.logits[(int64_t)(it.t0 + q) * p.ld + jj] = -INFINITY;
-      } else {
-        // every row cut back to exactly its top-k (compacting the warp regions)
+      } else if (!it.split) {
+        // the whole group in one item: cut each row's candidates back to at most SN
+        // (histogram first, the exact radix select only if that is not enough), then one
+        // warp per row sorts them in registers and writes the first k
+        const int P = p.pow2;
+        const int SN = P <= 128 ? 256 : (P <= 512 ? 2 * P : P);   // keys sorted per row
         group_sync<NT>();
 #pragma unroll 1
-        for (int q = 0; q < NQ; ++q) cut_row(q);
-        if (!it.split && kStage) {
-          // four-row items: the rows' top-k keys, unsorted, to the stage; the rank kernel
-          // sorts and writes them (the tensor cores go on with the next item meanwhile)
-          for (int q = 0; q < it.nreal; ++q) {
-            const int64_t t = it.t0 + q;
-            const int cn = (int)es->bcnt[q];
-            const uint64_t* buf = ebuf + (size_t)q * cap;
-            for (int s2 = et; s2 < p.topk; s2 += NT) p.stage[t * p.topk + s2] = s2 < cn ? buf[s2] : 0ull;
+        for (int q = 0; q < NQ; ++q) {
+          uint32_t cn = min(es->cnt[q], (uint32_t)cap);
+          uint64_t* buf = ebuf + (size_t)q * cap;
+          if (cn > (uint32_t)SN) {
+            engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, (uint32_t)SN, es->bins, &es->esc, et);
+            cn = es->cnt[q];
           }
-        } else if (!it.split) {
-          // one warp per row sorts its top-k in registers and writes them
-          const int P = p.pow2;
-          for (int q = ew; q < NQ; q += 4 * EG) {
-            const uint64_t* buf = ebuf + (size_t)q * cap;
-            const int cn = (int)es->bcnt[q];
-            const int64_t t = it.t0 + q;
-            const bool real = q < it.nreal;
-            int32_t* oi = p.out_idx + t * p.topk;
-            float* ov = p.out_val ? p.out_val + t * p.topk : nullptr;
-            if (P <= 256) rank_row<8>(buf, cn, p.topk, real, oi, ov);
-            else if (P <= 512) rank_row<16>(buf, cn, p.topk, real, oi, ov);
-            else if (P <= 1024) rank_row<32>(buf, cn, p.topk, real, oi, ov);
-            else rank_row_smem(ebuf + (size_t)q * cap, cn, P, p.topk, real, oi, ov);
+          if (cn > (uint32_t)SN) {
+            const uint64_t thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
+            engine_compact<NT, MAXPER>(buf, &es->cnt[q], (int)cn, thr, &es->esc, et);
           }
-        } else {
-          // a piece of a split group: its top-k, unsorted, with the piece's threshold, in
-          // the slice's list slot; the merge kernel ranks the group's lists
-          for (int q = 0; q < it.nreal; ++q) {
-            const int cn = (int)es->bcnt[q];
-            const size_t l = (size_t)it.slot * NQ + q;
-            const uint64_t* buf = ebuf + (size_t)q * cap;
-            for (int s2 = et; s2 < cn; s2 += NT) p.partial[l * cap + s2] = buf[s2];
-            if (et == 0) {
-              p.partial_meta[2 * l] = (uint64_t)cn;
-              p.partial_meta[2 * l + 1] = es->thr[q];
-            }
+        }
+        group_sync<NT>();
+        for (int q = ew; q < NQ; q += 4 * EG) {
+          uint64_t* buf = ebuf + (size_t)q * cap;
+          const int cn = min((int)es->cnt[q], cap);
+          const int64_t t = it.t0 + q;
+          const bool real = q < it.nreal;
+          int32_t* oi = p.out_idx + t * p.topk;
+          float* ov = p.out_val ? p.out_val + t * p.topk : nullptr;
+          if (SN == 256) rank_row<8>(buf, cn, p.topk, real, oi, ov);
+          else if (SN == 512) rank_row<16>(buf, cn, p.topk, real, oi, ov);
+          else if (SN == 1024) rank_row<32>(buf, cn, p.topk, real, oi, ov);
+          else rank_row_smem(buf, cn, P, p.topk, real, oi, ov);
+        }
+      } else {
+        // a piece of a split group: its candidates as they stand (unsorted, at least
+        // its top-k) with their count and the piece's threshold, in the slice's list
+        // slot; the merge kernel ranks the group's lists
+        group_sync<NT>();
+        for (int q = 0; q < it.nreal; ++q) {
+          const int cn = min((int)es->cnt[q], cap);
+          const size_t l = (size_t)it.slot * NQ + q;
+          const uint64_t* buf = ebuf + (size_t)q * cap;
+          for (int s = et; s < cn; s += NT) p.partial[l * cap + s] = buf[s];
+          if (et == 0) {
+            p.partial_meta[2 * l] = (uint64_t)cn;
+            p.partial_meta[2 * l + 1] = es->thr[q];
           }
         }
       }

@@ -30,9 +30,7 @@ struct IndexerPlan {
   size_t smem;       // dynamic shared memory per CTA
   int64_t items;     // logits mode: work items; top-k mode: query groups
   size_t ws_bytes;   // workspace bytes (top-k mode)
-  int region;        // top-k mode: candidate slots per epilogue warp and query row
-  size_t prefix_off, ufirst_off, split_off, order_off, partial_off, meta_off,   // byte offsets in ws
-      gsplit_off, stage_off;
+  size_t prefix_off, ufirst_off, split_off, order_off, partial_off, meta_off;   // byte offsets in ws
   bool ok;           // false: shape does not fit this build
 };
 
@@ -78,13 +76,6 @@ cudaError_t launch_topk(const float* logits, int64_t ld, const dsa_queries& qs, 
 cudaError_t launch_merge(const uint64_t* partial, const uint64_t* meta, int lcap, const int32_t* plan,
                          const int32_t* prefix, const int32_t* split, int slices, int nq, const dsa_queries& qs,
                          int topk, int32_t* out_idx, float* out_val, cudaStream_t stream);
-
-// Sorts the staged top-k keys of the rows of unsplit four-row groups (stage = [T][topk],
-// zero-padded; gsplit = per query group 1 if split, those rows are the merge kernel's)
-// and writes their indices / values.  Launched as a programmatic dependent.
-cudaError_t launch_rank_stage(const uint64_t* stage, const uint8_t* gsplit, int nq, int ngroups,
-                              const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val,
-                              cudaStream_t stream);
 
 // ------------------------------------------------------------------ gather (gather.cu)
 cudaError_t launch_mxfp4_gather(const uint8_t* fp4, const uint8_t* scale, int64_t num_blocks, int bs,

@@ -261,79 +261,6 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
   }
 }
 
-// One warp per query row: the row's staged top-k (unsorted, zero-padded to k) sorted in
-// registers (P = 32 * KPL >= k) and written in rank order; rows of split groups are left
-// to the merge kernel.
-template <int KPL>
-__global__ void __launch_bounds__(256) rank_stage_kernel(const uint64_t* __restrict__ stage,
-                                                         const uint8_t* __restrict__ gsplit, int64_t T, int topk,
-                                                         int nq, int next_n, int ngroups, int32_t* out_idx,
-                                                         float* out_val) {
-  grid_dependency_wait();                       // the fused kernel's stage is complete
-  grid_launch_dependents();
-  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (t >= T) return;
-  const int64_t b = t / next_n;
-  const int i = (int)(t - b * next_n);
-  if (__ldg(gsplit + b * ngroups + i / nq)) return;
-  rank_row<KPL>(stage + t * topk, topk, topk, true, out_idx + t * topk, out_val ? out_val + t * topk : nullptr);
-}
-
-// As rank_stage_kernel for k > 1024: each warp sorts its row in shared memory (P keys).
-__global__ void __launch_bounds__(128) rank_stage_smem_kernel(const uint64_t* __restrict__ stage,
-                                                              const uint8_t* __restrict__ gsplit, int64_t T,
-                                                              int topk, int P, int nq, int next_n, int ngroups,
-                                                              int32_t* out_idx, float* out_val) {
-  extern __shared__ uint64_t rbuf[];            // 4 warps x P keys
-  grid_dependency_wait();
-  grid_launch_dependents();
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int64_t t = (int64_t)blockIdx.x * 4 + w;
-  if (t >= T) return;
-  const int64_t b = t / next_n;
-  const int i = (int)(t - b * next_n);
-  if (__ldg(gsplit + b * ngroups + i / nq)) return;
-  uint64_t* buf = rbuf + (size_t)w * P;
-  for (int e = lane; e < topk; e += 32) buf[e] = __ldg(stage + t * topk + e);
-  __syncwarp();
-  rank_row_smem(buf, topk, P, topk, true, out_idx + t * topk, out_val ? out_val + t * topk : nullptr);
-}
-
-cudaError_t launch_rank_stage(const uint64_t* stage, const uint8_t* gsplit, int nq, int ngroups,
-                              const dsa_queries& qs, int topk, int32_t* out_idx, float* out_val,
-                              cudaStream_t stream) {
-  const int64_t T = (int64_t)qs.B * qs.next_n;
-  if (T <= 0) return cudaSuccess;
-  const int P = next_pow2(topk);
-  cudaLaunchConfig_t cfg{};
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-  if (P <= 1024) {
-    cfg.gridDim = dim3((unsigned)((T + 7) / 8));
-    cfg.blockDim = dim3(256);
-    if (P <= 256) e = cudaLaunchKernelEx(&cfg, rank_stage_kernel<8>, stage, gsplit, T, topk, nq, (int)qs.next_n, ngroups, out_idx, out_val);
-    else if (P <= 512) e = cudaLaunchKernelEx(&cfg, rank_stage_kernel<16>, stage, gsplit, T, topk, nq, (int)qs.next_n, ngroups, out_idx, out_val);
-    else e = cudaLaunchKernelEx(&cfg, rank_stage_kernel<32>, stage, gsplit, T, topk, nq, (int)qs.next_n, ngroups, out_idx, out_val);
-  } else {
-    const size_t smem = (size_t)4 * P * 8;
-    e = cudaFuncSetAttribute(rank_stage_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3((unsigned)((T + 3) / 4));
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = smem;
-    e = cudaLaunchKernelEx(&cfg, rank_stage_smem_kernel, stage, gsplit, T, topk, P, nq, (int)qs.next_n, ngroups,
-                           out_idx, out_val);
-  }
-  note_launch();
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
 TopkPlan plan_topk(const dsa_queries& qs, int topk) {
   TopkPlan pl{};
   pl.pow2 = next_pow2(topk);

@@ -52,14 +52,12 @@ def _qs(B=1, n=1, L=4096, causal=True):
 
 def test_workspace_plans_are_host_only(lib):
     ws = lambda qs, k: dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, qs, k)
-    # the fused call's workspace: the plan (9 B per query group) plus two partial top-k
-    # lists per CTA (one CTA per slice of the work, at least one per SM); four-row items
-    # also stage each row's top-k (8 B per slot) for the rank kernel
+    # the fused call's workspace: the plan (8 B per query group) plus two partial top-k
+    # lists per CTA (one CTA per slice of the work, at least one per SM)
     flash = dsa.make_queries(64, 1, 0x1000, 65536, True)
     n = ws(flash, 512)
     assert n >= 148 * 2 * 512 * 8
-    # per query group: its line start and list position (4 B each) and a split flag (1 B)
-    assert ws(dsa.make_queries(128, 1, 0x1000, 65536, True), 512) - n == 64 * 9
+    assert ws(dsa.make_queries(128, 1, 0x1000, 65536, True), 512) - n == 64 * 8
     # the partial lists grow with k, whatever the batch
     prefill = dsa.make_queries(1, 16384, 0x1000, 16384, True)
     for qs in (flash, prefill):
