@@ -41,6 +41,10 @@ dsa_status check_keys(const dsa_keys& k, dsa_dtype dt, int B) {
   if (k.data == nullptr || k.num_rows < 1) return DSA_ERR_INVALID_ARG;
   if (!aligned(k.data, 16)) return DSA_ERR_INVALID_ARG;
   if (dt == DSA_E4M3 && k.scale == nullptr) return DSA_ERR_INVALID_ARG;
+  if (dt == DSA_E4M3_MXFP4K) {
+    if (k.scale_e8m0 == nullptr || !aligned(k.scale_e8m0, 16)) return DSA_ERR_INVALID_ARG;
+    if (k.block_table == nullptr && k.num_rows % 4 != 0) return DSA_ERR_UNSUPPORTED;   // 16-byte scale copies
+  }
   if (k.num_rows > INT32_MAX) return DSA_ERR_UNSUPPORTED;
   if (k.block_table != nullptr) {
     const int bs = k.block_size;
@@ -54,12 +58,12 @@ dsa_status check_keys(const dsa_keys& k, dsa_dtype dt, int B) {
 
 dsa_status check_indexer_common(const void* q, const float* q_scale, dsa_dtype dtype, const float* weights, int H,
                                 int D, const dsa_keys& keys, const dsa_queries& qs) {
-  if (dtype != DSA_BF16 && dtype != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+  if (dtype != DSA_BF16 && dtype != DSA_E4M3 && dtype != DSA_E4M3_MXFP4K) return DSA_ERR_INVALID_ARG;
   if (H != 64 || D != 128) return DSA_ERR_UNSUPPORTED;
   dsa_status s = check_queries(qs);
   if (s != DSA_OK) return s;
   if (q == nullptr || weights == nullptr || !aligned(q, 16)) return DSA_ERR_INVALID_ARG;
-  if (dtype == DSA_E4M3 && q_scale == nullptr) return DSA_ERR_INVALID_ARG;
+  if (dtype != DSA_BF16 && q_scale == nullptr) return DSA_ERR_INVALID_ARG;
   return check_keys(keys, dtype, qs.B);
 }
 
@@ -79,12 +83,12 @@ dsa_status dsa_indexer_logits(const void* q, const float* q_scale, dsa_dtype dty
   if (s != DSA_OK) return s;
   if (logits == nullptr || ld_logits < qs.max_context_len) return DSA_ERR_INVALID_ARG;
   if ((int64_t)qs.B * qs.next_n == 0 || qs.max_context_len == 0) return DSA_OK;
-  const IndexerPlan pl = plan_indexer(dtype == DSA_E4M3, qs, 0);
+  const IndexerPlan pl = plan_indexer(dtype, qs, 0);
   if (!pl.ok) return DSA_ERR_UNSUPPORTED;
   IndexerArgs a{};
   a.q = q;
   a.q_scale = q_scale;
-  a.fp8 = dtype == DSA_E4M3;
+  a.fp8 = dtype != DSA_BF16;
   a.weights = weights;
   a.keys = keys;
   a.qs = qs;
@@ -115,13 +119,13 @@ dsa_status dsa_indexer_logits_topk(const void* q, const float* q_scale, dsa_dtyp
   if (s != DSA_OK) return s;
   if (topk < 1 || topk > 2048 || out_idx == nullptr) return DSA_ERR_INVALID_ARG;
   if ((int64_t)qs.B * qs.next_n == 0) return DSA_OK;
-  const IndexerPlan pl = plan_indexer(dtype == DSA_E4M3, qs, topk);
+  const IndexerPlan pl = plan_indexer(dtype, qs, topk);
   if (!pl.ok) return DSA_ERR_UNSUPPORTED;
   if (pl.ws_bytes > 0 && (ws == nullptr || ws_bytes < pl.ws_bytes || !aligned(ws, 8))) return DSA_ERR_WORKSPACE;
   IndexerArgs a{};
   a.q = q;
   a.q_scale = q_scale;
-  a.fp8 = dtype == DSA_E4M3;
+  a.fp8 = dtype != DSA_BF16;
   a.weights = weights;
   a.keys = keys;
   a.qs = qs;
@@ -177,7 +181,7 @@ size_t dsa_workspace_bytes(dsa_op op, dsa_dtype dtype, dsa_queries qs, int topk)
   if (check_queries(qs) != DSA_OK || topk < 1 || topk > 2048) return 0;
   if (op == DSA_OP_TOPK) return plan_topk(qs, topk).ws_bytes;
   if (op == DSA_OP_LOGITS_TOPK) {
-    const IndexerPlan pl = plan_indexer(dtype == DSA_E4M3, qs, topk);
+    const IndexerPlan pl = plan_indexer(dtype, qs, topk);
     return pl.ok ? pl.ws_bytes : 0;
   }
   return 0;

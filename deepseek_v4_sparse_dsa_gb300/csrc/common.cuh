@@ -107,6 +107,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// 1-D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global
+// to shared memory, completing that many bytes of transaction count on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------------
 // Work plan of the fused score + top-k (written by plan_kernel, read by the indexer and
 // merge kernels).  Query groups lie end to end on a line; group u spans positions
@@ -885,6 +893,19 @@ __device__ __forceinline__ uint2 lut_entry(uint32_t byte) {
     if (n & 7u) m |= 0xFFFFu << (16 * h);
   }
   return make_uint2(v, m);
+}
+
+// bf16 bit pattern of an OCP E4M3 code (exact: every E4M3 value is a bf16 value).
+// Normal codes keep their 3 mantissa bits under the rebased exponent (bias 7 -> 127);
+// subnormals m * 2^-9 are renormalised; S.1111.111 is NaN.
+__device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t c) {
+  const uint32_t s = (c & 0x80u) << 8;
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  if (e == 15u && m == 7u) return s | 0x7FC0u;
+  if (e != 0u) return s | ((e + 120u) << 7) | (m << 4);
+  if (m == 0u) return s;
+  const uint32_t k = 31u - __clz(m);                  // leading bit of m (0..2)
+  return s | ((k + 118u) << 7) | ((m << (7u - k)) & 0x7Fu);
 }
 
 // Eight elements (nibble bytes of w, low nibble first) times 2^(b-127) as bf16 pairs.

@@ -7,6 +7,7 @@
 // plan kernel -> indexer kernel -> merge kernel.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "indexer_kernel.cuh"
@@ -209,12 +210,30 @@ size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap) {
   return s;
 }
 
+// FP4-key mode: bf16 Q tile, `conv` converted bf16 key tiles, the E4M3 Q staging tile,
+// `stages` FP4 stages of 128 x (64 + 4) bytes, the 2 KB decode table.
+size_t smem_bytes_f4k(int nq, int stages, int conv, bool topk, int cap) {
+  size_t s = 1024;
+  s += (size_t)nq * 64 * 256;                        // bf16 Q tile
+  s += (size_t)conv * 128 * 256;                     // converted key tiles
+  s += (size_t)nq * 64 * 128;                        // E4M3 Q staging
+  s += (size_t)stages * 128 * 68;                    // FP4 stages
+  s += 2048;                                         // decode table
+  s += (size_t)(2 * stages + 16 + 2 * conv + 1) * 8; // barriers
+  s += sizeof(EpiSmem<4>) + 16;
+  if (topk) s += (size_t)nq * cap * 8;
+  return s;
+}
+
 }  // namespace
 
-IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
+IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk) {
   IndexerPlan pl{};
+  const bool fp8 = dt != DSA_BF16;                   // E4M3 queries
   const bool tk = topk > 0;
+  pl.f4k = dt == DSA_E4M3_MXFP4K;
   pl.nq = qs.next_n == 1 ? 1 : (qs.next_n == 2 ? 2 : 4);
+  if (pl.f4k && pl.nq > 2) pl.nq = 2;                // FP4 keys: one epilogue group, <= 2 rows per item
   if (tk) {
     pl.pow2 = next_pow2(topk);
     // room for several tiles of inserts between cut-backs
@@ -252,6 +271,19 @@ IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk) {
   if (pl.ctas_per_sm == 1 && pl.nq >= 2) pl.eg = 2;   // one CTA per SM: two groups take turns
   if (tk && (pl.cap < topk + 256 || pl.cap < pl.pow2)) pl.ok = false;
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
+  if (pl.f4k) {
+    // one CTA per SM: one epilogue group, four converter warps, a deep FP4 ring and as
+    // many converted tiles (2..3) as shared memory holds
+    pl.eg = 1;
+    pl.ctas_per_sm = 1;
+    pl.stages = 6;
+    pl.conv_slots = 3;
+    while (pl.conv_slots > 2 && smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap) > kSmemLimit)
+      --pl.conv_slots;
+    while (pl.stages > 2 && smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap) > kSmemLimit) --pl.stages;
+    pl.smem = smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap);
+    if (pl.smem > kSmemLimit) pl.ok = false;
+  }
   // as many accumulator buffers (up to 4) as TMEM holds for the CTAs sharing an SM, so
   // the MMAs can run ahead of an epilogue busy cutting its candidates back
   pl.nbuf_log2 = 2;
@@ -307,7 +339,8 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   CUtensorMap mq, mk;
   const uint32_t box_rows = paged ? (uint32_t)(a.keys.block_size < 128 ? a.keys.block_size : 128) : 128u;
   if (!make_map(&mq, a.q, a.fp8, (uint64_t)T * 64, (uint32_t)(pl.nq * 64))) return cudaErrorInvalidValue;
-  if (!make_map(&mk, a.keys.data, a.fp8, (uint64_t)a.keys.num_rows, box_rows)) return cudaErrorInvalidValue;
+  if (pl.f4k) memset(&mk, 0, sizeof(mk));             // FP4 keys arrive by plain bulk copies
+  else if (!make_map(&mk, a.keys.data, a.fp8, (uint64_t)a.keys.num_rows, box_rows)) return cudaErrorInvalidValue;
   IndexerParams prm{};
   prm.weights = a.weights;
   prm.q_scale = a.q_scale;
@@ -327,6 +360,9 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   prm.chunk = pl.chunk;
   prm.stages = pl.stages;
   prm.nbuf_log2 = pl.nbuf_log2;
+  prm.kv_fp4 = pl.f4k ? static_cast<const uint8_t*>(a.keys.data) : nullptr;
+  prm.kv_e8m0 = pl.f4k ? a.keys.scale_e8m0 : nullptr;
+  prm.conv_slots = pl.conv_slots;
   prm.logits = a.logits;
   prm.ld = a.ld;
   prm.topk = a.topk;

@@ -72,6 +72,11 @@ struct IndexerParams {
   int32_t ngroups, nchunks, chunk;  // static schedule (logits mode)
   int32_t topk, cap, pow2, stages;
   int32_t nbuf_log2;        // log2 of the TMEM accumulator buffers (1 or 2)
+  // FP4-key mode: keys read from the paged mxfp4 cache (nibble rows of 64 bytes, E8M0
+  // rows of 4 bytes), converted to bf16 tiles on chip by the converter warps
+  const uint8_t* kv_fp4;
+  const uint8_t* kv_e8m0;
+  int32_t conv_slots;       // converted bf16 key tiles in flight
 };
 
 constexpr int kMaxPer = 10;        // candidate capacity per query <= 256 * kMaxPer
@@ -95,6 +100,7 @@ struct EpiSmem {
   int abort;
   int stop;
   int last;
+  int cstop;                // FP4-key mode: the converters' own stop decision
   uint32_t cnt[4];
   uint64_t thr[4];
   EngineScratch esc;
@@ -225,31 +231,44 @@ __device__ bool next_slice_item(const IndexerParams& p, int slice, int r0, int r
   return false;
 }
 
-template <bool kFP8, int NQ, bool kTopk, int EG>
-__global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
+template <bool kFP8, int NQ, bool kTopk, int EG, bool kF4K>
+__global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && !kF4K) ? 2 : 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const IndexerParams p) {
+  // kF4K: E4M3 queries against mxfp4 keys; both become bf16 on chip (exactly: E4M3 and
+  // E2M1 x 2^(b-127) values are bf16 values) and the contraction runs as bf16.
+  static_assert(!kF4K || (kFP8 && EG == 1), "FP4-key mode: E4M3 queries, one epilogue group");
+  constexpr bool kMmaFP8 = kFP8 && !kF4K;          // E4M3 x E4M3 contraction
+  constexpr bool kKeyScale = kFP8 && !kF4K;        // per-key fp32 scale (E4M3 keys)
   constexpr int N = NQ * 64;                       // MMA N: (query, head) rows
-  constexpr int ELT = kFP8 ? 1 : 2;                // bytes per element
-  constexpr int KCH = kFP8 ? 1 : 2;                // 128-byte K chunks per row (D = 128)
+  constexpr int ELT = kFP8 ? 1 : 2;                // bytes per element as stored in HBM
+  constexpr int KCH = kMmaFP8 ? 1 : 2;             // 128-byte K chunks per row in the MMA operands
   constexpr uint32_t Q_CHUNK = N * 128;            // bytes of one K chunk of the Q tile
   constexpr uint32_t Q_BYTES = Q_CHUNK * KCH;
   constexpr uint32_t K_CHUNK = 128 * 128;          // 128 keys x 128 bytes
   constexpr uint32_t K_BYTES = K_CHUNK * KCH;
   constexpr int KSTEPS = KCH * 4;                  // 32 bytes of K per MMA
+  constexpr uint32_t F4_BYTES = 128 * 64 + 128 * 4;   // FP4-key stage: nibble rows, then E8M0 rows
   const int NBL = p.nbuf_log2;                     // NB = 2^NBL accumulator buffers in TMEM
   const int NBM = (1 << NBL) - 1;
   const uint32_t TMEM_COLS = ((N << NBL) < 32) ? 32u : (uint32_t)next_pow2(N << NBL);
-  constexpr uint32_t IDESC = kFP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N);
+  constexpr uint32_t IDESC = kMmaFP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
+  const int CR = kF4K ? p.conv_slots : 0;
+  // layout: Q tile (MMA operand) | key stages (TMA) or converted tiles [CR] (kF4K) |
+  //         kF4K: E4M3 Q staging, FP4 stages [S], decode table | barriers | epilogue state
   uint8_t* q_s = smem;
-  uint8_t* k_s = smem + Q_BYTES;                         // S stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(k_s + (size_t)S * K_BYTES);
+  uint8_t* k_s = smem + Q_BYTES;                         // S stages (kF4K: CR converted tiles)
+  uint8_t* q8_s = k_s + (size_t)(kF4K ? CR : S) * K_BYTES;   // kF4K: the E4M3 Q tile as loaded
+  uint8_t* f4_s = q8_s + (kF4K ? Q_CHUNK : 0);           // kF4K: S stages of F4_BYTES
+  uint2* lut = reinterpret_cast<uint2*>(f4_s + (kF4K ? (size_t)S * F4_BYTES : 0));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(lut) + (kF4K ? 2048 : 0));
   // full[S] | empty[S] | tfull[4] | tempty[4] | qfull | qempty | ifull[2] | iempty[2] | mmadone | tmemfree
-  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 16);
+  // | kF4K: cfull[CR] | cfree[CR] | qready
+  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 16 + (kF4K ? 2 * CR + 1 : 0));
   uint64_t* ebuf = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(es) + sizeof(EpiSmem<NQ>) + 15) & ~uintptr_t(15));
 
@@ -259,6 +278,8 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
   const uint32_t ifull0 = smem_u32(bars + 2 * S + 10), iempty0 = smem_u32(bars + 2 * S + 12);
   const uint32_t mmadone = smem_u32(bars + 2 * S + 14);
   const uint32_t tmemfree = smem_u32(bars + 2 * S + 15);   // every epilogue warp is done with TMEM
+  const uint32_t cfull0 = smem_u32(bars + 2 * S + 16), cfree0 = cfull0 + 8u * (uint32_t)CR;
+  const uint32_t qready = cfree0 + 8u * (uint32_t)CR;       // kF4K: the bf16 Q tile is written
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -271,15 +292,20 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kF4K ? 4 : 1);   // kF4K: the converter warps free FP4 stages
     }
+    for (int c = 0; c < CR; ++c) {
+      mbar_init(cfull0 + 8 * c, 4);              // the 4 converter warps wrote the tile
+      mbar_init(cfree0 + 8 * c, 1);              // the MMAs that read it are done
+    }
+    if (kF4K) mbar_init(qready, 4);
     for (int a = 0; a < 4; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
       mbar_init(tempty0 + 8 * a, 4);          // the 4 warps of the group that read the tile
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(ifull0 + 8 * a, 1);
-      mbar_init(iempty0 + 8 * a, 1 + 4 * EG);
+      mbar_init(iempty0 + 8 * a, 1 + 4 * EG + (kF4K ? 4 : 0));
     }
     mbar_init(qfull, 1);
     mbar_init(qempty, 1);
@@ -317,7 +343,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     }
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
+      if (!kF4K) tma_prefetch_desc(&tm_k);
       if (p.plan && mode == kPlanGroups) next = (int)atomicAdd(p.work, 1u);   // one item ahead
     }
     int tiles_issued = 0, items_issued = 0;
@@ -366,9 +392,14 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
       if (lane == 0) {
         ok = mbar_wait(qempty, ((uint32_t)n & 1u) ^ 1u, limit, abort_flag);
         if (ok) {
-          mbar_arrive_expect_tx(qfull, Q_BYTES);
-          for (int kc = 0; kc < KCH; ++kc)
-            tma_load_2d(smem_u32(q_s + kc * Q_CHUNK), &tm_q, qfull, kc * (128 / ELT), it.t0 * 64);
+          if (kF4K) {                           // the E4M3 tile, for the converters
+            mbar_arrive_expect_tx(qfull, Q_CHUNK);
+            tma_load_2d(smem_u32(q8_s), &tm_q, qfull, 0, it.t0 * 64);
+          } else {
+            mbar_arrive_expect_tx(qfull, Q_BYTES);
+            for (int kc = 0; kc < KCH; ++kc)
+              tma_load_2d(smem_u32(q_s + kc * Q_CHUNK), &tm_q, qfull, kc * (128 / ELT), it.t0 * 64);
+          }
           ++items_issued;
           mbar_arrive(ifull0 + 8 * slot);
         }
@@ -403,7 +434,37 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
           if (ok) {
             const uint32_t stage = smem_u32(k_s + (size_t)s * K_BYTES);
             const uint32_t fb = full0 + 8 * s;
-            if (!paged) {
+            if constexpr (kF4K) {
+              // nibble rows to the stage's front, E8M0 rows after them (plain bulk copies:
+              // 64 + 4 bytes per key; every source and size is a multiple of 16 bytes)
+              const uint32_t f4 = smem_u32(f4_s + (size_t)s * F4_BYTES);
+              if (!paged) {
+                const int rows = (int)max((int64_t)0, min((int64_t)128, p.num_rows - j0));
+                mbar_arrive_expect_tx(fb, (uint32_t)rows * 68u);
+                if (rows > 0) {
+                  bulk_load(f4, p.kv_fp4 + (size_t)j0 * 64, (uint32_t)rows * 64u, fb);
+                  bulk_load(f4 + 8192u, p.kv_e8m0 + (size_t)j0 * 4, (uint32_t)rows * 4u, fb);
+                }
+              } else {
+                const int pg0 = j0 / bs, pg1 = bs >= 128 ? pg0 : (jend - 1) / bs;
+                const int span = bs >= 128 ? 128 : bs;          // rows copied per page
+                uint32_t bytes = 0;
+                for (int pg = pg0; pg <= pg1; ++pg) {
+                  const int64_t blk = es->pages[pg - win0];
+                  if (blk >= 0 && blk < p.num_blocks) bytes += (uint32_t)span * 68u;
+                  else raise_error(DSA_DEVERR_INDEX);
+                }
+                mbar_arrive_expect_tx(fb, bytes);
+                for (int pg = pg0; pg <= pg1; ++pg) {
+                  const int64_t blk = es->pages[pg - win0];
+                  if (blk < 0 || blk >= p.num_blocks) continue;
+                  const int64_t row = blk * bs + (bs >= 128 ? (j0 % bs) : 0);
+                  const uint32_t at = (uint32_t)(pg - pg0) * (uint32_t)span;
+                  bulk_load(f4 + at * 64u, p.kv_fp4 + (size_t)row * 64, (uint32_t)span * 64u, fb);
+                  bulk_load(f4 + 8192u + at * 4u, p.kv_e8m0 + (size_t)row * 4, (uint32_t)span * 4u, fb);
+                }
+              }
+            } else if (!paged) {
               mbar_arrive_expect_tx(fb, K_BYTES);
               for (int kc = 0; kc < KCH; ++kc)
                 tma_load_2d(stage + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), j0);
@@ -465,12 +526,15 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
         if (!(ok = mbar_wait(ifull0 + 8 * slot, (uint32_t)(n >> 1) & 1u, limit, abort_flag))) break;
         const ItemInfo it = es->info[slot];
         if (!it.valid) break;
-        if (!(ok = mbar_wait(qfull, (uint32_t)n & 1u, limit, abort_flag))) break;
+        // the Q tile: loaded by TMA, or (kF4K) converted to bf16 by the converter warps
+        if (!(ok = mbar_wait(kF4K ? qready : qfull, (uint32_t)n & 1u, limit, abort_flag))) break;
         const uint32_t qbase = smem_u32(q_s);
         for (int i = 0; i < it.ntiles; ++i, ++T) {
-          const int s = T % S;
+          const int s = kF4K ? T % CR : T % S;      // key stage, or (kF4K) converted tile
           const int a = T & NBM;
-          ok = mbar_wait(full0 + 8 * s, (uint32_t)(T / S) & 1u, limit, abort_flag) &&
+          const uint32_t kready = kF4K ? cfull0 + 8 * s : full0 + 8 * s;
+          const uint32_t kphase = (uint32_t)(kF4K ? T / CR : T / S) & 1u;
+          ok = mbar_wait(kready, kphase, limit, abort_flag) &&
                mbar_wait(tempty0 + 8 * a, ((uint32_t)(T >> NBL) & 1u) ^ 1u, limit, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -481,12 +545,12 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
             const uint32_t off = (uint32_t)(kk & 3) * 32u;   // 16 bf16 / 32 E4M3 along K
             const uint64_t adesc = smem_desc_sw128(stage + (uint32_t)(kk >> 2) * K_CHUNK + off);
             const uint64_t bdesc = smem_desc_sw128(qbase + (uint32_t)(kk >> 2) * Q_CHUNK + off);
-            if (kFP8)
+            if (kMmaFP8)
               mma_e4m3(d, adesc, bdesc, IDESC, kk > 0 ? 1u : 0u);
             else
               mma_bf16(d, adesc, bdesc, IDESC, kk > 0 ? 1u : 0u);
           }
-          mma_commit(empty0 + 8 * s);
+          mma_commit(kF4K ? cfree0 + 8 * s : empty0 + 8 * s);
           mma_commit(tfull0 + 8 * a);
         }
         if (!ok) break;
@@ -506,7 +570,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
-  } else {
+  } else if (!kF4K || warp < 2 + 4 * EG) {
     // ============================ epilogue ============================
     // EG groups of 4 warps take the tiles in turn (global tile T goes to group T % EG);
     // all NT threads share the per-row candidate buffers and cut them back together.
@@ -565,7 +629,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
       };
       int64_t blk_next = (paged && first < it.ntiles) ? page_of(first) : -1;
       float ks_next = 1.f;                      // contiguous E4M3 keys: scale of the next tile's key
-      if (kFP8 && !paged && first < it.ntiles && it.ks + first * 128 + row < p.num_rows)
+      if (kKeyScale && !paged && first < it.ntiles && it.ks + first * 128 + row < p.num_rows)
         ks_next = __ldg(p.k_scale + it.ks + first * 128 + row);
       for (int m = 0; m < niter; ++m) {
         // One group checks its buffers every CI tiles (one barrier per check), leaving
@@ -603,10 +667,10 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
           const int64_t blk = blk_next;
           if (i + EG < it.ntiles) blk_next = page_of(i + EG);
           valid = blk >= 0 && blk < p.num_blocks;
-          if (kFP8 && valid) kscale = __ldg(p.k_scale + blk * bs + (j % bs));
+          if (kKeyScale && valid) kscale = __ldg(p.k_scale + blk * bs + (j % bs));
         } else {
           valid = j < p.num_rows;
-          if (kFP8) {
+          if (kKeyScale) {
             kscale = ks_next;
             const int jn = j + EG * 128;
             if (i + EG < it.ntiles && jn < p.num_rows) ks_next = __ldg(p.k_scale + jn);
@@ -628,7 +692,7 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           float sq = v[q];
-          if (kFP8) sq = sq * kscale;
+          if (kKeyScale) sq = sq * kscale;
           v[q] = canon_zero(sq);
         }
         tc_fence_before();
@@ -719,6 +783,105 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(tmemfree);
   }
+  else if constexpr (kF4K) {
+    // ============================ converters ============================
+    // Four warps turn each item's E4M3 Q tile, and each FP4 stage, into bf16 tiles in the
+    // MMA's operand layout (K-major rows of 128 bytes, 128-byte swizzle: 16-byte piece c
+    // of row r at r * 128 + ((c ^ (r & 7)) << 4)).  Thread ct owns key row ct of a tile.
+    // A failed wait skips that step's work; the group stops together at item boundaries.
+    constexpr int CBAR = 2;
+    const int ct = threadIdx.x - (64 + 128 * EG);
+    lut[ct] = lut_entry((uint32_t)ct);
+    lut[ct + 128] = lut_entry((uint32_t)ct + 128u);
+    group_sync<128>(CBAR);
+    int T = 0;
+    for (int n = 0;; ++n) {
+      const int slot = n & 1;
+      bool ok = (lane == 0) ? mbar_wait(ifull0 + 8 * slot, (uint32_t)(n >> 1) & 1u, limit, abort_flag) : true;
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (!ok && lane == 0) {
+        raise_error(DSA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      group_sync<128>(CBAR);
+      if (ct == 0) es->cstop = (*abort_flag != 0) || !es->info[slot].valid;
+      group_sync<128>(CBAR);
+      if (es->cstop) break;
+      const int ntiles = es->info[slot].ntiles;
+      // the item's Q tile
+      bool okq = (lane == 0) ? mbar_wait(qfull, (uint32_t)n & 1u, limit, abort_flag) : true;
+      okq = __shfl_sync(0xFFFFFFFFu, okq ? 1 : 0, 0) != 0;
+      if (okq) {
+        __syncwarp();
+        for (int r = ct; r < N; r += 128) {
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc) {           // E4M3 piece pc: elements 16 pc .. 16 pc + 15
+            const uint4 src = *reinterpret_cast<const uint4*>(q8_s + r * 128 + ((pc ^ (r & 7)) << 4));
+            const uint32_t wsrc[4] = {src.x, src.y, src.z, src.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t lo = e4m3_to_bf16_bits((wsrc[k] >> (16 * h)) & 0xFFu);
+                const uint32_t hi = e4m3_to_bf16_bits((wsrc[k] >> (16 * h + 8)) & 0xFFu);
+                o[2 * k + h] = lo | (hi << 16);
+              }
+            // bf16 elements 16 pc .. 16 pc + 15: K chunk pc / 4, pieces 2 (pc % 4) and + 1
+            uint8_t* dst = q_s + (pc >> 2) * Q_CHUNK + r * 128;
+            const int d0 = 2 * (pc & 3), d1 = d0 + 1;
+            *reinterpret_cast<uint4*>(dst + ((d0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + ((d1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the MMAs
+      } else if (lane == 0) {
+        raise_error(DSA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      __syncwarp();
+      if (lane == 0 && okq) mbar_arrive(qready);
+      // the item's key tiles
+      for (int i = 0; i < ntiles; ++i, ++T) {
+        const int s4 = T % S, c = T % CR;
+        bool okt = (lane == 0) ? (mbar_wait(full0 + 8 * s4, (uint32_t)(T / S) & 1u, limit, abort_flag) &&
+                                  mbar_wait(cfree0 + 8 * c, ((uint32_t)(T / CR) & 1u) ^ 1u, limit, abort_flag))
+                               : true;
+        okt = __shfl_sync(0xFFFFFFFFu, okt ? 1 : 0, 0) != 0;
+        if (!okt) {
+          if (lane == 0) {
+            raise_error(DSA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          continue;
+        }
+        __syncwarp();
+        const uint8_t* f4 = f4_s + (size_t)s4 * F4_BYTES;
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(f4 + 8192 + ct * 4);
+        uint8_t* dst = k_s + (size_t)c * K_BYTES + ct * 128;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {                 // group g: elements 32 g .. 32 g + 31
+          const uint4 v = *reinterpret_cast<const uint4*>(f4 + ct * 64 + g * 16);
+          const uint32_t b = (sw >> (8 * g)) & 0xFFu;
+          const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {               // elements 32 g + 8 w .. + 7
+            const uint4 o = decode8(words[w], b, lut);
+            const int pc = (g & 1) * 4 + w;           // piece within K chunk g / 2
+            *reinterpret_cast<uint4*>(dst + (g >> 1) * K_CHUNK + ((pc ^ (ct & 7)) << 4)) = o;
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(cfull0 + 8 * c);
+          mbar_arrive(empty0 + 8 * s4);
+        }
+      }
+      group_sync<128>(CBAR);
+      if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
+    }
+  }
   // No CTA-wide barrier here: the warps leave as their roles end (warp 1 last frees
   // TMEM); shared memory stays valid until every thread of the CTA has exited.
 }
@@ -727,15 +890,15 @@ __global__ void __launch_bounds__(64 + 128 * EG, EG == 1 ? 2 : 1)
 // Launch of one instantiation
 // =====================================================================================
 
-template <bool kFP8, int NQ, bool kTopk, int EG>
+template <bool kFP8, int NQ, bool kTopk, int EG, bool kF4K = false>
 static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& prm,
                               const IndexerPlan& pl, int grid, cudaStream_t st) {
-  auto kern = indexer_kernel<kFP8, NQ, kTopk, EG>;
+  auto kern = indexer_kernel<kFP8, NQ, kTopk, EG, kF4K>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(64 + 128 * EG);
+  cfg.blockDim = dim3(64 + 128 * EG + (kF4K ? 128 : 0));
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -752,6 +915,10 @@ static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, cons
 template <bool kFP8, bool kTopk>
 static cudaError_t dispatch_nq(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& prm,
                                const IndexerPlan& pl, int grid, cudaStream_t st) {
+  if constexpr (kFP8) {
+    if (pl.f4k) return pl.nq == 1 ? launch_one<true, 1, kTopk, 1, true>(mq, mk, prm, pl, grid, st)
+                                  : launch_one<true, 2, kTopk, 1, true>(mq, mk, prm, pl, grid, st);
+  }
   switch (pl.nq * 2 + pl.eg) {
     case 3: return launch_one<kFP8, 1, kTopk, 1>(mq, mk, prm, pl, grid, st);
     case 5: return launch_one<kFP8, 2, kTopk, 1>(mq, mk, prm, pl, grid, st);

@@ -31,11 +31,13 @@ struct IndexerPlan {
   int64_t items;     // logits mode: work items; top-k mode: query groups
   size_t ws_bytes;   // workspace bytes (top-k mode)
   size_t prefix_off, ufirst_off, split_off, order_off, partial_off, meta_off;   // byte offsets in ws
+  bool f4k;          // E4M3 queries, keys from the paged mxfp4 cache (converted on chip)
+  int conv_slots;    // FP4-key mode: converted bf16 key tiles in flight
   bool ok;           // false: shape does not fit this build
 };
 
 // topk == 0 plans the logits-only kernel.
-IndexerPlan plan_indexer(bool fp8, const dsa_queries& qs, int topk);
+IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk);
 
 struct IndexerArgs {
   const void* q;

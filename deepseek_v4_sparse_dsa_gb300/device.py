@@ -52,6 +52,8 @@ class DeviceBatch:
     @classmethod
     def from_workload(cls, wl, device="cuda") -> "DeviceBatch":
         dt = dsa.DSA_E4M3 if wl.dtype == "e4m3" else dsa.DSA_BF16
+        if getattr(wl, "k_format", "native") == "mxfp4":
+            dt = dsa.DSA_E4M3_MXFP4K
         return cls(wl.B, wl.next_n, wl.causal, wl.topk, dt, wl.max_context_len,
                    _dev(wl.context_lens.astype(np.int32), device),
                    _dev(wl.q, device), _dev(wl.q_scale, device), _dev(wl.weights, device),
@@ -60,6 +62,8 @@ class DeviceBatch:
                    _dev(wl.gather_block_table, device))
 
     def keys(self) -> dsa.dsa_keys:
+        if self.dtype == dsa.DSA_E4M3_MXFP4K:     # mxfp4 cache rows: nibbles + E8M0 bytes
+            return dsa.make_keys(self.k_data, None, self.block_table, self.block_size, scale_e8m0=self.k_scale)
         return dsa.make_keys(self.k_data, self.k_scale, self.block_table, self.block_size)
 
     def queries(self) -> dsa.dsa_queries:

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdsa_gb300.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_WORKSPACE = 0, 1, 2, 3, 4
-DSA_BF16, DSA_E4M3 = 0, 1
+DSA_BF16, DSA_E4M3, DSA_E4M3_MXFP4K = 0, 1, 2
 DSA_OP_TOPK, DSA_OP_LOGITS_TOPK = 1, 2
 DSA_DEVERR_INDEX, DSA_DEVERR_TIMEOUT = 1, 2
 
@@ -36,6 +36,7 @@ class dsa_keys(ctypes.Structure):
         ("bt_stride", c_int64),
         ("block_size", c_int32),
         ("num_rows", c_int64),
+        ("scale_e8m0", c_void_p),
     ]
 
 
@@ -118,11 +119,12 @@ def status_string(status: int) -> str:
     return load().dsa_status_string(status).decode()
 
 
-def make_keys(data, scale=None, block_table=None, block_size: int = 64, num_rows=None) -> dsa_keys:
-    """dsa_keys from tensors: data [rows, 128]; block_table [B, stride] (or None)."""
+def make_keys(data, scale=None, block_table=None, block_size: int = 64, num_rows=None, scale_e8m0=None) -> dsa_keys:
+    """dsa_keys from tensors: data [rows, 128] (mxfp4 keys: [rows, 64] nibble bytes with
+    scale_e8m0 [rows, 4]); block_table [B, stride] (or None)."""
     rows = int(num_rows if num_rows is not None else data.shape[0])
     stride = int(block_table.shape[1]) if block_table is not None else 0
-    return dsa_keys(_ptr(data), _ptr(scale), _ptr(block_table), stride, int(block_size), rows)
+    return dsa_keys(_ptr(data), _ptr(scale), _ptr(block_table), stride, int(block_size), rows, _ptr(scale_e8m0))
 
 
 def make_queries(B: int, next_n: int, context_lens, max_context_len: int, causal: bool) -> dsa_queries:

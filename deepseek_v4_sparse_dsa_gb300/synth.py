@@ -178,7 +178,8 @@ class Workload:
     weights   [T, H] float32
     k_data    [rows, D] uint16 / uint8: the paged pool (nblk * block_size rows)
               when block_table is set, else the contiguous keys of one sequence
-    k_scale   [rows] float32 or None
+              (k_format "mxfp4": [rows, D/2] nibble bytes of the paged mxfp4 cache)
+    k_scale   [rows] float32 or None (k_format "mxfp4": [rows, D/32] E8M0 bytes)
     block_table [B, max_blocks] int32 or None (unused entries are -1)
     kv_fp4    [nblk_g, block_size, D/2] uint8, low nibble = even element
     kv_scale  [nblk_g, block_size, D/32] uint8 E8M0
@@ -204,6 +205,7 @@ class Workload:
     gather_block_table: Optional[np.ndarray] = None
     gather_pad_frac: float = 0.0
     seed: int = 0
+    k_format: str = "native"   # "mxfp4": k_data = nibble rows [rows, D/2], k_scale = E8M0 rows [rows, D/32]
 
     @property
     def T(self) -> int:
@@ -292,6 +294,22 @@ def make_flash_decode(seed: int = 2, B: int = 64, lmin: int = 4096, lmax: int = 
 def make_pro_mtp(seed: int = 3, B: int = 32, lmin: int = 32768, lmax: int = 131072,
                  with_keys: bool = True) -> Workload:
     return make_decode(seed, B, 2, lmin, lmax, 1024, "pro_mtp", 0.02, with_keys=with_keys)
+
+
+def make_flash_decode_fp4k(seed: int = 2, B: int = 64) -> Workload:
+    """The Flash decode batch scored in its FP8-q x FP4-k form: the queries quantised to
+    E4M3 with a per-(token, head) scale (rowmax / 448), the keys read straight from the
+    batch's paged mxfp4 cache (the cache the gather reads, through the same table)."""
+    wl = make_flash_decode(seed=seed, B=B, with_keys=False)
+    qf = (wl.q.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    wl.q, wl.q_scale = quantize_e4m3_rows(qf)
+    wl.dtype = "e4m3"
+    wl.k_format = "mxfp4"
+    nblk = wl.kv_fp4.shape[0]
+    wl.k_data = wl.kv_fp4.reshape(nblk * wl.block_size, D // 2)
+    wl.k_scale = wl.kv_scale.reshape(nblk * wl.block_size, D // 32)
+    wl.name = "flash_decode_fp4k"
+    return wl
 
 
 def make_prefill(seed: int = 4, T: int = 16384, topk: int = 512) -> Workload:

@@ -58,7 +58,12 @@ typedef enum {
   DSA_ERR_WORKSPACE = 4      /* ws is NULL or smaller than dsa_workspace_bytes */
 } dsa_status;
 
-typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1 } dsa_dtype;
+/* Storage of the indexer's inputs.  DSA_BF16: bf16 q and keys.  DSA_E4M3: OCP E4M3 q
+ * and keys with fp32 row scales.  DSA_E4M3_MXFP4K: OCP E4M3 q (with q_scale) scored
+ * against keys read straight from the paged mxfp4 cache (the fp8-q x fp4-k MQA-logits
+ * form that xkernels issue #27 "DSA indexer + attention: validate/provide gfx942
+ * forward path", "Status", names; see dsa_keys.scale_e8m0). */
+typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1, DSA_E4M3_MXFP4K = 2 } dsa_dtype;
 
 typedef enum { DSA_OP_TOPK = 1, DSA_OP_LOGITS_TOPK = 2 } dsa_op;
 
@@ -81,6 +86,12 @@ typedef enum { DSA_OP_TOPK = 1, DSA_OP_LOGITS_TOPK = 2 } dsa_op;
  *  - Contiguous (block_table == NULL): only B == 1; key j is row j, num_rows >= L_0.
  * `scale` is the per-row fp32 scale of E4M3 keys (same row indexing as `data`,
  * non-negative), NULL for bf16.
+ * With dtype DSA_E4M3_MXFP4K the keys are rows of the paged mxfp4 cache that
+ * mxfp4_paged_gather reads: `data` holds D/2 nibble bytes per row (low nibble = even
+ * element, E2M1), `scale_e8m0` D/32 E8M0 bytes per row (2^(b-127), 0xFF -> 0), both
+ * 16-byte aligned; `scale` is unused; a contiguous key array needs num_rows % 4 == 0.
+ * The key's value is E2M1 * 2^(b-127) exactly (scale bytes >= 254 overflow bf16 and
+ * are outside this mode's domain).
  */
 typedef struct {
   const void* data;
@@ -89,6 +100,7 @@ typedef struct {
   int64_t bt_stride;
   int32_t block_size;
   int64_t num_rows;
+  const uint8_t* scale_e8m0;
 } dsa_keys;
 
 /*

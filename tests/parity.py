@@ -22,8 +22,10 @@ LOGIT_RTOL = 1e-3
 
 def make_case(seed: int, lens, next_n: int = 1, paged: bool = True, block_size: int = 64,
               dtype: str = "bf16", causal: bool = True, topk: int = 64, gather: bool = False,
-              pad_frac: float = 0.0) -> Workload:
-    """A small batch with the configs' distributions: q, k ~ N(0,1), w ~ U(0,1)/8."""
+              pad_frac: float = 0.0, k_format: str = "native") -> Workload:
+    """A small batch with the configs' distributions: q, k ~ N(0,1), w ~ U(0,1)/8.
+    k_format "mxfp4": E4M3 queries against keys in the paged mxfp4 cache layout (random
+    nibble bytes, E8M0 scales uniform on 120..134 with 1% 0xFF, as the gather's cache)."""
     rng = Rng(seed)
     lens = np.asarray(lens, dtype=np.int32)
     B = lens.size
@@ -34,6 +36,8 @@ def make_case(seed: int, lens, next_n: int = 1, paged: bool = True, block_size: 
     else:
         assert B == 1
         table, rows = None, int(lens[0])
+        if k_format == "mxfp4":
+            rows = (rows + 3) // 4 * 4          # whole 16-byte rows of E8M0 bytes
         nblk = (rows + block_size - 1) // block_size
     if dtype == "bf16":
         q = synth.normal_bf16(rng, (T, H, D), "q")
@@ -46,19 +50,25 @@ def make_case(seed: int, lens, next_n: int = 1, paged: bool = True, block_size: 
         kf = np.empty((rows, D), np.float32)
         rng.normal_into(kf, "k")
         k, ks = synth.quantize_e4m3_rows(kf)
+    if k_format == "mxfp4":
+        assert dtype == "e4m3"
+        kn, ks8 = synth._mxfp4_pool(rng, (rows + block_size - 1) // block_size, block_size, "kcache")
+        k = kn.reshape(-1, D // 2)[:rows]
+        ks = ks8.reshape(-1, D // 32)[:rows]
     w = synth._weights(rng, T, "w")
     fp4 = sc = gtab = None
     if gather:
         gtab, gblk = (table, nblk) if paged else synth._page_pool(rng, lens, block_size, "gtab")
         fp4, sc = synth._mxfp4_pool(rng, gblk, block_size, "cache")
     return Workload("case", B, next_n, lens, causal, topk, dtype, q, qs, w, k, ks, table, block_size,
-                    fp4, sc, gtab, pad_frac, seed)
+                    fp4, sc, gtab, pad_frac, seed, k_format)
 
 
 def oracle_logits(wl: Workload, rows=None, width=None) -> np.ndarray:
     return orc.indexer_logits(wl.q, wl.q_scale, wl.dtype, wl.weights, wl.k_data, wl.k_scale,
                               wl.block_table, wl.block_size, wl.B, wl.next_n, wl.context_lens,
-                              wl.causal, rows=rows, width=width)
+                              wl.causal, rows=rows, width=width,
+                              k_dtype="mxfp4" if wl.k_format == "mxfp4" else None)
 
 
 def assert_logits_close(got: np.ndarray, ref: np.ndarray) -> float:

@@ -101,6 +101,22 @@ def test_host_side_rejections_launch_nothing(lib):
     # E4M3 without scales
     assert _status(dsa.dsa_indexer_logits, FAKE, None, dsa.DSA_E4M3, FAKE, 64, 128, keys, qs, FAKE, 4096, s) \
         == dsa.DSA_ERR_INVALID_ARG
+    # FP4 keys: E8M0 rows required and 16-byte aligned; q scales required; a contiguous key
+    # array needs whole 16-byte rows of scale bytes
+    f4 = dsa.dsa_keys(FAKE, None, None, 0, 0, 4096, None)
+    assert _status(dsa.dsa_indexer_logits, FAKE, FAKE, dsa.DSA_E4M3_MXFP4K, FAKE, 64, 128, f4, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    f4 = dsa.dsa_keys(FAKE, None, None, 0, 0, 4096, FAKE + 4)
+    assert _status(dsa.dsa_indexer_logits, FAKE, FAKE, dsa.DSA_E4M3_MXFP4K, FAKE, 64, 128, f4, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    f4 = dsa.dsa_keys(FAKE, None, None, 0, 0, 4098, FAKE)
+    assert _status(dsa.dsa_indexer_logits, FAKE, FAKE, dsa.DSA_E4M3_MXFP4K, FAKE, 64, 128, f4, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_UNSUPPORTED
+    f4 = dsa.dsa_keys(FAKE, None, None, 0, 0, 4096, FAKE)
+    assert _status(dsa.dsa_indexer_logits, FAKE, None, dsa.DSA_E4M3_MXFP4K, FAKE, 64, 128, f4, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_INVALID_ARG
+    assert _status(dsa.dsa_indexer_logits, FAKE, FAKE, 3, FAKE, 64, 128, f4, qs, FAKE, 4096, s) \
+        == dsa.DSA_ERR_INVALID_ARG
     # contiguous keys with more than one sequence
     assert _status(dsa.dsa_indexer_logits, FAKE, None, dsa.DSA_BF16, FAKE, 64, 128, keys, _qs(B=2), FAKE,
                    4096, s) == dsa.DSA_ERR_INVALID_ARG
