@@ -620,8 +620,9 @@ __device__ uint64_t engine_cut_approx(uint64_t* buf, uint32_t* cnt, int n, int k
 // the k-th key; the few keys in that bin are sorted by one warp to name the k-th key
 // exactly; only when the bin holds more than 64 keys (values packed closely, e.g. ties)
 // does the exact radix select over the (compacted) set decide.  `bins` holds 512 words of
-// shared scratch; buf must have room for every candidate (the writes may overwrite any
-// of the slots the candidates came from: they are all in keep[] already).
+// shared scratch and must be 8-byte aligned (its front is reused as a list of 64-bit
+// keys); buf must have room for every candidate (the writes may overwrite any of the
+// slots the candidates came from: they are all in keep[] already).
 template <int KPL>
 __device__ __forceinline__ void warp_sort_regs(uint64_t (&x)[KPL]);
 

@@ -104,7 +104,7 @@ struct EpiSmem {
   uint32_t cnt[4];
   uint64_t thr[4];
   EngineScratch esc;
-  uint32_t bins[kCutBins];
+  alignas(16) uint32_t bins[kCutBins];
 };
 
 // Two fp32 fused multiply-adds in one instruction (each lane rounded as fmaf).

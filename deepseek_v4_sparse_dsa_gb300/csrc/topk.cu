@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
   __shared__ TopkShared sh;
   __shared__ uint64_t s_floor[kMergeNT / 32];
   __shared__ uint32_t s_off[33], s_li[32];
-  __shared__ uint32_t mbins[kCutBins];
+  __shared__ __align__(16) uint32_t mbins[kCutBins];   // also read as 64-bit words
   constexpr int NT = kMergeNT;
   constexpr int kHalf = kMergeKeys / 2;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
