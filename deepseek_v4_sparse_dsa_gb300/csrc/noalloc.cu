@@ -17,8 +17,10 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of the array on the current device, looked up once per device.  (In
-// host code the array's name is only a host-side stand-in, never a device address.)
+// Device address of the array on the current device, looked up once per device and kept
+// for the life of the process.  (In host code the array's name is only a host-side
+// stand-in, never a device address.)  A device reset (cudaDeviceReset) reloads the
+// library's device image and may move the array: do not use this entry point across one.
 static cudaError_t scratch_on_current_device(void** out) {
   static std::mutex mu;
   static void* addr[64] = {};
@@ -43,12 +45,14 @@ extern "C" dsa_status dsa_indexer_logits_topk_noalloc(const void* q, const float
                                                       const float* weights, int H, int D, dsa_keys keys,
                                                       dsa_queries qs, int topk, int32_t* out_idx, float* out_val,
                                                       void* stream) {
+  // The regular call checks every argument before the workspace, so a bad argument is
+  // reported as such whatever the batch size; a batch whose scratch exceeds the array is
+  // handed no workspace and gets DSA_ERR_WORKSPACE from that check.
   const size_t need = dsa_workspace_bytes(DSA_OP_LOGITS_TOPK, dtype, qs, topk);
-  if (need > dsa::kNoAllocScratchBytes) return DSA_ERR_WORKSPACE;   // batch too large for the fixed array
   void* scratch = nullptr;
-  if (need > 0) {
+  if (need > 0 && need <= dsa::kNoAllocScratchBytes) {
     if (dsa::scratch_on_current_device(&scratch) != cudaSuccess) return DSA_ERR_CUDA;
   }
   return dsa_indexer_logits_topk(q, q_scale, dtype, weights, H, D, keys, qs, topk, out_idx, out_val, scratch,
-                                 dsa::kNoAllocScratchBytes, stream);
+                                 scratch != nullptr ? dsa::kNoAllocScratchBytes : 0, stream);
 }

@@ -110,7 +110,6 @@ __global__ void __launch_bounds__(kRowNT) topk_rows_kernel(const float* __restri
 
 constexpr int kMergeNT = 512;       // merge: threads per row
 constexpr int kMergeKeys = 24576;   // merge: candidates held in shared memory at once (two halves)
-constexpr int kMergeRegs = 24;      // merge fast path: candidates per thread held in registers
 
 // One CTA per (split group, query row): block m handles row m % nq of the (m / nq)-th
 // split group of the plan.  The row's lists (one per slice the group's tiles fall in)
@@ -159,58 +158,6 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
 #pragma unroll
   for (int w = 0; w < NT / 32; ++w) fl = max(fl, s_floor[w]);
   if (tid == 0) sh.thr = fl;
-  // Fast path: at most 32 lists holding at most NT * kMergeRegs keys in all: every key
-  // at or above the floor goes straight into registers (all loads in flight at once),
-  // one exact cut leaves the row's top-k in shared memory, a bitonic sort orders them.
-  if (nl <= 32) {
-    if (wid == 0) {
-      uint32_t cn = 0;
-      size_t li = 0;
-      if (lane < nl) {
-        li = list_of(lane);
-        cn = (uint32_t)min((uint64_t)lcap, __ldcg(meta + 2 * li));
-      }
-      uint32_t incl = cn;
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      s_off[lane + 1] = incl;
-      s_li[lane] = (uint32_t)li;
-      if (lane == 0) s_off[0] = 0;
-    }
-    group_sync<NT>();
-    const int total = (int)s_off[nl];
-    if (total <= NT * kMergeRegs) {
-      uint64_t keep[kMergeRegs];
-#pragma unroll
-      for (int u = 0; u < kMergeRegs; ++u) {
-        const int e = u * NT + tid;
-        keep[u] = 0ull;
-        if (e < total) {
-          int l = 0;                                // last list with s_off[l] <= e
-#pragma unroll
-          for (int step = 16; step > 0; step >>= 1)
-            if (l + step < nl && (int)s_off[l + step] <= e) l += step;
-          const uint64_t key = __ldcg(partial + (size_t)s_li[l] * lcap + (e - (int)s_off[l]));
-          keep[u] = key >= fl ? key : 0ull;
-        }
-      }
-      uint64_t* buf = mbuf;
-      engine_cut_exact_keep<NT, kMergeRegs>(buf, &sh.cnt, keep, topk, mbins, &sh.esc, tid);
-      const int m = min((int)sh.cnt, topk);
-      for (int e = m + tid; e < P; e += NT) buf[e] = 0ull;
-      group_sync<NT>();
-      engine_sort<NT>(buf, P, 1, P, tid);
-      for (int s2 = tid; s2 < topk; s2 += NT) {
-        const uint64_t key = buf[s2];
-        out_idx[t * topk + s2] = key ? index_of_key(key) : -1;
-        if (out_val) out_val[t * topk + s2] = key ? value_of_key(key) : -INFINITY;
-      }
-      return;
-    }
-    group_sync<NT>();                           // s_off / s_li are rewritten below
-  }
   // 2. collect the keys at or above the running threshold, cutting back when full;
   //    lists are taken 32 at a time, their keys as one flat range
   uint64_t* cur = mbuf;

@@ -247,8 +247,12 @@ dsa_status dsa_indexer_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot_m
  * GPU that loads the library holds until the process exits.
  *  - A batch whose dsa_workspace_bytes(DSA_OP_LOGITS_TOPK, ...) exceeds 16 MiB is
  *    rejected with DSA_ERR_WORKSPACE before anything is launched.
- *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
- *    make that first call before any stream capture.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *    and keeps it for the process; make that first call before any stream capture, and do
+ *    not use this call across a device reset (cudaDeviceReset may move the array).
+ *  - Which batches fit depends on the device's SM count (the plan keeps two partial top-k
+ *    lists per SM): on a 152-SM GB300 the tiny, Flash decode, Pro decode MTP and 16K
+ *    prefill batches fit; the FP8 chunked prefill (8192 rows, top-1024) does not.
  *  - All calls share the one array; the call itself rewrites every part it reads
  *    (its work plan and partial top-k lists), so stale contents never matter.
  *    Calls whose executions overlap on the GPU (other streams, other threads) race on

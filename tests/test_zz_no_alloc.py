@@ -31,6 +31,8 @@ def test_noalloc_matches_workspace_call_twice():
         parity.make_case(201, [30000, 9000, 200, 0], next_n=1, block_size=64, topk=512),
         # a different shape right after: two queries per group, larger k
         parity.make_case(202, [20000, 5000, 77], next_n=2, block_size=32, topk=1024),
+        # E4M3 queries and keys, four rows per group (prefill-shaped items)
+        parity.make_case(203, [2500], next_n=40, paged=False, dtype="e4m3", topk=256),
     ]
     for wl in cases:
         db = DeviceBatch.from_workload(wl)
@@ -56,3 +58,39 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
                                             0x100000, None)
     assert e.value.status == dsa.DSA_ERR_WORKSPACE
     assert dsa.dsa_launch_count() == before
+
+
+def test_noalloc_allocates_nothing():
+    # after a first call (which looks up the array's address), further calls change
+    # neither torch's allocations nor the device's free memory
+    wl = parity.make_case(211, [30000, 9000, 200], next_n=1, block_size=64, topk=512)
+    db = DeviceBatch.from_workload(wl)
+    idx = torch.empty((db.T, wl.topk), dtype=torch.int32, device="cuda")
+    val = torch.empty((db.T, wl.topk), dtype=torch.float32, device="cuda")
+
+    def call():
+        dsa.dsa_indexer_logits_topk_noalloc(db.q, db.q_scale, db.dtype, db.weights, 64, 128, db.keys(),
+                                            db.queries(), wl.topk, idx, val)
+
+    call()
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    assert dsa.dsa_device_error() == 0
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] == free0
+
+
+def test_noalloc_bad_argument_reported_before_the_size():
+    # a batch too large for the array, but with an unsupported head count: the argument
+    # error comes first, as for the regular call
+    lens = torch.full((256,), 1 << 20, dtype=torch.int32, device="cuda")
+    qs = dsa.make_queries(256, 4, lens, 1 << 20, True)
+    keys = dsa.dsa_keys(0x100000, None, 0x100000, 1 << 14, 64, 1 << 20)
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_indexer_logits_topk_noalloc(0x100000, None, dsa.DSA_BF16, 0x100000, 32, 128, keys, qs, 2048,
+                                            0x100000, None)
+    assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
