@@ -30,6 +30,14 @@
 //    (sel_pos < 0) -> zero rows.  The E2M1 value set {0, 0.5, 1, 1.5, 2, 3, 4, 6} is the
 //    OCP Microscaling v1.0 definition, looked up by table here (the GPU decodes
 //    arithmetically); the low nibble of byte i holds element 2i.
+//  * orc_sparse_attn -- the sparse-attention consumer of the selection (ROCm/ATOM issue
+//    #707, "CSA": "index-gather + online softmax + attn_sink bias").  Reading: for query
+//    row t and head h, over the selected positions j of row t (sel_pos >= 0), the key and
+//    value are the same dequantised cache row x_j (the latent of the paged mxfp4 cache
+//    the gather reads); s_j = scale * q[t,h,:] . x_j; the head's sink logit joins the
+//    softmax denominator only:  out[t,h,:] = sum_j e^(s_j - m) x_j / (sum_j e^(s_j - m)
+//    + e^(sink_h - m)), m = max(max_j s_j, sink_h).  A row with no selected position
+//    gives zeros.  The online (streaming) softmax is the GPU's way to compute this sum.
 //  * orc_e4m3 -- OCP E4M3 (bias 7, no infinities, S.1111.111 = NaN, subnormals
 //    m * 2^-9), the byte format README "DeepSeek V4 Flash on a single AMD MI300X"
 //    ("FP8 format") contrasts with AMD's FNUZ variant; orc_e4m3_encode rounds to it
@@ -469,6 +477,55 @@ int orc_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot, int64_t N, int 
         }
         kv_fp4[row * (D / 2) + (g * 32 + e) / 2] = static_cast<uint8_t>(lo | (hi << 4));
       }
+    }
+  });
+  return bad.load() ? -1 : 0;
+}
+
+// q [T, H, D] bf16 bits, sel [T, k], cache kv_fp4 [num_blocks, block_size, D/2] +
+// kv_scale [num_blocks, block_size, D/32], block_table [B, bt_stride], sink [H] ->
+// out [T, H, D] (float64).  Returns -1 if a selected position maps outside the cache.
+int orc_sparse_attn(const uint16_t* q, const int32_t* sel, int64_t T, int H, int D, int k, const uint8_t* kv_fp4,
+                    const uint8_t* kv_scale, int64_t num_blocks, int block_size, const int32_t* block_table,
+                    int64_t bt_stride, int next_n, const double* sink, double scale, double* out, int threads) {
+  std::atomic<int> bad{0};
+  parallel_for(T, threads, [&](int64_t t) {
+    const int64_t b = t / next_n;
+    // the row's selected keys / values, dequantised
+    std::vector<double> x;
+    int n = 0;
+    for (int s = 0; s < k; ++s) {
+      const int64_t pos = sel[t * k + s];
+      if (pos < 0) continue;
+      const int64_t page = pos / block_size;
+      const int64_t block = page < bt_stride ? block_table[b * bt_stride + page] : -1;
+      if (block < 0 || block >= num_blocks) {
+        bad.store(1);
+        continue;
+      }
+      const int64_t crow = block * block_size + pos % block_size;
+      for (int e = 0; e < D; ++e) x.push_back(mxfp4_element(kv_fp4 + crow * (D / 2), kv_scale + crow * (D / 32), e));
+      ++n;
+    }
+    for (int h = 0; h < H; ++h) {
+      double* o = out + (t * H + h) * D;
+      for (int e = 0; e < D; ++e) o[e] = 0.0;
+      if (n == 0) continue;
+      std::vector<double> sc(n);
+      double m = sink[h];
+      for (int j = 0; j < n; ++j) {
+        double dot = 0.0;
+        for (int e = 0; e < D; ++e) dot += bf16_value(q[(t * H + h) * D + e]) * x[(size_t)j * D + e];
+        sc[j] = scale * dot;
+        m = std::max(m, sc[j]);
+      }
+      double denom = std::exp(sink[h] - m);
+      for (int j = 0; j < n; ++j) {
+        const double p = std::exp(sc[j] - m);
+        denom += p;
+        for (int e = 0; e < D; ++e) o[e] += p * x[(size_t)j * D + e];
+      }
+      for (int e = 0; e < D; ++e) o[e] /= denom;
     }
   });
   return bad.load() ? -1 : 0;

@@ -108,6 +108,10 @@ class Oracle:
         L.orc_k_hadamard_mxfp4.restype = c_int
         L.orc_k_hadamard_mxfp4.argtypes = [POINTER(c_uint16), POINTER(c_int64), c_int64, c_int, POINTER(c_uint8),
                                            POINTER(c_uint8), c_int64, c_int]
+        L.orc_sparse_attn.restype = c_int
+        L.orc_sparse_attn.argtypes = [POINTER(c_uint16), POINTER(c_int32), c_int64, c_int, c_int, c_int,
+                                      POINTER(c_uint8), POINTER(c_uint8), c_int64, c_int, POINTER(c_int32), c_int64,
+                                      c_int, POINTER(c_double), c_double, POINTER(c_double), c_int]
         L.orc_mxfp4_gather.restype = c_int
         L.orc_mxfp4_gather.argtypes = [POINTER(c_uint8), POINTER(c_uint8), c_int64, c_int, c_int, POINTER(c_int32),
                                        c_int64, POINTER(c_int32), c_int64, c_int, c_int, POINTER(c_uint16), c_int]
@@ -252,6 +256,26 @@ class Oracle:
         assert rc == 0, "a slot lies outside the pool"
         return fp4, sc
 
+    # ------------------------------------------------------------------ consumer
+    def sparse_attn(self, q, sel_pos, kv_fp4, kv_scale, block_table, B: int, next_n: int, block_size: int,
+                    sink, scale: float):
+        """Sparse attention over the selected cache rows (key = value = the dequantised
+        row), with a per-head sink logit in the softmax denominator.  q [T, H, D] bf16
+        bits, sel_pos [T, k] -> out [T, H, D] float64 (zeros for a row with no selection)."""
+        qb = _c(q, np.uint16)
+        T, H, Dm = qb.shape
+        sel = _c(sel_pos, np.int32)
+        nib = _c(kv_fp4, np.uint8)
+        sc = _c(kv_scale, np.uint8)
+        tab = _c(block_table, np.int32)
+        snk = _c(sink, np.float64)
+        out = np.empty((T, H, Dm), dtype=np.float64)
+        rc = self.lib.orc_sparse_attn(_p(qb, c_uint16), _p(sel, c_int32), T, H, Dm, sel.shape[1], _p(nib, c_uint8),
+                                      _p(sc, c_uint8), nib.shape[0], int(block_size), _p(tab, c_int32), tab.shape[1],
+                                      int(next_n), _p(snk, c_double), float(scale), _p(out, c_double), threads())
+        assert rc == 0, "a selected position maps outside the block table or the cache"
+        return out
+
     def threads_used(self) -> int:
         return int(self.lib.orc_threads_used(threads()))
 
@@ -321,3 +345,7 @@ def k_hadamard_mxfp4(*a, **kw):
 
 def e2m1_encode(*a, **kw):
     return _get().e2m1_encode(*a, **kw)
+
+
+def sparse_attn(*a, **kw):
+    return _get().sparse_attn(*a, **kw)

@@ -555,10 +555,65 @@ def check_k_hadamard_mxfp4(orc, seed=12):
     assert np.all(err <= half_step * (1 + 1e-6) + np.where(v > 6, np.abs(g) - 6 * 2.0**e, 0))
 
 
+# --------------------------------------------------------------------------- consumer
+
+def _attn_cache(seed, nblk=4, bs=8):
+    r = np.random.default_rng(seed)
+    fp4 = r.integers(0, 256, (nblk, bs, 64)).astype(np.uint8)
+    sc = r.integers(124, 129, (nblk, bs, 4)).astype(np.uint8)
+    table = np.array([r.permutation(nblk)], np.int32)
+    return fp4, sc, table, bs
+
+
+def check_sparse_attn(orc, seed=13):
+    """Sparse attention with a sink: closed forms on special cases (a zero query gives the
+    plain mean of the selected rows when the sink is negligible; one selected row is
+    scaled by the logistic of its score against the sink; two rows mix by their softmax),
+    padded slots ignored, order of the selection irrelevant, an empty selection -> 0."""
+    fp4, sc, table, bs = _attn_cache(seed)
+    H, Dm = 3, 128
+    rows = orc.mxfp4_dequant(fp4.reshape(-1, 64), sc.reshape(-1, 4))       # pool rows, pinned above
+    def x_of(pos):
+        return rows[int(table[0, pos // bs]) * bs + pos % bs]
+    r = np.random.default_rng(seed)
+    q0 = np.zeros((1, H, Dm), np.uint16)
+    sel = np.array([[3, 17, -1, 9, 30]], np.int32)
+    sink_off = np.full(H, -1e300)
+    got = orc.sparse_attn(q0, sel, fp4, sc, table, 1, 1, bs, sink_off, 0.125)
+    want = np.mean([x_of(p) for p in (3, 17, 9, 30)], axis=0)
+    assert np.allclose(got[0], want[None, :], rtol=1e-12, atol=1e-12)
+    # one selected row, sink 0.5: out = x * sigmoid(s - 0.5), s = scale * q . x
+    qv = r.integers(-4, 5, (1, H, Dm)).astype(np.float64) / 16
+    qb = f64_to_bf16_exact(qv)
+    sel1 = np.array([[-1, 12, -1]], np.int32)
+    got = orc.sparse_attn(qb, sel1, fp4, sc, table, 1, 1, bs, np.full(H, 0.5), 0.0625)
+    x = x_of(12)
+    for h in range(H):
+        sc_ = 0.0625 * float(np.dot(qv[0, h], x))
+        assert np.allclose(got[0, h], x / (1.0 + np.exp(0.5 - sc_)), rtol=1e-10, atol=1e-12)
+    # two rows, negligible sink: softmax of the two scores
+    sel2 = np.array([[5, 22]], np.int32)
+    got = orc.sparse_attn(qb, sel2, fp4, sc, table, 1, 1, bs, sink_off, 0.0625)
+    x5, x22 = x_of(5), x_of(22)
+    for h in range(H):
+        a5, a22 = 0.0625 * float(np.dot(qv[0, h], x5)), 0.0625 * float(np.dot(qv[0, h], x22))
+        w5 = 1.0 / (1.0 + np.exp(a22 - a5))
+        assert np.allclose(got[0, h], w5 * x5 + (1 - w5) * x22, rtol=1e-10, atol=1e-12)
+    # order of the selection and padded slots do not matter; an empty selection gives 0
+    sel3 = np.array([[9, 30, 3, 17]], np.int32)
+    sel4 = np.array([[-1, 17, 3, -1, 30, 9, -1]], np.int32)
+    a = orc.sparse_attn(qb, sel3, fp4, sc, table, 1, 1, bs, np.full(H, 0.25), 0.0625)
+    b = orc.sparse_attn(qb, sel4, fp4, sc, table, 1, 1, bs, np.full(H, 0.25), 0.0625)
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-14)
+    e = orc.sparse_attn(qb, np.full((1, 4), -1, np.int32), fp4, sc, table, 1, 1, bs, np.zeros(H), 0.0625)
+    assert not e.any()
+
+
 ALL_CHECKS = [
     check_bf16_decode, check_e4m3_decode, check_bf16_rounding, check_e8m0, check_e2m1,
     check_mxfp4_hand_rows, check_mxfp4_gather_hand, check_gather_invariant,
     check_logits_hand, check_logits_plain_matmul, check_logits_special,
     check_logits_invariances, check_logits_e4m3, check_logits_mxfp4_keys, check_topk_hand,
     check_topk_bruteforce, check_e4m3_encode, check_e2m1_encode, check_q_rope_quant, check_k_hadamard_mxfp4,
+    check_sparse_attn,
 ]

@@ -57,6 +57,12 @@ MUTANTS = {
     "mx_shared_exp": ("sexp = (e2 - 1) - 2;", "sexp = (e2 - 1) - 1;"),
     "e2m1_ties_odd": ("if (dc < db || (dc == db && (c & 1) == 0)) best = c;", "if (dc <= db) best = c;"),
     "writer_nibble_order": ("static_cast<uint8_t>(lo | (hi << 4));", "static_cast<uint8_t>(hi | (lo << 4));"),
+    "attn_sink_dropped": ("double denom = std::exp(sink[h] - m);", "double denom = 0.0;"),
+    "attn_scale_dropped": ("sc[j] = scale * dot;", "sc[j] = dot;"),
+    "attn_padded_counted": ("      if (pos < 0) continue;\n      const int64_t page = pos / block_size;",
+                            "      const int64_t page = (pos < 0 ? 0 : pos) / block_size;"),
+    "attn_value_is_query": ("for (int e = 0; e < D; ++e) o[e] += p * x[(size_t)j * D + e];",
+                            "for (int e = 0; e < D; ++e) o[e] += p * bf16_value(q[(t * H + h) * D + e]);"),
     "mxfp4_key_scale_row": ("static_cast<const uint8_t*>(k_scale) + row * (D / 32);",
                             "static_cast<const uint8_t*>(k_scale) + 0 * row * (D / 32);"),
 }
