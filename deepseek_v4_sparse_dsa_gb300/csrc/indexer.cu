@@ -219,7 +219,7 @@ size_t smem_bytes_f4k(int nq, int stages, int conv, bool topk, int cap) {
   s += (size_t)nq * 64 * 128;                        // E4M3 Q staging
   s += (size_t)stages * 128 * 68;                    // FP4 stages
   s += 2048;                                         // decode table
-  s += (size_t)(2 * stages + 16 + 2 * conv + 1) * 8; // barriers
+  s += (size_t)((2 * stages + 16 + 2 * conv + 1 + 1) & ~1) * 8;   // barriers (an even count)
   s += sizeof(EpiSmem<4>) + 16;
   if (topk) s += (size_t)nq * cap * 8;
   return s;

@@ -255,7 +255,9 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
   constexpr uint32_t IDESC = kMmaFP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N);
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte alignment by pointer arithmetic on the shared array (not through an
+  // integer), so the compiler keeps every access below in the shared window
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = p.stages;
   const int CR = kF4K ? p.conv_slots : 0;
   // layout: Q tile (MMA operand) | key stages (TMA) or converted tiles [CR] (kF4K) |
@@ -268,9 +270,9 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(lut) + (kF4K ? 2048 : 0));
   // full[S] | empty[S] | tfull[4] | tempty[4] | qfull | qempty | ifull[2] | iempty[2] | mmadone | tmemfree
   // | kF4K: cfull[CR] | cfree[CR] | qready
-  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + 2 * S + 16 + (kF4K ? 2 * CR + 1 : 0));
-  uint64_t* ebuf = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(es) + sizeof(EpiSmem<NQ>) + 15) & ~uintptr_t(15));
+  const int NBARS = (2 * S + 16 + (kF4K ? 2 * CR + 1 : 0) + 1) & ~1;   // even: es stays 16-byte aligned
+  EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + NBARS);
+  uint64_t* ebuf = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(es) + (sizeof(EpiSmem<NQ>) + 15) / 16 * 16);
 
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
   const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 4);
