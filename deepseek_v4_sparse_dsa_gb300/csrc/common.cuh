@@ -909,22 +909,47 @@ __device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t c) {
   return s | ((k + 118u) << 7) | ((m << (7u - k)) & 0x7Fu);
 }
 
-// Eight elements (nibble bytes of w, low nibble first) times 2^(b-127) as bf16 pairs.
+// Scale bytes whose results leave the table's reach: 0 and 1 (subnormal results), 253
+// and 254 (overflowing ones).  (x + 3) mod 256 maps them to 3, 4, 0, 1 and 0xFF to 2.
+__device__ __forceinline__ bool e8m0_off_table(uint32_t b) {
+  const uint32_t v = (b + 3u) & 0xFFu;
+  return v < 5u && v != 2u;
+}
+
+// Any of the four scale bytes packed in `w` off the table.
+__device__ __forceinline__ bool e8m0_word_off_table(uint32_t w) {
+  bool r = false;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) r |= e8m0_off_table((w >> (8 * g)) & 0xFFu);
+  return r;
+}
+
+// Eight elements (nibble bytes of w, low nibble first) times 2^(b-127) as bf16 pairs,
+// for b in 2..252 or 0xFF.  2..252 take the table; 0xFF (scale 0) keeps only the signs
+// of the b = 2 entries, by a select.  Callers test e8m0_off_table once per row and send
+// the other bytes to decode8_exact: a branch inside this decode, even one never taken,
+// cost the FP4-key score more than half its time, and one taken for 0xFF (about one
+// group in a hundred in cache data, so a quarter of all warp-wide calls diverged) cost
+// it more than four times.
 __device__ __forceinline__ uint4 decode8(uint32_t w, uint32_t b, const uint2* lut) {
   uint32_t o[4];
-  if (b >= 2u && b <= 252u) {
-    const uint32_t adj = ((b - 2u) << 7) * 0x10001u;
+  const uint32_t adj = ((b - 2u) << 7) * 0x10001u;
+  const bool zero = b == 255u;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint2 e = lut[(w >> (8 * k)) & 0xFFu];
-      o[k] = e.x + (adj & e.y);
-    }
-  } else {
+  for (int k = 0; k < 4; ++k) {
+    const uint2 e = lut[(w >> (8 * k)) & 0xFFu];
+    o[k] = zero ? (e.x & 0x80008000u) : e.x + (adj & e.y);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Same, for any scale byte, nibble by nibble.
+__device__ __forceinline__ uint4 decode8_exact(uint32_t w, uint32_t b) {
+  uint32_t o[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t byte = (w >> (8 * k)) & 0xFFu;
-      o[k] = e2m1_bf16_general(byte & 0xFu, (int)b) | (e2m1_bf16_general(byte >> 4, (int)b) << 16);
-    }
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t byte = (w >> (8 * k)) & 0xFFu;
+    o[k] = e2m1_bf16_general(byte & 0xFu, (int)b) | (e2m1_bf16_general(byte >> 4, (int)b) << 16);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }

@@ -81,13 +81,23 @@ __global__ void __launch_bounds__(256) mxfp4_gather_kernel(const GatherArgs g) {
         }
       }
       if (h == 0) src_next = gather_source(g, r1, pos_next);
+      // the lane's scale bytes decide, once, between the table and the exact decode
+      bool exact = false;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int64_t row = r0 + h * 16 + 2 * k + sub;
-        if (row >= g.rows) continue;
-        const uint4 v = srow[k] >= 0 ? decode8(w[k], sb[k], lut) : make_uint4(0u, 0u, 0u, 0u);
-        st_stream(reinterpret_cast<uint4*>(g.out + row * 128) + part, v);
-      }
+      for (int k = 0; k < 8; ++k) exact |= e8m0_off_table(sb[k]);
+      auto emit = [&](auto decode) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int64_t row = r0 + h * 16 + 2 * k + sub;
+          if (row >= g.rows) continue;
+          const uint4 v = srow[k] >= 0 ? decode(w[k], sb[k]) : make_uint4(0u, 0u, 0u, 0u);
+          st_stream(reinterpret_cast<uint4*>(g.out + row * 128) + part, v);
+        }
+      };
+      if (!exact)
+        emit([&](uint32_t x, uint32_t b) { return decode8(x, b, lut); });
+      else
+        emit([](uint32_t x, uint32_t b) { return decode8_exact(x, b); });
     }
   }
 }

@@ -70,3 +70,15 @@ def test_fp4_keys_bad_block_id_masks_and_flags():
     lg = lg.cpu().numpy()
     assert np.isneginf(lg[0, 128:192]).all()
     assert np.isfinite(lg[0, :128]).all() and np.isfinite(lg[0, 192:500]).all()
+
+
+def test_fp4_keys_subnormal_scale_bytes():
+    # scale bytes 0 and 1 (subnormal bf16 keys) take the exact per-nibble decode, 0xFF the
+    # table's signed zeros; the other rows of the same tiles keep the table path
+    wl = parity.make_case(641, [900, 300], next_n=1, block_size=64, dtype="e4m3", topk=64, k_format="mxfp4")
+    r = np.random.default_rng(641)
+    sc = wl.k_scale.copy()
+    rows = r.choice(sc.shape[0], sc.shape[0] // 10, replace=False)
+    sc[rows, r.integers(0, 4, rows.size)] = r.choice(np.array([0, 1, 2, 255], np.uint8), rows.size)
+    wl.k_scale = sc
+    check(wl)
