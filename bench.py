@@ -313,6 +313,142 @@ def sub_record(name: str, dev, stream, peaks, seconds: float):
     return rec
 
 
+# ----------------------------------------------------------------------------- the NEXT rows
+
+def time_calls(fn, dev, stream, seconds: float):
+    """Mean device ms of fn() (CUDA events on the launching stream around each call) over
+    about `seconds` of calls after a warm-up; also the library's launches per call."""
+    import torch
+
+    from deepseek_v4_sparse_dsa_gb300 import dsa
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    steps = int(min(400, max(10, seconds * 1e3 / max(a.elapsed_time(b), 1e-3))))
+    for _ in range(max(3, steps // 4)):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    n0 = dsa.dsa_launch_count()
+    for e in ev:
+        e[0].record(stream)
+        fn()
+        e[1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = (dsa.dsa_launch_count() - n0) / steps
+    assert dsa.dsa_device_error(stream) == 0
+    return statistics.mean(e[0].elapsed_time(e[1]) for e in ev), steps, launches
+
+
+def hbm_record(name, desc, nbytes, ms, peaks, steps, launches, l2):
+    gbps = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": name, "desc": desc, "ms": ms, "steps": steps, "launches_per_call": launches,
+            "l2": l2, "roofline": {"bound": "hbm", "achieved": gbps, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": gbps / peaks["hbm_gbs"], "bytes_per_call": int(nbytes),
+                                   "peak_source": f"{peaks['source']}: hbm_gbs"}}
+
+
+def attn_work(ab):
+    """Algorithmic bytes and flops of one sparse-attention call: the selected cache rows
+    (68 B each, padded slots none), q, the fp32 output, the selection and the sinks;
+    2 x 64 x 128 flops per (row, head, selected slot) for the scores and as many for P.V."""
+    live = int((ab.sel >= 0).sum())
+    nbytes = live * 68 + ab.T * 64 * 128 * (2 + 4) + ab.sel.size * 4 + 64 * 4
+    flops = 4 * 64 * 128 * ab.T * ab.topk
+    return nbytes, flops
+
+
+def next_records(dev, stream, peaks, seconds: float):
+    """Sub-records of the rows beyond the hot path proper: the FP8-q x FP4-k fused score
+    on the Flash decode batch, the two producers, and the sparse attention on three shapes."""
+    import torch
+
+    from deepseek_v4_sparse_dsa_gb300 import dsa, synth
+    from deepseek_v4_sparse_dsa_gb300.device import DeviceBatch
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    recs = []
+
+    # FP8 queries x FP4 keys read from the paged mxfp4 cache (fused score + top-k)
+    wl = synth.make_flash_decode_fp4k()
+    db = DeviceBatch.from_workload(wl, dev)
+    ws = db.workspace(dsa.DSA_OP_LOGITS_TOPK, wl.topk)
+    idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
+    ms, steps, launches = time_calls(lambda: db.logits_topk(wl.topk, ws=ws, out_idx=idx, with_values=False,
+                                                            stream=stream), dev, stream, seconds)
+    L = int(wl.context_lens.sum())
+    nbytes = L * 68 + wl.T * 64 * (128 + 4 + 4) + wl.T * wl.topk * 8 + wl.B * 4
+    rec = hbm_record("flash_decode_fp4k", "Flash decode batch, E4M3 queries x keys read from the paged mxfp4 "
+                     "cache (68 B per key instead of 256), fused top-512", nbytes, ms, peaks, steps, launches,
+                     "inputs larger than L2")
+    rec["key_bytes_per_key"] = 68
+    rec["indexer_qtok_s"] = wl.T / (ms * 1e-3)
+    recs.append(rec)
+    del db, ws, idx
+
+    # indexer-Q RoPE + E4M3 quantisation: the FP8 chunked prefill's 8192 x 64 query rows
+    rng = synth.Rng(9)
+    T, R, maxpos = 8192, 64, 65536
+    q = d(synth.normal_bf16(rng, (T, 64, 128), "q").view(np.int16))
+    pos = d((57344 + np.arange(T)).astype(np.int32))
+    ang = (np.arange(maxpos)[:, None] * (10000.0 ** (-np.arange(R // 2) / (R // 2)))[None, :])
+    table = d(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32))
+    codes = torch.empty((T, 64, 128), dtype=torch.uint8, device=dev)
+    qs = torch.empty((T, 64), dtype=torch.float32, device=dev)
+    ms, steps, launches = time_calls(lambda: dsa.dsa_indexer_q_rope_quant(q, pos, table, maxpos, R, T, 64, 128,
+                                                                          codes, qs, stream), dev, stream, seconds)
+    nbytes = T * 64 * 128 * (2 + 1) + T * 64 * 4 + T * (4 + R * 4)
+    recs.append(hbm_record("q_rope_quant", "8192 tokens x 64 heads x 128 dims bf16 -> E4M3 + per-row scale, "
+                           "RoPE on the first 64 dims", nbytes, ms, peaks, steps, launches,
+                           "input 128 MiB, about the L2 size; not flushed"))
+    del q, pos, table, codes, qs
+
+    # indexer-key Hadamard + mxfp4 write into a paged pool: 1M keys
+    N = 1 << 20
+    k = d(synth.normal_bf16(rng, (N, 128), "k").view(np.int16))
+    slots = d(rng.permutation(N, "slots").astype(np.int64))
+    fp4 = torch.empty((N, 64), dtype=torch.uint8, device=dev)
+    sc = torch.empty((N, 4), dtype=torch.uint8, device=dev)
+    ms, steps, launches = time_calls(lambda: dsa.dsa_indexer_k_hadamard_mxfp4(k, slots, N, 128, fp4, sc, N, stream),
+                                     dev, stream, seconds)
+    nbytes = N * (256 + 8 + 68)
+    recs.append(hbm_record("k_hadamard_mxfp4", "1,048,576 keys x 128 bf16 -> Hadamard -> mxfp4 rows at permuted "
+                           "pool slots", nbytes, ms, peaks, steps, launches, "inputs larger than L2"))
+    del k, slots, fp4, sc
+
+    # sparse attention over the selection, straight from the paged mxfp4 cache
+    for name in ("flash_decode", "pro_mtp", "fp8_chunked"):
+        ab = synth.make_attn_config(name)
+        aq, asel = d(ab.q.view(np.int16)), d(ab.sel)
+        afp4, asc, atab, asink = d(ab.kv_fp4), d(ab.kv_scale), d(ab.table), d(ab.sink)
+        out = torch.empty((ab.T, 64, 128), dtype=torch.float32, device=dev)
+        f = lambda: dsa.dsa_sparse_attn_mxfp4(aq, ab.T, 64, 128, asel, ab.topk, afp4, asc, afp4.shape[0],
+                                              ab.block_size, atab, atab.shape[1], ab.next_n, asink, ab.scale,
+                                              out, stream)
+        ms, steps, launches = time_calls(f, dev, stream, seconds)
+        nbytes, flops = attn_work(ab)
+        gbps, tflops = nbytes / (ms * 1e-3) / 1e9, flops / (ms * 1e-3) / 1e12
+        tpeak = peaks["bf16_tflops"]
+        bound = "hbm" if nbytes / peaks["hbm_gbs"] >= flops / (tpeak * 1e3) else "tensor"
+        recs.append({"workload": "sparse_attn_" + name,
+                     "desc": f"{ab.T} query rows x 64 heads x 128 dims over top-{ab.topk} rows of the paged "
+                             "mxfp4 cache, sink logits, fp32 out", "ms": ms, "steps": steps,
+                     "launches_per_call": launches, "qtok_s": ab.T / (ms * 1e-3),
+                     "roofline": {"bound": bound, "achieved": gbps if bound == "hbm" else tflops,
+                                  "peak": peaks["hbm_gbs"] if bound == "hbm" else tpeak,
+                                  "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                                  "frac": gbps / peaks["hbm_gbs"] if bound == "hbm" else tflops / tpeak,
+                                  "hbm_frac": gbps / peaks["hbm_gbs"], "tensor_frac": tflops / tpeak,
+                                  "bytes_per_call": int(nbytes), "flops_per_call": int(flops),
+                                  "peak_source": f"{peaks['source']}: hbm_gbs / bf16_tflops (burst)"}})
+        del aq, asel, afp4, asc, atab, asink, out
+    torch.cuda.empty_cache()
+    return recs
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -385,13 +521,14 @@ def run_ours(args, rank, world):
         torch.distributed.all_reduce(local, op=torch.distributed.ReduceOp.MAX)
     ms_step, e2e_ms = float(local[0]), float(local[1])
 
-    subs = []
+    subs, nxt = [], []
     if rank == 0 and world == 1 and not args.batch and args.sub:
         del run, db
         torch.cuda.empty_cache()
         for name in WORKLOADS:
             if name != args.workload:
                 subs.append(sub_record(name, dev, stream, peaks, args.sub_seconds))
+        nxt = next_records(dev, stream, peaks, args.sub_seconds)
     clocks = sampler.stop()
     if rank != 0:
         return None
@@ -419,6 +556,8 @@ def run_ours(args, rank, world):
     }
     if subs:
         out["configs"] = subs
+    if nxt:
+        out["next"] = nxt
     return out, wl
 
 

@@ -18,7 +18,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libdsa_gb300.so")
 
 SOURCES = ["indexer_bf16_topk.cu", "indexer_fp8_topk.cu", "indexer_bf16_logits.cu", "indexer_fp8_logits.cu",
-           "api.cu", "gather.cu", "indexer.cu", "topk.cu", "noalloc.cu", "producer.cu"]
+           "api.cu", "gather.cu", "indexer.cu", "topk.cu", "noalloc.cu", "producer.cu",
+           "sparse_attn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          f"-I{os.path.join(ROOT, 'include')}"]

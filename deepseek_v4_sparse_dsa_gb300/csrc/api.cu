@@ -1,5 +1,6 @@
 // C ABI of include/dsa.h: argument validation, launch planning and dispatch.
 // Every check that can be made on the host is made here, before anything is launched.
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -175,6 +176,25 @@ dsa_status dsa_indexer_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot_m
   if (!aligned(k, 8) || !aligned(kv_fp4, 2) || !aligned(kv_scale, 4)) return DSA_ERR_INVALID_ARG;
   return cuda_status(launch_k_hadamard_mxfp4(k, slot_mapping, N, kv_fp4, kv_scale, num_rows, device_sm_count(),
                                              static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status dsa_sparse_attn_mxfp4(const uint16_t* q, int64_t T, int H, int D, const int32_t* sel_pos, int topk,
+                                 const uint8_t* kv_fp4, const uint8_t* kv_scale, int64_t num_blocks, int block_size,
+                                 const int32_t* block_table, int64_t bt_stride, int next_n, const float* sink,
+                                 float softmax_scale, float* out, void* stream) {
+  if (H != 64 || D != 128) return DSA_ERR_UNSUPPORTED;
+  if (T < 0 || topk < 0 || num_blocks < 0 || block_size < 1 || T > 0x7FFFFFFF) return DSA_ERR_INVALID_ARG;
+  if (topk > sparse_attn_max_topk() || num_blocks * (int64_t)block_size > 0x7FFFFFFF) return DSA_ERR_UNSUPPORTED;
+  if (T == 0) return DSA_OK;
+  if (next_n < 1 || bt_stride < 1 || !std::isfinite(softmax_scale)) return DSA_ERR_INVALID_ARG;
+  if (q == nullptr || kv_fp4 == nullptr || kv_scale == nullptr || block_table == nullptr || sink == nullptr ||
+      out == nullptr || (topk > 0 && sel_pos == nullptr))
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_fp4, 16) || !aligned(kv_scale, 4) || !aligned(sink, 4) || !aligned(out, 4))
+    return DSA_ERR_INVALID_ARG;
+  return cuda_status(launch_sparse_attn(q, T, sel_pos, topk, kv_fp4, kv_scale, num_blocks, block_size, block_table,
+                                        bt_stride, next_n, sink, softmax_scale, out,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 size_t dsa_workspace_bytes(dsa_op op, dsa_dtype dtype, dsa_queries qs, int topk) {

@@ -91,6 +91,16 @@ cudaError_t launch_q_rope_quant(const uint16_t* q, const int32_t* positions, con
 cudaError_t launch_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot, int64_t n, uint8_t* fp4, uint8_t* scale,
                                     int64_t num_rows, int num_sms, cudaStream_t stream);
 
+// ------------------------------------------------------------------ sparse attention (sparse_attn.cu)
+// q [T, 64, 128] bf16 (16-byte aligned), sel [T, k], the paged mxfp4 cache, sink [64],
+// out [T, 64, 128] fp32.  One CTA per query row.
+cudaError_t launch_sparse_attn(const uint16_t* q, int64_t T, const int32_t* sel, int k, const uint8_t* fp4,
+                               const uint8_t* scale, int64_t num_blocks, int bs, const int32_t* table,
+                               int64_t bt_stride, int next_n, const float* sink, float softmax_scale, float* out,
+                               cudaStream_t stream);
+size_t sparse_attn_smem_bytes(int k);   // dynamic shared memory for a top-k of k slots
+int sparse_attn_max_topk();
+
 // ------------------------------------------------------------------ per-TU device words
 #define DSA_DECLARE_TU_ERROR_ACCESSORS(name)                                        \
   cudaError_t tu_##name##_read_clear_error(unsigned int* out);                      \
@@ -115,6 +125,7 @@ DSA_DECLARE_TU_ERROR_ACCESSORS(indexer_fp8_topk)
 DSA_DECLARE_TU_ERROR_ACCESSORS(indexer_fp8_logits)
 DSA_DECLARE_TU_ERROR_ACCESSORS(topk)
 DSA_DECLARE_TU_ERROR_ACCESSORS(producer)
+DSA_DECLARE_TU_ERROR_ACCESSORS(attn)
 
 // Every translation unit's accessors, for dsa_device_error / dsa_set_wait_limit_ns.
 struct TuWords {
@@ -125,7 +136,8 @@ struct TuWords {
 inline const TuWords* all_tu_words(int* n) {
   static const TuWords w[] = {DSA_TU_WORDS(gather), DSA_TU_WORDS(indexer), DSA_TU_WORDS(indexer_bf16_topk),
                               DSA_TU_WORDS(indexer_bf16_logits), DSA_TU_WORDS(indexer_fp8_topk),
-                              DSA_TU_WORDS(indexer_fp8_logits), DSA_TU_WORDS(topk), DSA_TU_WORDS(producer)};
+                              DSA_TU_WORDS(indexer_fp8_logits), DSA_TU_WORDS(topk), DSA_TU_WORDS(producer),
+                              DSA_TU_WORDS(attn)};
   *n = (int)(sizeof(w) / sizeof(w[0]));
   return w;
 }

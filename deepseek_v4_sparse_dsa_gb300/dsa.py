@@ -11,7 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import c_int, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+from ctypes import c_float, c_int, c_int32, c_int64, c_size_t, c_uint64, c_void_p
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdsa_gb300.so")
@@ -79,6 +79,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                              c_void_p, c_void_p, c_void_p]),
         "dsa_indexer_k_hadamard_mxfp4": (c_int, [c_void_p, c_void_p, c_int64, c_int, c_void_p, c_void_p, c_int64,
                                                  c_void_p]),
+        "dsa_sparse_attn_mxfp4": (c_int, [c_void_p, c_int64, c_int, c_int, c_void_p, c_int, c_void_p, c_void_p,
+                                          c_int64, c_int, c_void_p, c_int64, c_int, c_void_p, c_float, c_void_p,
+                                          c_void_p]),
         "dsa_workspace_bytes": (c_size_t, [c_int, c_int, dsa_queries, c_int]),
         "dsa_status_string": (ctypes.c_char_p, [c_int]),
         "dsa_device_error": (c_int, [c_void_p]),
@@ -168,6 +171,15 @@ def dsa_indexer_q_rope_quant(q, positions, cos_sin, max_pos, rope_dim, T, H, D, 
     _check(load().dsa_indexer_q_rope_quant(_ptr(q), _ptr(positions), _ptr(cos_sin), int(max_pos), int(rope_dim),
                                            int(T), int(H), int(D), _ptr(q_fp8), _ptr(q_scale), _stream(stream)),
            "dsa_indexer_q_rope_quant")
+
+
+def dsa_sparse_attn_mxfp4(q, T, H, D, sel_pos, topk, kv_fp4, kv_scale, num_blocks, block_size, block_table,
+                          bt_stride, next_n, sink, softmax_scale, out, stream=None):
+    _check(load().dsa_sparse_attn_mxfp4(_ptr(q), int(T), int(H), int(D), _ptr(sel_pos), int(topk), _ptr(kv_fp4),
+                                        _ptr(kv_scale), int(num_blocks), int(block_size), _ptr(block_table),
+                                        int(bt_stride), int(next_n), _ptr(sink), float(softmax_scale), _ptr(out),
+                                        _stream(stream)),
+           "dsa_sparse_attn_mxfp4")
 
 
 def dsa_indexer_k_hadamard_mxfp4(k, slot_mapping, N, D, kv_fp4, kv_scale, num_rows, stream=None):

@@ -242,12 +242,14 @@ def _page_pool(rng: Rng, context_lens: np.ndarray, block_size: int, stream: str)
     return table, total
 
 
-def _mxfp4_pool(rng: Rng, nblk: int, block_size: int, stream: str, ff_frac: float = 0.01):
-    """Random nibble bytes; E8M0 scales uniform on 120..134 with ~1% set to 0xFF."""
+def _mxfp4_pool(rng: Rng, nblk: int, block_size: int, stream: str, ff_frac: float = 0.01, sc_lo: int = 120,
+                sc_span: int = 14):
+    """Random nibble bytes; E8M0 scales uniform on sc_lo .. sc_lo + sc_span - 1 (120..133
+    by default) with ~1% set to 0xFF."""
     fp4 = np.empty((nblk, block_size, D // 2), dtype=np.uint8)
     rng.bytes_into(fp4, stream + "/nib")
     n_sc = nblk * block_size * (D // 32)
-    sc = (120 + rng.integers(0, 14, n_sc, stream + "/sc")).astype(np.uint8)
+    sc = (sc_lo + rng.integers(0, sc_span, n_sc, stream + "/sc")).astype(np.uint8)
     ff = rng.uniform(n_sc, stream + "/ff") < ff_frac
     sc[ff] = 0xFF
     return fp4, sc.reshape(nblk, block_size, D // 32)
@@ -368,6 +370,81 @@ def random_sel_pos(wl: Workload, seed: int, stream: str = "sel") -> np.ndarray:
         pick = np.argsort(keys, kind="stable")[: min(n, wl.topk)]
         out[t, : pick.size] = pick
     return out
+
+
+@dataclasses.dataclass
+class AttnBatch:
+    """Sparse-attention inputs: query rows, their selection and the paged mxfp4 cache.
+
+    q        [T, 64, 128] uint16 (bf16 bits); row t belongs to sequence t // next_n
+    sel      [T, topk] int32 positions (-1: padded slot)
+    kv_fp4   [nblk, block_size, 64] uint8, kv_scale [nblk, block_size, 4] uint8
+    table    [B, max_blocks] int32
+    sink     [64] float32 per-head sink logits; scale = the softmax scale
+    """
+
+    name: str
+    B: int
+    next_n: int
+    context_lens: np.ndarray
+    topk: int
+    block_size: int
+    q: np.ndarray
+    sel: np.ndarray
+    kv_fp4: np.ndarray
+    kv_scale: np.ndarray
+    table: np.ndarray
+    sink: np.ndarray
+    scale: float
+
+    @property
+    def T(self) -> int:
+        return self.B * self.next_n
+
+
+def make_attn(seed: int, lens, next_n: int, topk: int, block_size: int = 64, pad_frac: float = 0.02,
+              distinct: bool = True, name: str = "attn", sc_lo: int = 124, sc_span: int = 5,
+              sink_lo: float = -2.0, sink_hi: float = 2.0, scale: float = 128 ** -0.5) -> AttnBatch:
+    """A sparse-attention batch: len(lens) sequences with next_n causal query rows each,
+    topk selected positions per row (distinct when `distinct`, else drawn uniformly with
+    repeats), a seeded fraction padded; a cache whose scale bytes span sc_lo ..
+    sc_lo + sc_span - 1 (124..128: elements within +-12, like a Hadamard-rotated key
+    quantised per 32 elements) with ~1% 0xFF groups; sinks uniform on [sink_lo, sink_hi)."""
+    rng = Rng(seed)
+    lens = np.asarray(lens, dtype=np.int32)
+    B = lens.size
+    table, nblk = _page_pool(rng, lens, block_size, "attn_table")
+    fp4, sc = _mxfp4_pool(rng, nblk, block_size, "attn_cache", sc_lo=sc_lo, sc_span=sc_span)
+    T = B * next_n
+    q = normal_bf16(rng, (T, H, D), "attn_q")
+    vis = np.repeat(lens.astype(np.int64), next_n) - next_n + np.tile(np.arange(next_n), B) + 1
+    sel = np.full((T, topk), -1, dtype=np.int32)
+    if distinct:
+        for t in range(T):
+            n = int(vis[t])
+            pick = np.argsort(rng.u64(n, f"attn_sel/{t}"), kind="stable")[: min(n, topk)]
+            sel[t, : pick.size] = pick
+    else:
+        u = rng.uniform(T * topk, "attn_sel").reshape(T, topk)
+        sel[:] = np.minimum((u * vis[:, None]).astype(np.int64), vis[:, None] - 1)
+    sel = pad_sel_pos(sel, pad_frac, seed, "attn_pad")
+    sink = (sink_lo + (sink_hi - sink_lo) * rng.uniform(H, "attn_sink")).astype(np.float32)
+    return AttnBatch(name, B, next_n, lens, topk, block_size, q, sel, fp4, sc, table, sink, float(scale))
+
+
+def make_attn_config(name: str, seed: int = 7) -> AttnBatch:
+    """The sparse-attention batch of a named shape: Flash decode (64 sequences of 4K-64K
+    keys, top-512), Pro decode MTP (32 sequences of 32K-128K keys, two query rows each,
+    top-1024), FP8 chunked prefill (8192 causal rows at the end of a 64K-key sequence,
+    top-1024); selections drawn uniformly (with repeats), 2% padded."""
+    rng = Rng(seed)
+    if name == "flash_decode":
+        return make_attn(seed, rng.integers(4096, 65536, 64, "lens"), 1, 512, distinct=False, name=name)
+    if name == "pro_mtp":
+        return make_attn(seed, rng.integers(32768, 131072, 32, "lens"), 2, 1024, distinct=False, name=name)
+    if name == "fp8_chunked":
+        return make_attn(seed, [65536], 8192, 1024, distinct=False, name=name)
+    raise KeyError(name)
 
 
 CONFIGS = {

@@ -237,6 +237,42 @@ dsa_status dsa_indexer_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot_m
                                         uint8_t* kv_fp4, uint8_t* kv_scale, int64_t num_rows, void* stream);
 
 /*
+ * dsa_sparse_attn_mxfp4 -- the sparse-attention consumer of the selection, reading the
+ * paged mxfp4 cache directly (ROCm/ATOM issue #707, "CSA": "index-gather + online
+ * softmax + attn_sink bias").  This library's reading: for query row t and head h, over
+ * the selected positions of row t (sel_pos >= 0), the key and the value are the same
+ * dequantised cache row x (the row mxfp4_paged_gather produces); s = softmax_scale *
+ * q[t,h,:] . x; the head's sink logit joins the softmax denominator only:
+ *   out[t,h,:] = sum_j e^(s_j - m) x_j / (sum_j e^(s_j - m) + e^(sink[h] - m)),
+ * m any shift (the result does not depend on it).  A row with no selected position
+ * gives zeros.
+ *  q        [T, H, D] bf16 bit patterns, 16-byte aligned.  H must be 64 and D 128
+ *           (DSA_ERR_UNSUPPORTED otherwise).
+ *  sel_pos  [T, topk] int32 positions in row t's sequence b = t / next_n (< 0: padded);
+ *           may be NULL when topk == 0.
+ *  kv_fp4 [num_blocks, block_size, D/2] (16-byte aligned), kv_scale [num_blocks,
+ *           block_size, D/32] (4-byte aligned), block_table [ceil(T / next_n), bt_stride]:
+ *           the cache and table exactly as mxfp4_paged_gather reads them.
+ *  sink     [H] fp32 logits (-inf: no sink).  softmax_scale finite.
+ *  out      [T, H, D] fp32, 4-byte aligned; every element is written.
+ * Arithmetic: the scores on the tensor cores from bf16 q and the exactly decoded bf16
+ * rows with fp32 accumulation; the softmax in base 2; each weight rounded once to bf16
+ * and the same weights summed for the denominator.  So the result is a weighted mean of
+ * the selected rows whose weights are off by the bf16 rounding (2^-9 relative) and by
+ * the fp32 score error: |out - exact| <= (2^-8 + 2 max_j |ds_j|) max_j |x_j[e]| to first
+ * order, ds_j the fp32 error of score j.  Scores must be finite: a row whose scale
+ * overflows bf16 (scale bytes 253, 254 with large codes) gives undefined output.
+ * A block id outside [0, num_blocks) or a page at or past bt_stride drops that position
+ * (as if padded) and sets DSA_DEVERR_INDEX.  topk above 16384 or a cache of 2^31 rows or
+ * more (num_blocks * block_size) is DSA_ERR_UNSUPPORTED.  One CTA of 160 threads per
+ * query row; two share an SM up to topk 2048.
+ */
+dsa_status dsa_sparse_attn_mxfp4(const uint16_t* q, int64_t T, int H, int D, const int32_t* sel_pos, int topk,
+                                 const uint8_t* kv_fp4, const uint8_t* kv_scale, int64_t num_blocks,
+                                 int block_size, const int32_t* block_table, int64_t bt_stride, int next_n,
+                                 const float* sink, float softmax_scale, float* out, void* stream);
+
+/*
  * dsa_indexer_logits_topk_noalloc -- dsa_indexer_logits_topk for callers that cannot
  * allocate device memory: a process whose device memory is all reserved at start-up
  * and handed out by its own pool, or a latency-critical loop that cannot afford

@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["dsa_indexer_logits", "dsa_indexer_topk", "dsa_indexer_logits_topk", "mxfp4_paged_gather",
-              "dsa_workspace_bytes", "dsa_status_string", "dsa_device_error"]:
+              "dsa_workspace_bytes", "dsa_status_string", "dsa_device_error", "dsa_sparse_attn_mxfp4"]:
         assert n in names
 
 
@@ -163,6 +163,19 @@ def test_host_side_rejections_launch_nothing(lib):
     assert _status(dsa.dsa_indexer_k_hadamard_mxfp4, FAKE, FAKE, 10, 128, FAKE, FAKE + 2, 100, s) \
         == dsa.DSA_ERR_INVALID_ARG
     assert _status(dsa.dsa_indexer_k_hadamard_mxfp4, None, None, 0, 128, None, None, 0, s) == dsa.DSA_OK
+    # sparse attention: heads / dim, misaligned q or cache, null selection, bad scale, empty batch
+    def attn(q=FAKE, T=4, H=64, D=128, sel=FAKE, topk=512, fp4=FAKE, sc=FAKE, bs=64, tab=FAKE, stride=8, nn=1,
+             sink=FAKE, scale=0.088, out=FAKE):
+        return _status(dsa.dsa_sparse_attn_mxfp4, q, T, H, D, sel, topk, fp4, sc, 100, bs, tab, stride, nn, sink,
+                       scale, out, s)
+    assert attn(H=128) == dsa.DSA_ERR_UNSUPPORTED and attn(D=64) == dsa.DSA_ERR_UNSUPPORTED
+    assert attn(topk=16385) == dsa.DSA_ERR_UNSUPPORTED and attn(bs=1 << 25) == dsa.DSA_ERR_UNSUPPORTED
+    assert attn(q=FAKE + 8) == dsa.DSA_ERR_INVALID_ARG and attn(fp4=FAKE + 4) == dsa.DSA_ERR_INVALID_ARG
+    assert attn(sel=None) == dsa.DSA_ERR_INVALID_ARG and attn(sink=None) == dsa.DSA_ERR_INVALID_ARG
+    assert attn(scale=float("nan")) == dsa.DSA_ERR_INVALID_ARG and attn(scale=float("inf")) == dsa.DSA_ERR_INVALID_ARG
+    assert attn(bs=0) == dsa.DSA_ERR_INVALID_ARG and attn(T=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert attn(nn=0) == dsa.DSA_ERR_INVALID_ARG and attn(topk=-1) == dsa.DSA_ERR_INVALID_ARG
+    assert attn(q=None, T=0, sel=None, fp4=None, sc=None, tab=None, sink=None, out=None) == dsa.DSA_OK
     # empty problems are valid no-ops
     assert _status(dsa.mxfp4_paged_gather, None, None, 0, 64, 128, None, 0, None, 0, 1, 512, None, s) == dsa.DSA_OK
     assert dsa.dsa_launch_count() == before
