@@ -7,9 +7,12 @@ long-context chunked prefill, the largest configuration that fits one GPU (8192 
 queries at positions 57344..65535 over 65536 E4M3 keys, causal, top-1024, then the
 gather of all 8,388,608 selected rows).  The same JSON line carries one sub-record per
 other configuration (tiny, Flash decode, Pro decode MTP, 16K prefill) with its fused
-and gather times and its own roofline fraction, each from its own timed loop.
+and gather times and its own roofline fraction, each from its own timed loop, and under
+"next" the rows beyond the hot path proper (FP8-q x FP4-k score, the query and key
+producers, the sparse attention over the selection), each with its own roofline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py --next NAME      # one of the "next" rows alone (a profiler target)
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a bounded
 sample of the same workload.  Under torchrun each rank runs its own batch (weak
@@ -362,91 +365,113 @@ def attn_work(ab):
     return nbytes, flops
 
 
-def next_records(dev, stream, peaks, seconds: float):
-    """Sub-records of the rows beyond the hot path proper: the FP8-q x FP4-k fused score
-    on the Flash decode batch, the two producers, and the sparse attention on three shapes."""
+NEXT_NAMES = ("flash_decode_fp4k", "q_rope_quant", "k_hadamard_mxfp4", "sparse_attn_flash_decode",
+              "sparse_attn_pro_mtp", "sparse_attn_fp8_chunked")
+
+
+def next_record(name: str, dev, stream, peaks, seconds: float):
+    """One sub-record of the rows beyond the hot path proper: the FP8-q x FP4-k fused score
+    on the Flash decode batch, the two producers, or the sparse attention on one shape."""
     import torch
 
     from deepseek_v4_sparse_dsa_gb300 import dsa, synth
     from deepseek_v4_sparse_dsa_gb300.device import DeviceBatch
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    recs = []
 
-    # FP8 queries x FP4 keys read from the paged mxfp4 cache (fused score + top-k)
-    wl = synth.make_flash_decode_fp4k()
-    db = DeviceBatch.from_workload(wl, dev)
-    ws = db.workspace(dsa.DSA_OP_LOGITS_TOPK, wl.topk)
-    idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
-    ms, steps, launches = time_calls(lambda: db.logits_topk(wl.topk, ws=ws, out_idx=idx, with_values=False,
-                                                            stream=stream), dev, stream, seconds)
-    L = int(wl.context_lens.sum())
-    nbytes = L * 68 + wl.T * 64 * (128 + 4 + 4) + wl.T * wl.topk * 8 + wl.B * 4
-    rec = hbm_record("flash_decode_fp4k", "Flash decode batch, E4M3 queries x keys read from the paged mxfp4 "
-                     "cache (68 B per key instead of 256), fused top-512", nbytes, ms, peaks, steps, launches,
-                     "inputs larger than L2")
-    rec["key_bytes_per_key"] = 68
-    rec["indexer_qtok_s"] = wl.T / (ms * 1e-3)
-    recs.append(rec)
-    del db, ws, idx
+    if name == "flash_decode_fp4k":
+        # FP8 queries x FP4 keys read from the paged mxfp4 cache (fused score + top-k)
+        wl = synth.make_flash_decode_fp4k()
+        db = DeviceBatch.from_workload(wl, dev)
+        ws = db.workspace(dsa.DSA_OP_LOGITS_TOPK, wl.topk)
+        idx = torch.empty((wl.T, wl.topk), dtype=torch.int32, device=dev)
+        ms, steps, launches = time_calls(lambda: db.logits_topk(wl.topk, ws=ws, out_idx=idx, with_values=False,
+                                                                stream=stream), dev, stream, seconds)
+        L = int(wl.context_lens.sum())
+        nbytes = L * 68 + wl.T * 64 * (128 + 4 + 4) + wl.T * wl.topk * 8 + wl.B * 4
+        rec = hbm_record(name, "Flash decode batch, E4M3 queries x keys read from the paged mxfp4 cache "
+                         "(68 B per key instead of 256), fused top-512", nbytes, ms, peaks, steps, launches,
+                         "inputs larger than L2")
+        rec["key_bytes_per_key"] = 68
+        rec["indexer_qtok_s"] = wl.T / (ms * 1e-3)
+        return rec
 
-    # indexer-Q RoPE + E4M3 quantisation: the FP8 chunked prefill's 8192 x 64 query rows
     rng = synth.Rng(9)
-    T, R, maxpos = 8192, 64, 65536
-    q = d(synth.normal_bf16(rng, (T, 64, 128), "q").view(np.int16))
-    pos = d((57344 + np.arange(T)).astype(np.int32))
-    ang = (np.arange(maxpos)[:, None] * (10000.0 ** (-np.arange(R // 2) / (R // 2)))[None, :])
-    table = d(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32))
-    codes = torch.empty((T, 64, 128), dtype=torch.uint8, device=dev)
-    qs = torch.empty((T, 64), dtype=torch.float32, device=dev)
-    ms, steps, launches = time_calls(lambda: dsa.dsa_indexer_q_rope_quant(q, pos, table, maxpos, R, T, 64, 128,
-                                                                          codes, qs, stream), dev, stream, seconds)
-    nbytes = T * 64 * 128 * (2 + 1) + T * 64 * 4 + T * (4 + R * 4)
-    recs.append(hbm_record("q_rope_quant", "8192 tokens x 64 heads x 128 dims bf16 -> E4M3 + per-row scale, "
-                           "RoPE on the first 64 dims", nbytes, ms, peaks, steps, launches,
-                           "input 128 MiB, about the L2 size; not flushed"))
-    del q, pos, table, codes, qs
+    if name == "q_rope_quant":
+        # indexer-Q RoPE + E4M3 quantisation: the FP8 chunked prefill's 8192 x 64 query rows
+        T, R, maxpos = 8192, 64, 65536
+        q = d(synth.normal_bf16(rng, (T, 64, 128), "q").view(np.int16))
+        pos = d((57344 + np.arange(T)).astype(np.int32))
+        ang = (np.arange(maxpos)[:, None] * (10000.0 ** (-np.arange(R // 2) / (R // 2)))[None, :])
+        table = d(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32))
+        codes = torch.empty((T, 64, 128), dtype=torch.uint8, device=dev)
+        qs = torch.empty((T, 64), dtype=torch.float32, device=dev)
+        ms, steps, launches = time_calls(lambda: dsa.dsa_indexer_q_rope_quant(q, pos, table, maxpos, R, T, 64, 128,
+                                                                              codes, qs, stream),
+                                         dev, stream, seconds)
+        nbytes = T * 64 * 128 * (2 + 1) + T * 64 * 4 + T * (4 + R * 4)
+        return hbm_record(name, "8192 tokens x 64 heads x 128 dims bf16 -> E4M3 + per-row scale, RoPE on the "
+                          "first 64 dims", nbytes, ms, peaks, steps, launches,
+                          "input 128 MiB, about the L2 size; not flushed")
 
-    # indexer-key Hadamard + mxfp4 write into a paged pool: 1M keys
-    N = 1 << 20
-    k = d(synth.normal_bf16(rng, (N, 128), "k").view(np.int16))
-    slots = d(rng.permutation(N, "slots").astype(np.int64))
-    fp4 = torch.empty((N, 64), dtype=torch.uint8, device=dev)
-    sc = torch.empty((N, 4), dtype=torch.uint8, device=dev)
-    ms, steps, launches = time_calls(lambda: dsa.dsa_indexer_k_hadamard_mxfp4(k, slots, N, 128, fp4, sc, N, stream),
-                                     dev, stream, seconds)
-    nbytes = N * (256 + 8 + 68)
-    recs.append(hbm_record("k_hadamard_mxfp4", "1,048,576 keys x 128 bf16 -> Hadamard -> mxfp4 rows at permuted "
-                           "pool slots", nbytes, ms, peaks, steps, launches, "inputs larger than L2"))
-    del k, slots, fp4, sc
+    if name == "k_hadamard_mxfp4":
+        # indexer-key Hadamard + mxfp4 write into a paged pool: 1M keys
+        N = 1 << 20
+        k = d(synth.normal_bf16(rng, (N, 128), "k").view(np.int16))
+        slots = d(rng.permutation(N, "slots").astype(np.int64))
+        fp4 = torch.empty((N, 64), dtype=torch.uint8, device=dev)
+        sc = torch.empty((N, 4), dtype=torch.uint8, device=dev)
+        ms, steps, launches = time_calls(lambda: dsa.dsa_indexer_k_hadamard_mxfp4(k, slots, N, 128, fp4, sc, N,
+                                                                                  stream), dev, stream, seconds)
+        return hbm_record(name, "1,048,576 keys x 128 bf16 -> Hadamard -> mxfp4 rows at permuted pool slots",
+                          N * (256 + 8 + 68), ms, peaks, steps, launches, "inputs larger than L2")
 
     # sparse attention over the selection, straight from the paged mxfp4 cache
-    for name in ("flash_decode", "pro_mtp", "fp8_chunked"):
-        ab = synth.make_attn_config(name)
-        aq, asel = d(ab.q.view(np.int16)), d(ab.sel)
-        afp4, asc, atab, asink = d(ab.kv_fp4), d(ab.kv_scale), d(ab.table), d(ab.sink)
-        out = torch.empty((ab.T, 64, 128), dtype=torch.float32, device=dev)
-        f = lambda: dsa.dsa_sparse_attn_mxfp4(aq, ab.T, 64, 128, asel, ab.topk, afp4, asc, afp4.shape[0],
-                                              ab.block_size, atab, atab.shape[1], ab.next_n, asink, ab.scale,
-                                              out, stream)
-        ms, steps, launches = time_calls(f, dev, stream, seconds)
-        nbytes, flops = attn_work(ab)
-        gbps, tflops = nbytes / (ms * 1e-3) / 1e9, flops / (ms * 1e-3) / 1e12
-        tpeak = peaks["bf16_tflops"]
-        bound = "hbm" if nbytes / peaks["hbm_gbs"] >= flops / (tpeak * 1e3) else "tensor"
-        recs.append({"workload": "sparse_attn_" + name,
-                     "desc": f"{ab.T} query rows x 64 heads x 128 dims over top-{ab.topk} rows of the paged "
-                             "mxfp4 cache, sink logits, fp32 out", "ms": ms, "steps": steps,
-                     "launches_per_call": launches, "qtok_s": ab.T / (ms * 1e-3),
-                     "roofline": {"bound": bound, "achieved": gbps if bound == "hbm" else tflops,
-                                  "peak": peaks["hbm_gbs"] if bound == "hbm" else tpeak,
-                                  "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
-                                  "frac": gbps / peaks["hbm_gbs"] if bound == "hbm" else tflops / tpeak,
-                                  "hbm_frac": gbps / peaks["hbm_gbs"], "tensor_frac": tflops / tpeak,
-                                  "bytes_per_call": int(nbytes), "flops_per_call": int(flops),
-                                  "peak_source": f"{peaks['source']}: hbm_gbs / bf16_tflops (burst)"}})
-        del aq, asel, afp4, asc, atab, asink, out
-    torch.cuda.empty_cache()
+    shape = name[len("sparse_attn_"):]
+    ab = synth.make_attn_config(shape)
+    aq, asel = d(ab.q.view(np.int16)), d(ab.sel)
+    afp4, asc, atab, asink = d(ab.kv_fp4), d(ab.kv_scale), d(ab.table), d(ab.sink)
+    out = torch.empty((ab.T, 64, 128), dtype=torch.float32, device=dev)
+    f = lambda: dsa.dsa_sparse_attn_mxfp4(aq, ab.T, 64, 128, asel, ab.topk, afp4, asc, afp4.shape[0],
+                                          ab.block_size, atab, atab.shape[1], ab.next_n, asink, ab.scale, out,
+                                          stream)
+    ms, steps, launches = time_calls(f, dev, stream, seconds)
+    nbytes, flops = attn_work(ab)
+    gbps, tflops = nbytes / (ms * 1e-3) / 1e9, flops / (ms * 1e-3) / 1e12
+    tpeak = peaks["bf16_tflops"]
+    bound = "hbm" if nbytes / peaks["hbm_gbs"] >= flops / (tpeak * 1e3) else "tensor"
+    return {"workload": name,
+            "desc": f"{ab.T} query rows x 64 heads x 128 dims over top-{ab.topk} rows of the paged mxfp4 cache, "
+                    "sink logits, fp32 out", "ms": ms, "steps": steps, "launches_per_call": launches,
+            "qtok_s": ab.T / (ms * 1e-3),
+            "roofline": {"bound": bound, "achieved": gbps if bound == "hbm" else tflops,
+                         "peak": peaks["hbm_gbs"] if bound == "hbm" else tpeak,
+                         "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                         "frac": gbps / peaks["hbm_gbs"] if bound == "hbm" else tflops / tpeak,
+                         "hbm_frac": gbps / peaks["hbm_gbs"], "tensor_frac": tflops / tpeak,
+                         "bytes_per_call": int(nbytes), "flops_per_call": int(flops),
+                         "peak_source": f"{peaks['source']}: hbm_gbs / bf16_tflops (burst)"}}
+
+
+def next_records(dev, stream, peaks, seconds: float):
+    import torch
+    recs = []
+    for name in NEXT_NAMES:
+        recs.append(next_record(name, dev, stream, peaks, seconds))
+        torch.cuda.empty_cache()
     return recs
+
+
+def run_one_next(args):
+    """--next NAME: time one of the rows beyond the hot path on its own (for profiler
+    captures of that kernel) and print its record."""
+    import torch
+
+    from deepseek_v4_sparse_dsa_gb300 import dsa
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dsa.load()
+    rec = next_record(args.next, dev, torch.cuda.current_stream(dev), load_peaks(), args.sub_seconds)
+    print(json.dumps(rec), flush=True)
 
 
 def run_ours(args, rank, world):
@@ -639,8 +664,13 @@ def main():
                     help="skip the sub-records of the other configurations")
     ap.add_argument("--sub-seconds", type=float, default=0.5, help="timed seconds per sub-record")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
+    ap.add_argument("--next", default=None, choices=NEXT_NAMES,
+                    help="time only this row beyond the hot path (a profiler target) and print its record")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.next:
+        run_one_next(args)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
 

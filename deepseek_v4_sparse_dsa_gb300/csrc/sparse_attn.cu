@@ -350,15 +350,6 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
       if (ntiles > 1) raw = load_row(a, rows_s[kTile + j]);
 
       for (int i = 0; i < ntiles; ++i) {
-        // decode tile i + 1 once the products of tile i - 1 are done with its buffer
-        if (i + 1 < ntiles) {
-          const int T = i + 1, b = T & 1;
-          ok &= mbar_wait(xfree(b), ((uint32_t)(T >> 1) & 1u) ^ 1u, limit, abort_flag);
-          decode_row(raw, x_s + b * kXBytes, j, lut);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(xfull(b));
-          if (i + 2 < ntiles) raw = load_row(a, rows_s[(i + 2) * kTile + j]);
-        }
         // scores of tile i (read twice from tensor memory: for the maximum, then for P)
         const int b = i & 1;
         const bool live = rows_s[i * kTile + j] >= 0;
@@ -407,6 +398,16 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
           if (f != 1.f) flags[0] = i + 1;
         }
         if (!(ok = group_all(ok))) break;
+        // decode tile i + 1 into the buffer of tile i - 1: its products were issued with
+        // tile i - 1's P, before this tile's maximum was taken, so they are done or nearly
+        if (i + 1 < ntiles) {
+          const int T = i + 1, xb = T & 1;
+          ok &= mbar_wait(xfree(xb), ((uint32_t)(T >> 1) & 1u) ^ 1u, limit, abort_flag);
+          decode_row(raw, x_s + xb * kXBytes, j, lut);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(xfull(xb));
+          if (i + 2 < ntiles) raw = load_row(a, rows_s[(i + 2) * kTile + j]);
+        }
         // P (and the rescale of O and L) once the products of tile i - 1 are done
         if (i > 0) ok &= mbar_wait(pfree, (uint32_t)(i - 1) & 1u, limit, abort_flag);
         tc_fence_after();

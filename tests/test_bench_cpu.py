@@ -79,3 +79,20 @@ def test_config_is_shared_by_both_arms():
     c = bench.config_of("fp8_chunked", wl, 0, 1)
     assert c["workload"] == "fp8_chunked" and c["topk"] == 1024 and c["dtype"] == "e4m3"
     assert "gather" in c["l2"]                   # the 2 GiB output write flushes L2 every step
+
+
+def test_attention_work_closed_form():
+    # 3 rows x top-4 with 2 padded slots: 10 live rows of 68 B, q bf16 + fp32 out per row,
+    # 4 B per slot, the 64 sinks; 4 x 64 x 128 flops per (row, slot) for S and P.V
+    from deepseek_v4_sparse_dsa_gb300.synth import AttnBatch
+    sel = np.array([[1, 2, -1, 3], [0, 0, 0, 0], [5, -1, 6, 7]], np.int32)
+    z = np.zeros(0, np.uint8)
+    ab = AttnBatch("shape", 3, 1, np.array([8, 8, 8]), 4, 16, z, sel, z, z, z, z, 0.1)
+    nbytes, flops = bench.attn_work(ab)
+    assert nbytes == 10 * 68 + 3 * 64 * 128 * (2 + 4) + 12 * 4 + 64 * 4
+    assert flops == 4 * 64 * 128 * 3 * 4
+
+
+def test_next_rows_are_named():
+    assert bench.NEXT_NAMES == ("flash_decode_fp4k", "q_rope_quant", "k_hadamard_mxfp4",
+                                "sparse_attn_flash_decode", "sparse_attn_pro_mtp", "sparse_attn_fp8_chunked")
