@@ -17,7 +17,13 @@ dsa_oracle_np.py):
 * ``mxfp4_paged_gather``, ``mxfp4_dequant``, ``e2m1_value``, ``e8m0_scale``,
   ``f64_to_bf16_bits`` -- the paged mxfp4 gather of xkernels issue #28
   "DeepSeek-V4 serving support -- tracking", comment 2 "What it does";
-* ``bf16_to_f64``, ``e4m3_to_f64`` -- the storage decoders.
+* ``bf16_to_f64``, ``e4m3_to_f64`` -- the storage decoders;
+* ``e4m3_encode``, ``q_rope_quant`` -- the indexer-query RoPE + E4M3 producer (vllm PR #1
+  "Sparse-MLA bring-up on MI300X", "Root cause story" items 1 and 3);
+* ``e2m1_encode``, ``k_hadamard_mxfp4`` -- the indexer-key Hadamard + mxfp4 writer
+  (ROCm/ATOM issue #707, "CSA");
+* ``sparse_attn`` -- the sparse attention over the selection with sink logits
+  (ROCm/ATOM issue #707, "CSA").
 
 The worker count is ``DSA_ORACLE_THREADS`` (default: every hardware thread).
 """

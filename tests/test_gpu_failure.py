@@ -5,6 +5,8 @@ window refill.
   wait that does not succeed at once gives up: the kernels abandon the call's work,
   drain their own copies and MMAs, free tensor memory, flag DSA_DEVERR_TIMEOUT and
   return.  The host reads the flag, and the next call on the same context is correct.
+  The same holds for the FP4-key score's converter warps and for the sparse attention
+  (whose group barriers AND the waits' results, so its warps leave together).
 * A paged sequence whose work items span more than the producer's 256-entry window of
   block-table entries (block size 8, items of up to 5000 keys = 625 pages) makes the
   producer refill that window in the middle of an item.
@@ -66,3 +68,34 @@ def test_block_table_window_refilled_mid_item():
     ref = parity.oracle_logits(wl, rows=rows)
     parity.assert_logits_close(lg[rows], ref)
     parity.selection_parity(idx.cpu().numpy()[rows], ref, wl.topk)
+
+
+def test_expired_waits_in_fp4_key_mode():
+    # the converter warps' waits are bounded too; the next call on the context is right
+    wl = parity.make_case(321, [9000, 3000], next_n=2, block_size=64, dtype="e4m3", topk=128, k_format="mxfp4")
+    db = DeviceBatch.from_workload(wl)
+    err = _with_wait_limit(1, lambda: db.logits_topk())
+    assert err >= 0 and err & dsa.DSA_DEVERR_TIMEOUT, err
+    idx, val = db.logits_topk()
+    lg = db.logits()
+    assert dsa.dsa_device_error() == 0
+    lg = lg.cpu().numpy()
+    parity.assert_topk_exact(idx.cpu().numpy(), lg, wl.topk, val.cpu().numpy())
+    parity.assert_logits_close(lg, parity.oracle_logits(wl))
+
+
+def test_expired_waits_in_sparse_attention():
+    # every wait of the attention kernel is bounded: with a 1 ns limit its group leaves
+    # together through the barrier's AND, the MMA thread drains, tensor memory is freed
+    import test_gpu_attn as ta
+    from deepseek_v4_sparse_dsa_gb300 import synth
+    ab = synth.make_attn(331, [3000, 900], next_n=2, topk=512)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q, sel, fp4, sc, tab, sink = (d(ab.q.view(np.int16)), d(ab.sel), d(ab.kv_fp4), d(ab.kv_scale), d(ab.table),
+                                  d(ab.sink))
+    out = torch.empty((ab.T, 64, 128), dtype=torch.float32, device="cuda")
+    err = _with_wait_limit(1, lambda: dsa.dsa_sparse_attn_mxfp4(
+        q, ab.T, 64, 128, sel, ab.topk, fp4, sc, fp4.shape[0], ab.block_size, tab, tab.shape[1], ab.next_n, sink,
+        ab.scale, out))
+    assert err >= 0 and err & dsa.DSA_DEVERR_TIMEOUT, err
+    ta.check(ab)                                  # default limit: right again
