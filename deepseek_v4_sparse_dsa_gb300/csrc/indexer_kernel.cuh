@@ -861,19 +861,23 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
         const uint8_t* f4 = f4_s + (size_t)s4 * F4_BYTES;
         const uint32_t sw = *reinterpret_cast<const uint32_t*>(f4 + 8192 + ct * 4);
         uint8_t* dst = k_s + (size_t)c * K_BYTES + ct * 128;
-        // the row's scale bytes decide, once, between the table and the exact decode
+        // the row's scale bytes decide, once, between the table and the exact decode; all
+        // 16 pieces are decoded before any is stored (a store between two table reads would
+        // keep the compiler from issuing the reads together)
         auto convert = [&](auto decode) {
+          uint4 o[16];
 #pragma unroll
           for (int g = 0; g < 4; ++g) {               // group g: elements 32 g .. 32 g + 31
             const uint4 v = *reinterpret_cast<const uint4*>(f4 + ct * 64 + g * 16);
             const uint32_t b = (sw >> (8 * g)) & 0xFFu;
             const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {             // elements 32 g + 8 w .. + 7
-              const uint4 o = decode(words[w], b);
-              const int pc = (g & 1) * 4 + w;         // piece within K chunk g / 2
-              *reinterpret_cast<uint4*>(dst + (g >> 1) * K_CHUNK + ((pc ^ (ct & 7)) << 4)) = o;
-            }
+            for (int w = 0; w < 4; ++w) o[4 * g + w] = decode(words[w], b);   // elements 32 g + 8 w ..
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int pc = ((i >> 2) & 1) * 4 + (i & 3);   // piece within K chunk i / 8
+            *reinterpret_cast<uint4*>(dst + (i >> 3) * K_CHUNK + ((pc ^ (ct & 7)) << 4)) = o[i];
           }
         };
         if (!e8m0_word_off_table(sw))

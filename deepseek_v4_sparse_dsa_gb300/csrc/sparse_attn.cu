@@ -180,17 +180,21 @@ __device__ __forceinline__ RawRow load_row(const AttnArgs& a, int32_t row) {
 // 16-byte piece p of row j at j * 128 + ((p ^ (j & 7)) << 4).
 __device__ __forceinline__ void decode_row(const RawRow& r, uint8_t* tile, int j, const uint2* lut) {
   uint8_t* dst = tile + j * 128;
+  // all 16 pieces are decoded before any is stored: a store between two table reads would
+  // keep the compiler from issuing the reads together (it cannot tell them apart)
   auto put = [&](auto decode) {
+    uint4 o[16];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const uint32_t b = (r.sc >> (8 * g)) & 0xFFu;
       const uint32_t words[4] = {r.w[g].x, r.w[g].y, r.w[g].z, r.w[g].w};
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint4 o = decode(words[w], b);
-        const int pc = (g & 1) * 4 + w;
-        *reinterpret_cast<uint4*>(dst + (g >> 1) * 16384 + ((pc ^ (j & 7)) << 4)) = o;
-      }
+      for (int w = 0; w < 4; ++w) o[4 * g + w] = decode(words[w], b);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int pc = ((i >> 2) & 1) * 4 + (i & 3);
+      *reinterpret_cast<uint4*>(dst + (i >> 3) * 16384 + ((pc ^ (j & 7)) << 4)) = o[i];
     }
   };
   if (!r.valid)
@@ -430,23 +434,28 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(sfree(b));
-          uint8_t* prow = p_s + j * 128;
+          // P for all 64 heads first, then the stores (the running maxima are read without a
+          // store in between)
+          uint32_t pw[32];
 #pragma unroll
           for (int pc = 0; pc < 8; ++pc) {          // heads 8 pc .. 8 pc + 7
             const float4 m0 = reinterpret_cast<const float4*>(mrun)[2 * pc];
             const float4 m1 = reinterpret_cast<const float4*>(mrun)[2 * pc + 1];
             const float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-            uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int h = 8 * pc + 2 * e;
               const float p0 = live ? ex2(__uint_as_float(sv[h]) * a.scale_log2 - mm[2 * e]) : 0.f;
               const float p1 = live ? ex2(__uint_as_float(sv[h + 1]) * a.scale_log2 - mm[2 * e + 1]) : 0.f;
               const __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
-              w[e] = *reinterpret_cast<const uint32_t*>(&pr);
+              pw[4 * pc + e] = *reinterpret_cast<const uint32_t*>(&pr);
             }
-            *reinterpret_cast<uint4*>(prow + ((pc ^ (j & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
+          uint8_t* prow = p_s + j * 128;
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc)
+            *reinterpret_cast<uint4*>(prow + ((pc ^ (j & 7)) << 4)) =
+                make_uint4(pw[4 * pc], pw[4 * pc + 1], pw[4 * pc + 2], pw[4 * pc + 3]);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
