@@ -17,8 +17,8 @@
 // lane, five across lanes by shuffles) scaled by 1/sqrt(128), then the OCP MX encoding
 // of the gather's layout: per 32-element group (8 lanes) the E8M0 byte is
 // max(exponent field of amax - 2, 0) (= floor(log2 amax) - 2 + 127), each element the
-// nearest E2M1 code of value / 2^(byte - 127) (ties to the even code, saturating at 6),
-// packed two per byte, low nibble = even element.
+// nearest E2M1 code of value / 2^(byte - 127) (ties to the even code, saturating at 6, by
+// the hardware conversion; zero results +0), packed two per byte, low nibble = even element.
 //
 // Both are HBM-bound streams (a few hundred bytes per row); loads for several rows are
 // issued before any of them is used.
@@ -119,14 +119,20 @@ struct KWriteArgs {
   uint8_t* scale;
 };
 
-// Nearest E2M1 code of v (ties to the even code, saturating at 6): the number of rounding
-// boundaries at or below |v|.  A tie goes to the neighbour whose code is even: down at
-// 0.25, 1.25, 2.5 and 5 (codes 0, 2, 4, 6 below), up at 0.75, 1.75 and 3.5.
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-  const float a = fabsf(v);
-  const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) + (uint32_t)(a >= 1.75f) +
-                     (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
-  return c | ((v < 0.f && c != 0u) ? 8u : 0u);
+// Nearest E2M1 codes of a pair (ties to the even code, saturating at +-6) by the tensor-core
+// conversion instruction: `hi` in the high nibble, `lo` in the low one.
+__device__ __forceinline__ uint32_t e2m1x2(float hi, float lo) {
+  uint16_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Clears the sign of every nibble of `nib` (4 nibbles) whose magnitude is 0: a value that
+// rounds to zero is written as +0.
+__device__ __forceinline__ uint32_t positive_zeros4(uint32_t nib) {
+  const uint32_t mag = nib & 0x7777u;
+  const uint32_t nz = (mag | (mag >> 1) | (mag >> 2)) & 0x1111u;
+  return nib & ((nz << 3) | 0x7777u);
 }
 
 __global__ void __launch_bounds__(256) k_hadamard_mxfp4_kernel(const KWriteArgs a) {
@@ -183,8 +189,9 @@ __global__ void __launch_bounds__(256) k_hadamard_mxfp4_kernel(const KWriteArgs 
       const int byte = amax > 0.f ? max(ef - 2, 0) : 0;
       const float inv = __uint_as_float((uint32_t)(254 - byte) << 23);   // 2^(127 - byte)
       uint32_t nib = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) nib |= (amax > 0.f ? e2m1_code(__fmul_rn(x[i], inv)) : 0u) << (4 * i);
+      if (amax > 0.f)                            // element 4 lane + i in nibble i
+        nib = positive_zeros4(e2m1x2(__fmul_rn(x[1], inv), __fmul_rn(x[0], inv)) |
+                              (e2m1x2(__fmul_rn(x[3], inv), __fmul_rn(x[2], inv)) << 8));
       // the 4 scale bytes of the row, from lanes 0, 8, 16, 24
       uint32_t sbytes = 0;
 #pragma unroll
