@@ -162,7 +162,7 @@ dsa_status dsa_indexer_q_rope_quant(const uint16_t* q, const int32_t* positions,
   if ((int64_t)T * H == 0) return DSA_OK;
   if (q == nullptr || positions == nullptr || q_fp8 == nullptr || q_scale == nullptr) return DSA_ERR_INVALID_ARG;
   if (rope_dim > 0 && (cos_sin == nullptr || !aligned(cos_sin, 8))) return DSA_ERR_INVALID_ARG;
-  if (!aligned(q, 8) || !aligned(q_fp8, 4) || !aligned(q_scale, 4)) return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(q_fp8, 8) || !aligned(q_scale, 4)) return DSA_ERR_INVALID_ARG;
   return cuda_status(launch_q_rope_quant(q, positions, cos_sin, max_pos, rope_dim, T, H, q_fp8, q_scale,
                                          device_sm_count(), static_cast<cudaStream_t>(stream)));
 }
@@ -173,7 +173,7 @@ dsa_status dsa_indexer_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot_m
   if (N < 0 || num_rows < 0) return DSA_ERR_INVALID_ARG;
   if (N == 0) return DSA_OK;
   if (k == nullptr || slot_mapping == nullptr || kv_fp4 == nullptr || kv_scale == nullptr) return DSA_ERR_INVALID_ARG;
-  if (!aligned(k, 8) || !aligned(kv_fp4, 2) || !aligned(kv_scale, 4)) return DSA_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(kv_fp4, 4) || !aligned(kv_scale, 4)) return DSA_ERR_INVALID_ARG;
   return cuda_status(launch_k_hadamard_mxfp4(k, slot_mapping, N, kv_fp4, kv_scale, num_rows, device_sm_count(),
                                              static_cast<cudaStream_t>(stream)));
 }

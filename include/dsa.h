@@ -202,12 +202,12 @@ dsa_status mxfp4_paged_gather(const uint8_t* kv_fp4, const uint8_t* kv_scale, in
  *   3. q_fp8[t, h, d] = E4M3(y[d] / q_scale[t, h]), nearest even, saturating at +-448.
  * All arithmetic in fp32, each product and sum rounded on its own.  The output is the
  * (q, q_scale) pair dsa_indexer_logits* take with dtype DSA_E4M3.
- *  q        [T, H, D] bf16 bit patterns, 8-byte aligned.
+ *  q        [T, H, D] bf16 bit patterns, 16-byte aligned.
  *  positions [T] int32; a position outside [0, max_pos) gives a zero row (codes 0,
  *           scale 0) and sets DSA_DEVERR_INDEX.
  *  cos_sin  [max_pos, rope_dim] fp32 (rope_dim / 2 cosines, then rope_dim / 2 sines per
  *           position), 8-byte aligned; may be NULL when rope_dim == 0.
- *  q_fp8    [T, H, D] E4M3 codes (4-byte aligned); q_scale [T, H] fp32.
+ *  q_fp8    [T, H, D] E4M3 codes (8-byte aligned); q_scale [T, H] fp32.
  * D must be 128 (DSA_ERR_UNSUPPORTED otherwise); rope_dim a multiple of 4, <= D.
  */
 dsa_status dsa_indexer_q_rope_quant(const uint16_t* q, const int32_t* positions, const float* cos_sin,
@@ -225,10 +225,10 @@ dsa_status dsa_indexer_q_rope_quant(const uint16_t* q, const int32_t* positions,
  *       code of y / 2^(byte - 127) (ties to the even code, saturating at 6; zero results
  *       are +0), packed two per byte of kv_fp4[r], low nibble = even element
  *       (the OCP MX v1.0 conversion, in the layout mxfp4_paged_gather reads).
- *  k            [N, D] bf16 bit patterns, 8-byte aligned.
+ *  k            [N, D] bf16 bit patterns, 16-byte aligned.
  *  slot_mapping [N] int64 pool rows (block * block_size + offset); < 0: key skipped;
  *               >= num_rows: skipped and DSA_DEVERR_INDEX set.
- *  kv_fp4       [num_rows, D/2] bytes; kv_scale [num_rows, D/32] bytes (4-byte aligned).
+ *  kv_fp4       [num_rows, D/2] bytes; kv_scale [num_rows, D/32] bytes (both 4-byte aligned).
  * D must be 128.  The transform is summed by butterflies in fp32: a code can differ
  * from the one of the exactly rounded rotation only where that value lies within a few
  * fp32 ulps of an E2M1 rounding boundary.
