@@ -943,6 +943,53 @@ __device__ __forceinline__ uint4 decode8(uint32_t w, uint32_t b, const uint2* lu
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// The same decode without a table in shared memory, by byte permutation.  For one scale
+// byte b (2..252, or 0xFF), the bf16 patterns of the 8 magnitudes (code 0 -> 0, code c >= 1
+// -> ((b - 1) << 7) + (c << 6), minus 64 for code 1) are split into their low and high
+// bytes, 8 of each in two registers; a word's 8 magnitude codes select from them with
+// `prmt` (4 selectors per instruction), two more `prmt` interleave low and high bytes into
+// bf16 pairs, and the signs are or-ed in.  Shared-memory table reads of random bytes
+// conflict across banks; this form is all ALU work.
+struct E2M1Bytes {
+  uint32_t lo0, lo1, hi0, hi1;   // low / high bytes of the patterns of codes 0-3 and 4-7
+};
+
+__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ E2M1Bytes e2m1_bytes(uint32_t b) {
+  const uint32_t e = (b - 1u) << 7;
+  uint32_t p01 = e << 16;                            // codes 0, 1 (bf16 pairs)
+  uint32_t p23 = (e + 128u) | ((e + 192u) << 16);
+  uint32_t p45 = (e + 256u) | ((e + 320u) << 16);
+  uint32_t p67 = (e + 384u) | ((e + 448u) << 16);
+  if (b == 255u) p01 = p23 = p45 = p67 = 0u;         // scale 0: signed zeros only
+  E2M1Bytes t;
+  t.lo0 = byte_perm(p01, p23, 0x6420u);
+  t.hi0 = byte_perm(p01, p23, 0x7531u);
+  t.lo1 = byte_perm(p45, p67, 0x6420u);
+  t.hi1 = byte_perm(p45, p67, 0x7531u);
+  return t;
+}
+
+// Eight elements (nibbles of w, low nibble first) as four bf16 pairs, by the tables of
+// e2m1_bytes (scale bytes 2..252 or 0xFF; the others take decode8_exact).
+__device__ __forceinline__ uint4 decode8_perm(uint32_t w, const E2M1Bytes& t) {
+  const uint32_t m = w & 0x77777777u, sg = w & 0x88888888u;
+  const uint32_t l0 = byte_perm(t.lo0, t.lo1, m), h0 = byte_perm(t.hi0, t.hi1, m);
+  const uint32_t l1 = byte_perm(t.lo0, t.lo1, m >> 16), h1 = byte_perm(t.hi0, t.hi1, m >> 16);
+  uint32_t o0 = byte_perm(l0, h0, 0x5140u), o1 = byte_perm(l0, h0, 0x7362u);
+  uint32_t o2 = byte_perm(l1, h1, 0x5140u), o3 = byte_perm(l1, h1, 0x7362u);
+  o0 |= ((sg << 12) & 0x8000u) | ((sg << 24) & 0x80000000u);   // nibble k's sign (bit 4k + 3)
+  o1 |= ((sg << 4) & 0x8000u) | ((sg << 16) & 0x80000000u);    // to bit 15 or 31 of its pair
+  o2 |= ((sg >> 4) & 0x8000u) | ((sg << 8) & 0x80000000u);
+  o3 |= ((sg >> 12) & 0x8000u) | (sg & 0x80000000u);
+  return make_uint4(o0, o1, o2, o3);
+}
+
 // Same, for any scale byte, nibble by nibble.
 __device__ __forceinline__ uint4 decode8_exact(uint32_t w, uint32_t b) {
   uint32_t o[4];

@@ -47,9 +47,6 @@ __device__ __forceinline__ int64_t gather_source(const GatherArgs& g, int64_t r,
 }
 
 __global__ void __launch_bounds__(256) mxfp4_gather_kernel(const GatherArgs g) {
-  __shared__ uint2 lut[256];
-  lut[threadIdx.x] = lut_entry(threadIdx.x);
-  __syncthreads();
   grid_dependency_wait();              // positions may come from the kernel just before
   const uint32_t lane = threadIdx.x & 31u;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -95,7 +92,7 @@ __global__ void __launch_bounds__(256) mxfp4_gather_kernel(const GatherArgs g) {
         }
       };
       if (!exact)
-        emit([&](uint32_t x, uint32_t b) { return decode8(x, b, lut); });
+        emit([](uint32_t x, uint32_t b) { return decode8_perm(x, e2m1_bytes(b)); });
       else
         emit([](uint32_t x, uint32_t b) { return decode8_exact(x, b); });
     }

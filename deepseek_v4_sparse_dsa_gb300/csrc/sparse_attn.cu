@@ -8,7 +8,8 @@
 // One CTA per query row: 64 heads x 128 dims, the selection in tiles of 128 rows.
 //  * Four converter / softmax warps.  Thread j owns row j of each tile: it resolves the
 //    row's cache position (block table), loads its 64 nibble bytes and 4 scale bytes,
-//    decodes them to bf16 (exact: every E2M1 x E8M0 value is a bf16 value) into the
+//    decodes them to bf16 (exact: every E2M1 x E8M0 value is a bf16 value; by byte
+//    permutation, no shared table) into the
 //    tile X [128 rows][128 dims] (K-major, 128-byte swizzle).  The next tile's bytes are
 //    in flight while the current tile's softmax runs.
 //  * One MMA thread, three tcgen05 products per tile, accumulators in tensor memory:
@@ -28,7 +29,7 @@
 // Every selected slot's cache row is resolved (selection, then block table) into shared
 // memory when the CTA starts, so the per-tile loads depend on nothing in flight.
 // Tensor memory: S double-buffered (2 x 64 columns), O and L (64 each): 256 columns;
-// 103 KB of shared memory + 4 B per selected slot: two CTAs per SM up to top-2048.
+// 101 KB of shared memory + 4 B per selected slot: two CTAs per SM up to top-2048.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -51,8 +52,7 @@ constexpr uint32_t kXOff = 16384;           // X tiles [2][2 K chunks][128 rows]
 constexpr uint32_t kXBytes = 32768;
 constexpr uint32_t kPOff = kXOff + 2 * kXBytes;        // P [128 rows][64 heads] bf16
 constexpr uint32_t kOnesOff = kPOff + 16384;           // two 1 KB swizzle atoms of bf16 1.0
-constexpr uint32_t kLutOff = kOnesOff + 2048;          // decode table, uint2[256]
-constexpr uint32_t kRedOff = kLutOff + 2048;           // per-warp head maxima [4][64]
+constexpr uint32_t kRedOff = kOnesOff + 2048;          // per-warp head maxima [4][64]
 constexpr uint32_t kMOff = kRedOff + 1024;             // running max [64]
 constexpr uint32_t kFacOff = kMOff + 256;              // this tile's rescale factors [64]
 constexpr uint32_t kSinkOff = kFacOff + 256;           // sink logits, base 2 [64]
@@ -178,7 +178,7 @@ __device__ __forceinline__ RawRow load_row(const AttnArgs& a, int32_t row) {
 
 // Row j of an X tile: 128 bf16 dims, dims 64 c .. 64 c + 63 in K chunk c (16 KB apart),
 // 16-byte piece p of row j at j * 128 + ((p ^ (j & 7)) << 4).
-__device__ __forceinline__ void decode_row(const RawRow& r, uint8_t* tile, int j, const uint2* lut) {
+__device__ __forceinline__ void decode_row(const RawRow& r, uint8_t* tile, int j) {
   uint8_t* dst = tile + j * 128;
   // all 16 pieces are decoded before any is stored: a store between two table reads would
   // keep the compiler from issuing the reads together (it cannot tell them apart)
@@ -200,7 +200,7 @@ __device__ __forceinline__ void decode_row(const RawRow& r, uint8_t* tile, int j
   if (!r.valid)
     put([](uint32_t, uint32_t) { return make_uint4(0u, 0u, 0u, 0u); });
   else if (!e8m0_word_off_table(r.sc))
-    put([&](uint32_t w, uint32_t b) { return decode8(w, b, lut); });
+    put([](uint32_t w, uint32_t b) { return decode8_perm(w, e2m1_bytes(b)); });
   else
     put([](uint32_t w, uint32_t b) { return decode8_exact(w, b); });
 }
@@ -211,7 +211,6 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
   uint8_t* q_s = sm + kQOff;
   uint8_t* x_s = sm + kXOff;
   uint8_t* p_s = sm + kPOff;
-  uint2* lut = reinterpret_cast<uint2*>(sm + kLutOff);
   float* red = reinterpret_cast<float*>(sm + kRedOff);
   float* mrun = reinterpret_cast<float*>(sm + kMOff);
   float* fac = reinterpret_cast<float*>(sm + kFacOff);
@@ -247,8 +246,6 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
   if (warp == 0) tmem_alloc(smem_u32(flags + 2), kTmemCols);
   if (warp > 0) {
     const int gt = threadIdx.x - 32;
-    lut[gt] = lut_entry((uint32_t)gt);
-    lut[gt + 128] = lut_entry((uint32_t)gt + 128u);
     // the ones tile: 2 KB of bf16 1.0
     reinterpret_cast<uint4*>(sm + kOnesOff)[gt] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   }
@@ -348,7 +345,7 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
 
       bool ok = true;
       RawRow raw = load_row(a, rows_s[j]);
-      decode_row(raw, x_s, j, lut);
+      decode_row(raw, x_s, j);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(xfull(0));
       if (ntiles > 1) raw = load_row(a, rows_s[kTile + j]);
@@ -407,7 +404,7 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
         if (i + 1 < ntiles) {
           const int T = i + 1, xb = T & 1;
           ok &= mbar_wait(xfree(xb), ((uint32_t)(T >> 1) & 1u) ^ 1u, limit, abort_flag);
-          decode_row(raw, x_s + xb * kXBytes, j, lut);
+          decode_row(raw, x_s + xb * kXBytes, j);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           mbar_arrive(xfull(xb));
           if (i + 2 < ntiles) raw = load_row(a, rows_s[(i + 2) * kTile + j]);
