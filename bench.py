@@ -528,15 +528,61 @@ def run_ours(args, rank, world):
         if run.has_gather:
             h_out.copy_(run.gout, non_blocking=True)
 
+    # Without padded slots (the headline) the steps are pipelined as a caller would run them:
+    # a copy stream brings each step's inputs in once the previous fused call has read them,
+    # and takes each step's results out while the next step computes (results double-
+    # buffered on the device and on the host).  Every step still copies its own inputs in
+    # and its own results out inside the timed region.
+    pipelined = run.has_gather and wl.gather_pad_frac == 0
+    if pipelined:
+        cs = torch.cuda.Stream(dev)
+        idxs = [run.idx, torch.empty_like(run.idx)]
+        gouts = [run.gout, torch.empty_like(run.gout)]
+        h_idxs = [h_idx, torch.empty(h_idx.shape, dtype=h_idx.dtype).pin_memory()]
+        h_outs = [h_out, torch.empty(h_out.shape, dtype=h_out.dtype).pin_memory()]
+        ev_in, ev_read = torch.cuda.Event(), torch.cuda.Event()
+        ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_copied = [torch.cuda.Event(), torch.cuda.Event()]
+        step_no = [0]
+
+        def e2e_step():
+            b = step_no[0] % 2
+            step_no[0] += 1
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev_read)                 # the previous fused call has read the inputs
+                db.q.copy_(h_q, non_blocking=True)
+                db.weights.copy_(h_w, non_blocking=True)
+                if h_qs is not None:
+                    db.q_scale.copy_(h_qs, non_blocking=True)
+                db.context_lens.copy_(h_lens, non_blocking=True)
+                if h_bt is not None:
+                    db.block_table.copy_(h_bt, non_blocking=True)
+                ev_in.record(cs)
+            stream.wait_event(ev_in)
+            stream.wait_event(ev_copied[b])            # this buffer's previous results are out
+            db.logits_topk(k, ws=run.ws, out_idx=idxs[b], with_values=False, stream=stream)
+            ev_read.record(stream)
+            db.gather(idxs[b], out=gouts[b], stream=stream)
+            ev_done[b].record(stream)
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev_done[b])
+                h_idxs[b].copy_(idxs[b], non_blocking=True)
+                h_outs[b].copy_(gouts[b], non_blocking=True)
+                ev_copied[b].record(cs)
+
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(3):
         e2e_step()
+    if pipelined:
+        stream.wait_stream(cs)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
+    if pipelined:
+        stream.wait_stream(cs)                         # the last results are on the host
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -577,7 +623,9 @@ def run_ours(args, rank, world):
         "gpu_launches": int(launches),
         "clocks": clocks,
         "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": e2e_steps},
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": e2e_steps,
+                "copies": "overlapped with the next step's compute on a copy stream" if pipelined
+                else "in line with the compute on one stream"},
     }
     if subs:
         out["configs"] = subs
