@@ -150,3 +150,10 @@ def test_attn_fp8_chunked_full_size_sampled_rows():
     ab = synth.make_attn_config("fp8_chunked")
     rows = np.sort(np.random.default_rng(7).choice(ab.T, 48, replace=False))
     check(ab, rows)
+
+
+@pytest.mark.parametrize("bs", [1, 256])
+def test_attn_block_sizes(bs):
+    # one cache row per page, and pages larger than a tile; three causal rows per sequence
+    ab = synth.make_attn(70 + bs, [1500, 333], next_n=3, topk=300, block_size=bs, pad_frac=0.03)
+    check(ab)
