@@ -193,7 +193,7 @@ dsa_status dsa_sparse_attn_mxfp4(const uint16_t* q, int64_t T, int H, int D, con
   if (!aligned(q, 16) || !aligned(kv_fp4, 16) || !aligned(kv_scale, 4) || !aligned(sink, 4) || !aligned(out, 4))
     return DSA_ERR_INVALID_ARG;
   return cuda_status(launch_sparse_attn(q, T, sel_pos, topk, kv_fp4, kv_scale, num_blocks, block_size, block_table,
-                                        bt_stride, next_n, sink, softmax_scale, out,
+                                        bt_stride, next_n, sink, softmax_scale, out, device_sm_count(),
                                         static_cast<cudaStream_t>(stream)));
 }
 

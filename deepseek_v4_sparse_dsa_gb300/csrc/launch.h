@@ -97,7 +97,7 @@ cudaError_t launch_k_hadamard_mxfp4(const uint16_t* k, const int64_t* slot, int6
 cudaError_t launch_sparse_attn(const uint16_t* q, int64_t T, const int32_t* sel, int k, const uint8_t* fp4,
                                const uint8_t* scale, int64_t num_blocks, int bs, const int32_t* table,
                                int64_t bt_stride, int next_n, const float* sink, float softmax_scale, float* out,
-                               cudaStream_t stream);
+                               int num_sms, cudaStream_t stream);
 size_t sparse_attn_smem_bytes(int k);   // dynamic shared memory for a top-k of k slots
 int sparse_attn_max_topk();
 

@@ -92,6 +92,7 @@ struct AttnArgs {
   const float* sink;         // [64]
   float scale_log2;          // softmax scale * log2 e
   float* out;                // [T, 64, 128] fp32
+  int split;                 // CTAs per query row (a cluster; 1, 2 or 4)
 };
 
 // Shared-memory descriptor with explicit byte offsets (128-byte swizzle).  K-major: SBO =
@@ -205,6 +206,20 @@ __device__ __forceinline__ void decode_row(const RawRow& r, uint8_t* tile, int j
     put([](uint32_t w, uint32_t b) { return decode8_exact(w, b); });
 }
 
+// Thread-block cluster: a barrier over every thread of the cluster (release / acquire), and
+// a load from the same shared-memory variable of another CTA of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
 __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -225,8 +240,12 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
   volatile int* abort_flag = flags + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t t = blockIdx.x;
-  const int ntiles = (a.k + kTile - 1) / kTile;
+  const int S = a.split;                          // the cluster of CTAs sharing query row t
+  const int64_t t = blockIdx.x / S;
+  const int rank = (int)(blockIdx.x % S);         // = the CTA's rank in its cluster
+  const int nall = (a.k + kTile - 1) / kTile;
+  const int tile0 = (int)((int64_t)nall * rank / S);          // this CTA's tiles of the selection
+  const int ntiles = (int)((int64_t)nall * (rank + 1) / S) - tile0;
   const unsigned long long limit = wait_limit_ns();
 
   if (threadIdx.x == 0) {
@@ -308,8 +327,20 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
     const int j = 32 * (warp & 3) + lane;         // TMEM lane: tile row (S^T) and dim (O^T)
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     float* orow = a.out + t * (kHeads * kDim);
+    float* opart = reinterpret_cast<float*>(x_s);   // split rows: this CTA's O [64 heads][128 dims]
+    float* lpart = red;                              // and its row sums L [64]
     if (ntiles == 0) {
-      for (int h = 0; h < kHeads; ++h) orow[h * kDim + j] = 0.f;
+      if (S == 1) {
+        for (int h = 0; h < kHeads; ++h) orow[h * kDim + j] = 0.f;
+      } else {
+        for (int h = 0; h < kHeads; ++h) opart[h * kDim + j] = 0.f;
+        if (gt < kHeads) {
+          const float s2 = __ldg(a.sink + gt) * kLog2e;
+          sink2[gt] = s2;
+          mrun[gt] = s2;
+          lpart[gt] = 0.f;
+        }
+      }
     } else {
       // the Q tile (K-major, 128-byte swizzle) and the sinks
       const uint4* qrow = reinterpret_cast<const uint4*>(a.q + t * (kHeads * kDim));
@@ -335,7 +366,7 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
         int32_t pos[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int slot = (m0 + u) * kTile + j;
+          const int slot = (tile0 + m0 + u) * kTile + j;
           pos[u] = (m0 + u < ntiles && slot < a.k) ? __ldg(a.sel + t * a.k + slot) : -1;
         }
 #pragma unroll
@@ -469,11 +500,19 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
           uint32_t o[32], l[32];
           tmem_ld32(tl + kColO + 32u * (uint32_t)hh, o);
           tmem_ld32(tl + kColL + 32u * (uint32_t)hh, l);
+          if (S == 1) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int h = 32 * hh + e;
-            const float den = __uint_as_float(l[e]) + ex2(sink2[h] - mrun[h]);
-            orow[h * kDim + j] = den > 0.f ? __uint_as_float(o[e]) / den : 0.f;
+            for (int e = 0; e < 32; ++e) {
+              const int h = 32 * hh + e;
+              const float den = __uint_as_float(l[e]) + ex2(sink2[h] - mrun[h]);
+              orow[h * kDim + j] = den > 0.f ? __uint_as_float(o[e]) / den : 0.f;
+            }
+          } else {                                // unnormalised, relative to mrun; the sink is added once
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              opart[(32 * hh + e) * kDim + j] = __uint_as_float(o[e]);
+              if (j == 32 * hh + e) lpart[j] = __uint_as_float(l[e]);
+            }
           }
         }
       } else {
@@ -485,6 +524,34 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (S > 1) {
+    // every CTA of the row's cluster holds its partial (O, L, running max); CTA r combines
+    // heads [r * 64 / S, (r + 1) * 64 / S) from all of them:
+    //   out = sum_p 2^(m_p - M) O_p / (sum_p 2^(m_p - M) L_p + 2^(sink - M)), M = max(sink, m_p).
+    // Every thread of every CTA passes both cluster barriers exactly once (the second one
+    // keeps each CTA's shared memory alive until its peers have read it).
+    cluster_sync_all();
+    if (warp > 0) {
+      const int j = 32 * (warp & 3) + lane;
+      const int hs = kHeads / S;
+      float* orow = a.out + t * (kHeads * kDim);
+      for (int h = rank * hs; h < (rank + 1) * hs; ++h) {
+        float M = sink2[h];
+        for (int r = 0; r < S; ++r) M = fmaxf(M, ld_peer(mrun + h, (uint32_t)r));
+        float num = 0.f, den = 0.f;
+        if (M > -INFINITY) {
+          den = ex2(sink2[h] - M);
+          for (int r = 0; r < S; ++r) {
+            const float f = ex2(ld_peer(mrun + h, (uint32_t)r) - M);
+            num += f * ld_peer(reinterpret_cast<const float*>(x_s) + h * kDim + j, (uint32_t)r);
+            den += f * ld_peer(red + h, (uint32_t)r);
+          }
+        }
+        orow[h * kDim + j] = den > 0.f ? num / den : 0.f;
+      }
+    }
+    cluster_sync_all();
+  }
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -493,23 +560,32 @@ __global__ void __launch_bounds__(32 + kGroup, 2) sparse_attn_kernel(const AttnA
 cudaError_t launch_sparse_attn(const uint16_t* q, int64_t T, const int32_t* sel, int k, const uint8_t* fp4,
                                const uint8_t* scale, int64_t num_blocks, int bs, const int32_t* table,
                                int64_t bt_stride, int next_n, const float* sink, float softmax_scale, float* out,
-                               cudaStream_t stream) {
+                               int num_sms, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   const size_t smem = attn_smem_bytes(k);
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  // A batch too small to fill the GPU (two CTAs per SM) splits each row's selection over a
+  // cluster of 2 or 4 CTAs (at most one per tile), combined through distributed shared memory.
+  const int nall = (k + kTile - 1) / kTile;
+  int split = 1;
+  while (split < 4 && (int64_t)T * split * 2 <= (int64_t)2 * num_sms && 2 * split <= nall) split *= 2;
   AttnArgs a{q, sel, k, fp4, scale, num_blocks, bs, table, bt_stride, next_n, sink,
-             (float)((double)softmax_scale * 1.4426950408889634), out};
+             (float)((double)softmax_scale * 1.4426950408889634), out, split};
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)T);
+  cfg.gridDim = dim3((unsigned)(T * split));
   cfg.blockDim = dim3(32 + kGroup);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)split;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, a);
   note_launch();
   if (e != cudaSuccess) return e;
