@@ -197,7 +197,10 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
         }
       }
       group_sync<NT>();
-      const uint32_t n = sh.cnt;
+      // The count runs past kHalf only when appends were dropped (flagged as an overflow):
+      // lists left stale by an abandoned call can hold thousands of equal keys, which no
+      // cut can thin.  Nothing past the half is ever read.
+      const uint32_t n = min(sh.cnt, (uint32_t)kHalf);
       if (n > (uint32_t)(kHalf - 4 * NT)) {
         uint64_t th = engine_cut_approx<NT, kHalf / NT>(cur, &sh.cnt, (int)n, topk, (uint32_t)(kHalf / 2), mbins,
                                                         &sh.esc, tid);
@@ -220,10 +223,10 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
   }
   // 3. exactly the top-k (or every candidate when there are fewer): a histogram cut
   //    first, then the radix select over what is left
-  uint32_t n = sh.cnt;
+  uint32_t n = min(sh.cnt, (uint32_t)kHalf);
   if (n > (uint32_t)topk) {
     engine_cut_approx<NT, kHalf / NT>(cur, &sh.cnt, (int)n, topk, n, mbins, &sh.esc, tid);
-    n = sh.cnt;
+    n = min(sh.cnt, (uint32_t)kHalf);
   }
   const uint64_t thr = engine_select<NT>(cur, (int)n, topk, &sh.esc, tid);
   uint64_t* out = mbuf + kMergeKeys;

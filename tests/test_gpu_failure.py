@@ -54,6 +54,29 @@ def test_expired_waits_flag_timeout_and_leave_the_context_usable(lens, next_n, t
     parity.assert_logits_close(lg[rows], parity.oracle_logits(wl, rows=rows))
 
 
+def test_merge_is_safe_on_a_stale_workspace():
+    # Lists left in the workspace by an abandoned call are read by the next merge.  Fill it
+    # with one repeated nonzero word (two -inf floats, as a freed logits buffer leaves it):
+    # every stale list then holds the same key, which no cut can thin, so the merge's
+    # candidate count runs past its shared buffer and must be held there.  A completed call
+    # rewrites every list it merges, so its result does not depend on what was there.
+    wl = parity.make_case(305, [20000, 9000, 3000], next_n=1, block_size=64, topk=512)
+    db = DeviceBatch.from_workload(wl)
+    poison = np.array([0xFF800000FF800000], dtype=np.uint64).view(np.int64)[0]
+
+    def stale_ws():
+        ws = db.workspace(dsa.DSA_OP_LOGITS_TOPK, wl.topk)
+        ws[: ws.numel() // 8 * 8].view(torch.int64).fill_(int(poison))
+        return ws
+
+    err = _with_wait_limit(1, lambda: db.logits_topk(ws=stale_ws()))
+    assert err >= 0 and err & dsa.DSA_DEVERR_TIMEOUT, err
+    idx, val = db.logits_topk(ws=stale_ws())
+    lg = db.logits()
+    assert dsa.dsa_device_error() == 0
+    parity.assert_topk_exact(idx.cpu().numpy(), lg.cpu().numpy(), wl.topk, val.cpu().numpy())
+
+
 def test_block_table_window_refilled_mid_item():
     # one sequence of 5000 keys in blocks of 8 (625 pages), 1216 causal queries: the
     # fused call's items cover up to 40 key tiles = 640 pages each
