@@ -215,6 +215,38 @@ __device__ __forceinline__ void mma_e4m3(uint32_t tmem_d, uint64_t a, uint64_t b
       : "memory");
 }
 
+// Block-scaled contraction (kind::mxf8f6f4, one E8M0 scale per 32 elements along K of
+// each operand row; fp32 accumulate; both operands K-major): A holds E2M1 codes in the
+// padded shared layout (16 codes = 8 packed bytes followed by 8 unused bytes, so a row of
+// 128 codes spans 128 bytes like an E4M3 row), B holds E4M3 codes.  The scale bytes are
+// read from tensor memory: byte `a_sf` (`b_sf`) of the 32-bit cells at the given columns
+// serves the 32 elements of this K step.  For M = 128 the scales of operand row
+// r = l + 32 j sit in column j of lane l, the same in each of the four lane quarters
+// (measured: a layout with row r in lane r scores only the first 32 rows right).
+__host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(int M, int N, uint32_t a_sf, uint32_t b_sf) {
+  return (b_sf << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | (a_sf << 29);
+}
+
+__device__ __forceinline__ void mma_mx(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t tmem_sfa,
+                                       uint32_t tmem_sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(tmem_sfa), "r"(tmem_sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Each thread of the warp writes 4 consecutive 32-bit columns of its own TMEM lane (the
+// warp's lane quarter is given in taddr); tmem_st_wait completes the warp's stores.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+               "r"(v2), "r"(v3)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -871,52 +903,14 @@ __device__ __forceinline__ uint32_t e2m1_bf16_general(uint32_t n, int b) {
   return s | ((2u + M) << (E + 5));                            // subnormal (E = 0 or -1)
 }
 
-// Fast form for 2 <= b <= 252 (every code lands in the normal range):
-// bits = ((b-1) << 7) + (code << 6), minus 64 for code 1; code 0 -> signed zero.
-__device__ __forceinline__ uint32_t e2m1_bf16_fast(uint32_t n, uint32_t base) {
-  const uint32_t s = (n & 8u) << 12;
-  const uint32_t c = n & 7u;
-  const uint32_t v = base + (c << 6) - (c == 1u ? 64u : 0u);
-  return (c != 0u ? v : 0u) | s;
-}
-
-// Decode table: entry `byte` holds the bf16 pair of its two nibbles (low nibble in the
-// low half) at scale byte b = 2, and a mask of the nonzero halves.  For 2 <= b <= 252
-// the pair at scale b is entry + ((b - 2) << 7 in both halves, masked): that moves the
-// exponent field of each nonzero half (at most 0x7F40 with the sign clear, so no carry
-// crosses a half) and leaves signed zeros alone.
-__device__ __forceinline__ uint2 lut_entry(uint32_t byte) {
-  uint32_t v = 0, m = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t n = (byte >> (4 * h)) & 0xFu;
-    v |= e2m1_bf16_fast(n, 1u << 7) << (16 * h);
-    if (n & 7u) m |= 0xFFFFu << (16 * h);
-  }
-  return make_uint2(v, m);
-}
-
-// bf16 bit pattern of an OCP E4M3 code (exact: every E4M3 value is a bf16 value).
-// Normal codes keep their 3 mantissa bits under the rebased exponent (bias 7 -> 127);
-// subnormals m * 2^-9 are renormalised; S.1111.111 is NaN.
-__device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t c) {
-  const uint32_t s = (c & 0x80u) << 8;
-  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
-  if (e == 15u && m == 7u) return s | 0x7FC0u;
-  if (e != 0u) return s | ((e + 120u) << 7) | (m << 4);
-  if (m == 0u) return s;
-  const uint32_t k = 31u - __clz(m);                  // leading bit of m (0..2)
-  return s | ((k + 118u) << 7) | ((m << (7u - k)) & 0x7Fu);
-}
-
-// Scale bytes whose results leave the table's reach: 0 and 1 (subnormal results), 253
-// and 254 (overflowing ones).  (x + 3) mod 256 maps them to 3, 4, 0, 1 and 0xFF to 2.
+// Scale bytes outside the fast decode's reach (which covers 2..252 and 0xFF): 0 and 1
+// (subnormal results), 253 and 254 (overflowing ones).  (x + 3) mod 256 maps them to 3, 4, 0, 1 and 0xFF to 2.
 __device__ __forceinline__ bool e8m0_off_table(uint32_t b) {
   const uint32_t v = (b + 3u) & 0xFFu;
   return v < 5u && v != 2u;
 }
 
-// Any of the four scale bytes packed in `w` off the table.
+// Any of the four scale bytes packed in `w` outside the fast decode's reach.
 __device__ __forceinline__ bool e8m0_word_off_table(uint32_t w) {
   bool r = false;
 #pragma unroll
@@ -925,26 +919,7 @@ __device__ __forceinline__ bool e8m0_word_off_table(uint32_t w) {
 }
 
 // Eight elements (nibble bytes of w, low nibble first) times 2^(b-127) as bf16 pairs,
-// for b in 2..252 or 0xFF.  2..252 take the table; 0xFF (scale 0) keeps only the signs
-// of the b = 2 entries, by a select.  Callers test e8m0_off_table once per row and send
-// the other bytes to decode8_exact: a branch inside this decode, even one never taken,
-// cost the FP4-key score more than half its time, and one taken for 0xFF (about one
-// group in a hundred in cache data, so a quarter of all warp-wide calls diverged) cost
-// it more than four times.
-__device__ __forceinline__ uint4 decode8(uint32_t w, uint32_t b, const uint2* lut) {
-  uint32_t o[4];
-  const uint32_t adj = ((b - 2u) << 7) * 0x10001u;
-  const bool zero = b == 255u;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint2 e = lut[(w >> (8 * k)) & 0xFFu];
-    o[k] = zero ? (e.x & 0x80008000u) : e.x + (adj & e.y);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// The same decode without a table in shared memory, by byte permutation.  For one scale
-// byte b (2..252, or 0xFF), the bf16 patterns of the 8 magnitudes (code 0 -> 0, code c >= 1
+// by byte permutation, with no table in shared memory.  For one scale byte b (2..252, or 0xFF), the bf16 patterns of the 8 magnitudes (code 0 -> 0, code c >= 1
 // -> ((b - 1) << 7) + (c << 6), minus 64 for code 1) are split into their low and high
 // bytes, 8 of each in two registers; a word's 8 magnitude codes select from them with
 // `prmt` (4 selectors per instruction), two more `prmt` interleave low and high bytes into

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(256) mxfp4_gather_kernel(const GatherArgs g) {
         }
       }
       if (h == 0) src_next = gather_source(g, r1, pos_next);
-      // the lane's scale bytes decide, once, between the table and the exact decode
+      // the lane's scale bytes decide, once, between the fast decode and the exact one
       bool exact = false;
 #pragma unroll
       for (int k = 0; k < 8; ++k) exact |= e8m0_off_table(sb[k]);

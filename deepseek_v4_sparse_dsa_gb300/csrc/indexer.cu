@@ -210,16 +210,14 @@ size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap) {
   return s;
 }
 
-// FP4-key mode: bf16 Q tile, `conv` converted bf16 key tiles, the E4M3 Q staging tile,
-// `stages` FP4 stages of 128 x (64 + 4) bytes, the 2 KB decode table.
+// FP4-key mode: `conv` padded E2M1 key tiles of 128 x 128 bytes, the E4M3 Q tile,
+// `stages` FP4 stages of 128 x (64 + 4) bytes.
 size_t smem_bytes_f4k(int nq, int stages, int conv, bool topk, int cap) {
   size_t s = 1024;
-  s += (size_t)nq * 64 * 256;                        // bf16 Q tile
-  s += (size_t)conv * 128 * 256;                     // converted key tiles
-  s += (size_t)nq * 64 * 128;                        // E4M3 Q staging
+  s += (size_t)conv * 128 * 128;                     // padded key tiles
+  s += (size_t)nq * 64 * 128;                        // E4M3 Q tile
   s += (size_t)stages * 128 * 68;                    // FP4 stages
-  s += 2048;                                         // decode table
-  s += (size_t)((2 * stages + 16 + 2 * conv + 1 + 1) & ~1) * 8;   // barriers (an even count)
+  s += (size_t)((2 * stages + 16 + 2 * conv + 1) & ~1) * 8;   // barriers (an even count)
   s += sizeof(EpiSmem<4>) + 16;
   if (topk) s += (size_t)nq * cap * 8;
   return s;
@@ -273,21 +271,27 @@ IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk) {
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
   if (pl.f4k) {
     // one CTA per SM: one epilogue group, four converter warps, a deep FP4 ring and as
-    // many converted tiles (2..3) as shared memory holds
+    // many padded key tiles (2..4) as shared memory holds
     pl.eg = 1;
     pl.ctas_per_sm = 1;
-    pl.stages = 6;
-    pl.conv_slots = 3;
+    pl.stages = 8;
+    pl.conv_slots = 4;
     while (pl.conv_slots > 2 && smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap) > kSmemLimit)
       --pl.conv_slots;
     while (pl.stages > 2 && smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap) > kSmemLimit) --pl.stages;
     pl.smem = smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap);
     if (pl.smem > kSmemLimit) pl.ok = false;
+    // Each CTA holds all 512 TMEM columns (accumulators and scale cells): the request is
+    // kept above half an SM's shared memory, so no second CTA is placed beside it.
+    if (pl.smem <= kSmemHalf) pl.smem = kSmemHalf + 1024;
   }
   // as many accumulator buffers (up to 4) as TMEM holds for the CTAs sharing an SM, so
   // the MMAs can run ahead of an epilogue busy cutting its candidates back
   pl.nbuf_log2 = 2;
   while (pl.nbuf_log2 > 1 && pl.ctas_per_sm * next_pow2((pl.nq * 64) << pl.nbuf_log2) > 512) --pl.nbuf_log2;
+  // FP4-key mode: the accumulators stay below column 256, the scale cells above it
+  if (pl.f4k)
+    while (pl.nbuf_log2 > 1 && ((pl.nq * 64) << pl.nbuf_log2) > 256) --pl.nbuf_log2;
   pl.ngroups = (qs.next_n + pl.nq - 1) / pl.nq;
   const int64_t units = (int64_t)qs.B * pl.ngroups;
   // logits mode: static chunks of the longest row, split when groups are few

@@ -231,12 +231,18 @@ __device__ bool next_slice_item(const IndexerParams& p, int slice, int r0, int r
   return false;
 }
 
+// E8M0 scale cells for the tensor cores: a byte 0xFF (scale 0 here, NaN there) becomes 127.
+__device__ __forceinline__ uint32_t e8m0_ff_to_one(uint32_t w) {
+  return w ^ (__vcmpeq4(w, 0xFFFFFFFFu) & 0x80808080u);
+}
+
 template <bool kFP8, int NQ, bool kTopk, int EG, bool kF4K>
 __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && !kF4K) ? 2 : 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const IndexerParams p) {
-  // kF4K: E4M3 queries against mxfp4 keys; both become bf16 on chip (exactly: E4M3 and
-  // E2M1 x 2^(b-127) values are bf16 values) and the contraction runs as bf16.
+  // kF4K: E4M3 queries against mxfp4 keys, contracted by the block-scaled MMA: the key
+  // codes in the padded E2M1 layout, their E8M0 scales in tensor memory, the E4M3 Q tile
+  // as loaded with scale 1.
   static_assert(!kF4K || (kFP8 && EG == 1), "FP4-key mode: E4M3 queries, one epilogue group");
   constexpr bool kMmaFP8 = kFP8 && !kF4K;          // E4M3 x E4M3 contraction
   constexpr bool kKeyScale = kFP8 && !kF4K;        // per-key fp32 scale (E4M3 keys)
@@ -249,9 +255,14 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
   constexpr uint32_t K_BYTES = K_CHUNK * KCH;
   constexpr int KSTEPS = KCH * 4;                  // 32 bytes of K per MMA
   constexpr uint32_t F4_BYTES = 128 * 64 + 128 * 4;   // FP4-key stage: nibble rows, then E8M0 rows
+  constexpr uint32_t KT_BYTES = kF4K ? K_CHUNK : K_BYTES;   // kF4K: a padded E2M1 tile, 128 B per key
+  constexpr uint32_t QS_BYTES = kF4K ? 0u : Q_BYTES;        // kF4K: the E4M3 Q tile is the operand as loaded
   const int NBL = p.nbuf_log2;                     // NB = 2^NBL accumulator buffers in TMEM
   const int NBM = (1 << NBL) - 1;
-  const uint32_t TMEM_COLS = ((N << NBL) < 32) ? 32u : (uint32_t)next_pow2(N << NBL);
+  // kF4K: accumulators in columns [0, 256), then the scale cells: 8 columns of the queries'
+  // scale bytes (all 127: scale 1), 4 columns of key scale bytes per converted tile
+  constexpr uint32_t SFB_COL = 256, SFA_COL = 264;
+  const uint32_t TMEM_COLS = kF4K ? 512u : ((N << NBL) < 32) ? 32u : (uint32_t)next_pow2(N << NBL);
   constexpr uint32_t IDESC = kMmaFP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N);
 
   extern __shared__ uint8_t smem_raw[];
@@ -260,17 +271,16 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int S = p.stages;
   const int CR = kF4K ? p.conv_slots : 0;
-  // layout: Q tile (MMA operand) | key stages (TMA) or converted tiles [CR] (kF4K) |
-  //         kF4K: E4M3 Q staging, FP4 stages [S], decode table | barriers | epilogue state
+  // layout: Q tile (MMA operand; none in kF4K) | key stages (TMA) or padded key tiles [CR]
+  //         (kF4K) | kF4K: E4M3 Q tile, FP4 stages [S] | barriers | epilogue state
   uint8_t* q_s = smem;
-  uint8_t* k_s = smem + Q_BYTES;                         // S stages (kF4K: CR converted tiles)
-  uint8_t* q8_s = k_s + (size_t)(kF4K ? CR : S) * K_BYTES;   // kF4K: the E4M3 Q tile as loaded
+  uint8_t* k_s = smem + QS_BYTES;                        // S stages (kF4K: CR padded tiles)
+  uint8_t* q8_s = k_s + (size_t)(kF4K ? CR : S) * KT_BYTES;  // kF4K: the E4M3 Q tile as loaded
   uint8_t* f4_s = q8_s + (kF4K ? Q_CHUNK : 0);           // kF4K: S stages of F4_BYTES
-  uint2* lut = reinterpret_cast<uint2*>(f4_s + (kF4K ? (size_t)S * F4_BYTES : 0));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(lut) + (kF4K ? 2048 : 0));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(f4_s + (kF4K ? (size_t)S * F4_BYTES : 0));
   // full[S] | empty[S] | tfull[4] | tempty[4] | qfull | qempty | ifull[2] | iempty[2] | mmadone | tmemfree
-  // | kF4K: cfull[CR] | cfree[CR] | qready
-  const int NBARS = (2 * S + 16 + (kF4K ? 2 * CR + 1 : 0) + 1) & ~1;   // even: es stays 16-byte aligned
+  // | kF4K: cfull[CR] | cfree[CR]
+  const int NBARS = (2 * S + 16 + (kF4K ? 2 * CR : 0) + 1) & ~1;   // even: es stays 16-byte aligned
   EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + NBARS);
   uint64_t* ebuf = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(es) + (sizeof(EpiSmem<NQ>) + 15) / 16 * 16);
 
@@ -281,7 +291,6 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
   const uint32_t mmadone = smem_u32(bars + 2 * S + 14);
   const uint32_t tmemfree = smem_u32(bars + 2 * S + 15);   // every epilogue warp is done with TMEM
   const uint32_t cfull0 = smem_u32(bars + 2 * S + 16), cfree0 = cfull0 + 8u * (uint32_t)CR;
-  const uint32_t qready = cfree0 + 8u * (uint32_t)CR;       // kF4K: the bf16 Q tile is written
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -300,7 +309,6 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
       mbar_init(cfull0 + 8 * c, 4);              // the 4 converter warps wrote the tile
       mbar_init(cfree0 + 8 * c, 1);              // the MMAs that read it are done
     }
-    if (kF4K) mbar_init(qready, 4);
     for (int a = 0; a < 4; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
       mbar_init(tempty0 + 8 * a, 4);          // the 4 warps of the group that read the tile
@@ -312,7 +320,7 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
     mbar_init(qfull, 1);
     mbar_init(qempty, 1);
     mbar_init(mmadone, 1);
-    mbar_init(tmemfree, 4 * EG);
+    mbar_init(tmemfree, 4 * EG + (kF4K ? 4 : 0));   // kF4K: the converters write scale cells
     es->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -394,7 +402,7 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
       if (lane == 0) {
         ok = mbar_wait(qempty, ((uint32_t)n & 1u) ^ 1u, limit, abort_flag);
         if (ok) {
-          if (kF4K) {                           // the E4M3 tile, for the converters
+          if (kF4K) {                           // the E4M3 tile, the MMAs' B operand as loaded
             mbar_arrive_expect_tx(qfull, Q_CHUNK);
             tma_load_2d(smem_u32(q8_s), &tm_q, qfull, 0, it.t0 * 64);
           } else {
@@ -528,11 +536,11 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
         if (!(ok = mbar_wait(ifull0 + 8 * slot, (uint32_t)(n >> 1) & 1u, limit, abort_flag))) break;
         const ItemInfo it = es->info[slot];
         if (!it.valid) break;
-        // the Q tile: loaded by TMA, or (kF4K) converted to bf16 by the converter warps
-        if (!(ok = mbar_wait(kF4K ? qready : qfull, (uint32_t)n & 1u, limit, abort_flag))) break;
-        const uint32_t qbase = smem_u32(q_s);
+        // the Q tile, loaded by TMA
+        if (!(ok = mbar_wait(qfull, (uint32_t)n & 1u, limit, abort_flag))) break;
+        const uint32_t qbase = smem_u32(kF4K ? q8_s : q_s);
         for (int i = 0; i < it.ntiles; ++i, ++T) {
-          const int s = kF4K ? T % CR : T % S;      // key stage, or (kF4K) converted tile
+          const int s = kF4K ? T % CR : T % S;      // key stage, or (kF4K) padded key tile
           const int a = T & NBM;
           const uint32_t kready = kF4K ? cfull0 + 8 * s : full0 + 8 * s;
           const uint32_t kphase = (uint32_t)(kF4K ? T / CR : T / S) & 1u;
@@ -540,8 +548,16 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
                mbar_wait(tempty0 + 8 * a, ((uint32_t)(T >> NBL) & 1u) ^ 1u, limit, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t stage = smem_u32(k_s + (size_t)s * K_BYTES);
+          const uint32_t stage = smem_u32(k_s + (size_t)s * KT_BYTES);
           const uint32_t d = tmem_base + (uint32_t)(a * N);
+          if constexpr (kF4K) {
+            // four K steps of 32: E2M1 keys (scale byte kk of the tile's cells) x E4M3 queries
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_mx(d, smem_desc_sw128(stage + (uint32_t)kk * 32u), smem_desc_sw128(qbase + (uint32_t)kk * 32u),
+                     idesc_mx_e2m1_e4m3(128, N, (uint32_t)kk, (uint32_t)kk), tmem_base + SFA_COL + 4u * (uint32_t)s,
+                     tmem_base + SFB_COL, kk > 0 ? 1u : 0u);
+          } else
 #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk) {
             const uint32_t off = (uint32_t)(kk & 3) * 32u;   // 16 bf16 / 32 E4M3 along K
@@ -787,15 +803,23 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
   }
   else if constexpr (kF4K) {
     // ============================ converters ============================
-    // Four warps turn each item's E4M3 Q tile, and each FP4 stage, into bf16 tiles in the
-    // MMA's operand layout (K-major rows of 128 bytes, 128-byte swizzle: 16-byte piece c
-    // of row r at r * 128 + ((c ^ (r & 7)) << 4)).  Thread ct owns key row ct of a tile.
-    // A failed wait skips that step's work; the group stops together at item boundaries.
+    // Four warps put each FP4 stage into the block-scaled MMA's operand form.  Thread ct
+    // copies key row ct's 64 nibble bytes to a 128-byte row of the padded E2M1 layout
+    // (16 codes = 8 packed bytes, the even code in the low nibble as in the cache, then
+    // 8 unused bytes) with the 128-byte swizzle (16-byte
+    // piece c of row r at r * 128 + ((c ^ (r & 7)) << 4)); each warp writes the tile's
+    // E8M0 bytes into its own lane quarter of the tile's scale cells: lane l, column j holds
+    // the four scale bytes of key row l + 32 j (the same in every quarter).  A scale byte
+    // 0xFF means scale 0 in this cache format but NaN to the tensor cores: its 32 codes are
+    // zeroed and the byte becomes 127.  A failed wait skips that step's work; the group
+    // stops together at item boundaries.
     constexpr int CBAR = 2;
     const int ct = threadIdx.x - (64 + 128 * EG);
-    lut[ct] = lut_entry((uint32_t)ct);
-    lut[ct + 128] = lut_entry((uint32_t)ct + 128u);
-    group_sync<128>(CBAR);
+    const uint32_t tq = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16);   // this warp's lane quarter
+    tmem_st4(tq + SFB_COL, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);   // the queries: scale 1
+    tmem_st4(tq + SFB_COL + 4u, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    tmem_st_wait();
+    tc_fence_before();
     int T = 0;
     for (int n = 0;; ++n) {
       const int slot = n & 1;
@@ -810,40 +834,6 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
       group_sync<128>(CBAR);
       if (es->cstop) break;
       const int ntiles = es->info[slot].ntiles;
-      // the item's Q tile
-      bool okq = (lane == 0) ? mbar_wait(qfull, (uint32_t)n & 1u, limit, abort_flag) : true;
-      okq = __shfl_sync(0xFFFFFFFFu, okq ? 1 : 0, 0) != 0;
-      if (okq) {
-        __syncwarp();
-        for (int r = ct; r < N; r += 128) {
-#pragma unroll
-          for (int pc = 0; pc < 8; ++pc) {           // E4M3 piece pc: elements 16 pc .. 16 pc + 15
-            const uint4 src = *reinterpret_cast<const uint4*>(q8_s + r * 128 + ((pc ^ (r & 7)) << 4));
-            const uint32_t wsrc[4] = {src.x, src.y, src.z, src.w};
-            uint32_t o[8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t lo = e4m3_to_bf16_bits((wsrc[k] >> (16 * h)) & 0xFFu);
-                const uint32_t hi = e4m3_to_bf16_bits((wsrc[k] >> (16 * h + 8)) & 0xFFu);
-                o[2 * k + h] = lo | (hi << 16);
-              }
-            // bf16 elements 16 pc .. 16 pc + 15: K chunk pc / 4, pieces 2 (pc % 4) and + 1
-            uint8_t* dst = q_s + (pc >> 2) * Q_CHUNK + r * 128;
-            const int d0 = 2 * (pc & 3), d1 = d0 + 1;
-            *reinterpret_cast<uint4*>(dst + ((d0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(dst + ((d1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the MMAs
-      } else if (lane == 0) {
-        raise_error(DSA_DEVERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-      __syncwarp();
-      if (lane == 0 && okq) mbar_arrive(qready);
-      // the item's key tiles
       for (int i = 0; i < ntiles; ++i, ++T) {
         const int s4 = T % S, c = T % CR;
         bool okt = (lane == 0) ? (mbar_wait(full0 + 8 * s4, (uint32_t)(T / S) & 1u, limit, abort_flag) &&
@@ -858,33 +848,25 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
           continue;
         }
         __syncwarp();
+        tc_fence_after();                           // the MMAs that read this tile's cells are done
         const uint8_t* f4 = f4_s + (size_t)s4 * F4_BYTES;
-        const uint32_t sw = *reinterpret_cast<const uint32_t*>(f4 + 8192 + ct * 4);
-        uint8_t* dst = k_s + (size_t)c * K_BYTES + ct * 128;
-        // the row's scale bytes decide, once, between the table and the exact decode; all
-        // 16 pieces are decoded before any is stored (a store between two table reads would
-        // keep the compiler from issuing the reads together)
-        auto convert = [&](auto decode) {
-          uint4 o[16];
+        const uint32_t* sc = reinterpret_cast<const uint32_t*>(f4 + 8192);
+        const uint32_t sw = sc[ct];
+        uint4 v[4];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {               // group g: elements 32 g .. 32 g + 31
-            const uint4 v = *reinterpret_cast<const uint4*>(f4 + ct * 64 + g * 16);
-            const uint32_t b = (sw >> (8 * g)) & 0xFFu;
-            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+        for (int g = 0; g < 4; ++g) v[g] = *reinterpret_cast<const uint4*>(f4 + ct * 64 + g * 16);
+        uint8_t* dst = k_s + (size_t)c * KT_BYTES + ct * 128;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) o[4 * g + w] = decode(words[w], b);   // elements 32 g + 8 w ..
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int pc = ((i >> 2) & 1) * 4 + (i & 3);   // piece within K chunk i / 8
-            *reinterpret_cast<uint4*>(dst + (i >> 3) * K_CHUNK + ((pc ^ (ct & 7)) << 4)) = o[i];
-          }
-        };
-        if (!e8m0_word_off_table(sw))
-          convert([&](uint32_t w, uint32_t b) { return decode8(w, b, lut); });
-        else
-          convert([](uint32_t w, uint32_t b) { return decode8_exact(w, b); });
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int g = 0; g < 4; ++g) {               // group g: codes 32 g .. 32 g + 31, pieces 2 g, 2 g + 1
+          const uint4 x = ((sw >> (8 * g)) & 0xFFu) == 0xFFu ? make_uint4(0u, 0u, 0u, 0u) : v[g];
+          *reinterpret_cast<uint4*>(dst + (((2 * g) ^ (ct & 7)) << 4)) = make_uint4(x.x, x.y, 0u, 0u);
+          *reinterpret_cast<uint4*>(dst + (((2 * g + 1) ^ (ct & 7)) << 4)) = make_uint4(x.z, x.w, 0u, 0u);
+        }
+        tmem_st4(tq + SFA_COL + 4u * (uint32_t)c, e8m0_ff_to_one(sc[lane]), e8m0_ff_to_one(sc[lane + 32]),
+                 e8m0_ff_to_one(sc[lane + 64]), e8m0_ff_to_one(sc[lane + 96]));
+        tmem_st_wait();
+        tc_fence_before();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // codes visible to the MMAs
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(cfull0 + 8 * c);
@@ -894,6 +876,8 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
       group_sync<128>(CBAR);
       if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tmemfree);           // no scale cell is written after this
   }
   // No CTA-wide barrier here: the warps leave as their roles end (warp 1 last frees
   // TMEM); shared memory stays valid until every thread of the CTA has exited.
