@@ -231,7 +231,7 @@ IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk) {
   const bool tk = topk > 0;
   pl.f4k = dt == DSA_E4M3_MXFP4K;
   pl.nq = qs.next_n == 1 ? 1 : (qs.next_n == 2 ? 2 : 4);
-  if (pl.f4k && pl.nq > 2) pl.nq = 2;                // FP4 keys: one epilogue group, <= 2 rows per item
+  if (pl.f4k && pl.nq > 2) pl.nq = 2;                // FP4 keys: <= 2 rows per item
   if (tk) {
     pl.pow2 = next_pow2(topk);
     // room for several tiles of inserts between cut-backs
@@ -270,9 +270,9 @@ IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk) {
   if (tk && (pl.cap < topk + 256 || pl.cap < pl.pow2)) pl.ok = false;
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap);
   if (pl.f4k) {
-    // one CTA per SM: one epilogue group, four converter warps, a deep FP4 ring and as
-    // many padded key tiles (2..4) as shared memory holds
-    pl.eg = 1;
+    // one CTA per SM: two epilogue groups taking the tiles in turn, four converter warps,
+    // a deep FP4 ring and as many padded key tiles (2..4) as shared memory holds
+    pl.eg = 2;
     pl.ctas_per_sm = 1;
     pl.stages = 8;
     pl.conv_slots = 4;

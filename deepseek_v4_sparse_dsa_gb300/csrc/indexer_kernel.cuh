@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
   // kF4K: E4M3 queries against mxfp4 keys, contracted by the block-scaled MMA: the key
   // codes in the padded E2M1 layout, their E8M0 scales in tensor memory, the E4M3 Q tile
   // as loaded with scale 1.
-  static_assert(!kF4K || (kFP8 && EG == 1), "FP4-key mode: E4M3 queries, one epilogue group");
+  static_assert(!kF4K || kFP8, "FP4-key mode: E4M3 queries");
   constexpr bool kMmaFP8 = kFP8 && !kF4K;          // E4M3 x E4M3 contraction
   constexpr bool kKeyScale = kFP8 && !kF4K;        // per-key fp32 scale (E4M3 keys)
   constexpr int N = NQ * 64;                       // MMA N: (query, head) rows
@@ -357,6 +357,9 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
       if (p.plan && mode == kPlanGroups) next = (int)atomicAdd(p.work, 1u);   // one item ahead
     }
     int tiles_issued = 0, items_issued = 0;
+    int s_run = 0;                                          // stage of the next tile (tiles_issued % S)
+    uint32_t ph_run = 0;                                    // its ring pass parity
+    const int bsl = (bs & (bs - 1)) == 0 ? __ffs(bs) - 1 : -1;   // log2(block size), or -1
     int last_issue[8];
     for (int s = 0; s < 8; ++s) last_issue[s] = -1;
     bool ok = true;
@@ -421,11 +424,13 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
       int win0 = -1;                                        // first page held in the window
       for (int i = 0; i < it.ntiles; ++i) {
         const int T = tiles_issued + i;
-        const int s = T % S;
-        const int j0 = it.ks + i * 128;
+        const int s = s_run;                                // T % S
+        const int j0 = it.ks + i * 128;                     // a multiple of 128
         const int jend = min(j0 + 128, ke);
+        int pg0 = 0, pg1 = 0;
         if (paged) {
-          const int pg0 = j0 / bs, pg1 = (jend - 1) / bs;
+          pg0 = bsl >= 0 ? j0 >> bsl : j0 / bs;
+          pg1 = bs >= 128 ? pg0 : (jend - 1) >> bsl;
           if (win0 < 0 || pg1 >= win0 + kPageWindow) {
             __syncwarp();
             win0 = pg0;
@@ -439,78 +444,84 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
             __syncwarp();
           }
         }
-        if (lane == 0) {
-          ok = mbar_wait(empty0 + 8 * s, ((uint32_t)(T / S) & 1u) ^ 1u, limit, abort_flag);
-          if (ok) {
-            const uint32_t stage = smem_u32(k_s + (size_t)s * K_BYTES);
-            const uint32_t fb = full0 + 8 * s;
+        // Block size < 128 (a power of two dividing 128): lane k resolves page pg0 + k of
+        // the tile (at most 16) while lane 0 waits for the stage, then issues its copies.
+        const bool small_pages = paged && bs < 128;
+        int64_t myblk = -1;
+        const bool mine = small_pages && pg0 + lane <= pg1;
+        if (mine) myblk = es->pages[pg0 + lane - win0];
+        if (lane == 0) ok = mbar_wait(empty0 + 8 * s, ph_run ^ 1u, limit, abort_flag);
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t stage = smem_u32(k_s + (size_t)s * K_BYTES);
+        const uint32_t fb = full0 + 8 * s;
+        const uint32_t f4 = kF4K ? smem_u32(f4_s + (size_t)s * F4_BYTES) : 0u;
+        if (small_pages) {
+          const bool good = mine && myblk >= 0 && myblk < p.num_blocks;
+          const uint32_t gm = __ballot_sync(0xFFFFFFFFu, good);
+          const uint32_t bm = __ballot_sync(0xFFFFFFFFu, mine && !good);
+          if (lane == 0) {
+            if (bm) raise_error(DSA_DEVERR_INDEX);
+            // nibble and E8M0 rows (kF4K), or the page's rows of every K chunk
+            const uint32_t per_page = kF4K ? (uint32_t)bs * 68u : (uint32_t)bs * 128u * KCH;
+            mbar_arrive_expect_tx(fb, (uint32_t)__popc(gm) * per_page);
+          }
+          __syncwarp();
+          if (good) {
+            const uint32_t at = (uint32_t)lane * (uint32_t)bs;     // the page's first row in the tile
+            const int64_t row = myblk * bs;
             if constexpr (kF4K) {
-              // nibble rows to the stage's front, E8M0 rows after them (plain bulk copies:
-              // 64 + 4 bytes per key; every source and size is a multiple of 16 bytes)
-              const uint32_t f4 = smem_u32(f4_s + (size_t)s * F4_BYTES);
-              if (!paged) {
-                const int rows = (int)max((int64_t)0, min((int64_t)128, p.num_rows - j0));
-                mbar_arrive_expect_tx(fb, (uint32_t)rows * 68u);
-                if (rows > 0) {
-                  bulk_load(f4, p.kv_fp4 + (size_t)j0 * 64, (uint32_t)rows * 64u, fb);
-                  bulk_load(f4 + 8192u, p.kv_e8m0 + (size_t)j0 * 4, (uint32_t)rows * 4u, fb);
-                }
-              } else {
-                const int pg0 = j0 / bs, pg1 = bs >= 128 ? pg0 : (jend - 1) / bs;
-                const int span = bs >= 128 ? 128 : bs;          // rows copied per page
-                uint32_t bytes = 0;
-                for (int pg = pg0; pg <= pg1; ++pg) {
-                  const int64_t blk = es->pages[pg - win0];
-                  if (blk >= 0 && blk < p.num_blocks) bytes += (uint32_t)span * 68u;
-                  else raise_error(DSA_DEVERR_INDEX);
-                }
-                mbar_arrive_expect_tx(fb, bytes);
-                for (int pg = pg0; pg <= pg1; ++pg) {
-                  const int64_t blk = es->pages[pg - win0];
-                  if (blk < 0 || blk >= p.num_blocks) continue;
-                  const int64_t row = blk * bs + (bs >= 128 ? (j0 % bs) : 0);
-                  const uint32_t at = (uint32_t)(pg - pg0) * (uint32_t)span;
-                  bulk_load(f4 + at * 64u, p.kv_fp4 + (size_t)row * 64, (uint32_t)span * 64u, fb);
-                  bulk_load(f4 + 8192u + at * 4u, p.kv_e8m0 + (size_t)row * 4, (uint32_t)span * 4u, fb);
-                }
-              }
-            } else if (!paged) {
-              mbar_arrive_expect_tx(fb, K_BYTES);
+              // plain bulk copies: 64 + 4 bytes per key, every source and size a multiple of 16 bytes
+              bulk_load(f4 + at * 64u, p.kv_fp4 + (size_t)row * 64, (uint32_t)bs * 64u, fb);
+              bulk_load(f4 + 8192u + at * 4u, p.kv_e8m0 + (size_t)row * 4, (uint32_t)bs * 4u, fb);
+            } else {
               for (int kc = 0; kc < KCH; ++kc)
-                tma_load_2d(stage + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), j0);
-            } else if (bs >= 128) {
-              const int64_t blk = es->pages[j0 / bs - win0];
+                tma_load_2d(stage + at * 128u + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), (int32_t)row);
+            }
+          }
+        } else if (lane == 0) {
+          if constexpr (kF4K) {
+            if (!paged) {
+              const int rows = (int)max((int64_t)0, min((int64_t)128, p.num_rows - j0));
+              mbar_arrive_expect_tx(fb, (uint32_t)rows * 68u);
+              if (rows > 0) {
+                bulk_load(f4, p.kv_fp4 + (size_t)j0 * 64, (uint32_t)rows * 64u, fb);
+                bulk_load(f4 + 8192u, p.kv_e8m0 + (size_t)j0 * 4, (uint32_t)rows * 4u, fb);
+              }
+            } else {                                        // one page of >= 128 rows
+              const int64_t blk = es->pages[pg0 - win0];
               if (blk >= 0 && blk < p.num_blocks) {
-                mbar_arrive_expect_tx(fb, K_BYTES);
-                const int32_t row = (int32_t)(blk * bs + (j0 % bs));
-                for (int kc = 0; kc < KCH; ++kc)
-                  tma_load_2d(stage + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), row);
+                mbar_arrive_expect_tx(fb, 128u * 68u);
+                const int64_t row = blk * bs + (j0 % bs);
+                bulk_load(f4, p.kv_fp4 + (size_t)row * 64, 128u * 64u, fb);
+                bulk_load(f4 + 8192u, p.kv_e8m0 + (size_t)row * 4, 128u * 4u, fb);
               } else {
                 raise_error(DSA_DEVERR_INDEX);
                 mbar_arrive_expect_tx(fb, 0);
               }
-            } else {
-              const int pg0 = j0 / bs, pg1 = (jend - 1) / bs;
-              uint32_t bytes = 0;
-              for (int pg = pg0; pg <= pg1; ++pg) {
-                const int64_t blk = es->pages[pg - win0];
-                if (blk >= 0 && blk < p.num_blocks) bytes += (uint32_t)bs * 128u * KCH;
-                else raise_error(DSA_DEVERR_INDEX);
-              }
-              mbar_arrive_expect_tx(fb, bytes);
-              for (int pg = pg0; pg <= pg1; ++pg) {
-                const int64_t blk = es->pages[pg - win0];
-                if (blk < 0 || blk >= p.num_blocks) continue;
-                const uint32_t dst = stage + (uint32_t)(pg - pg0) * (uint32_t)bs * 128u;
-                for (int kc = 0; kc < KCH; ++kc)
-                  tma_load_2d(dst + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), (int32_t)(blk * bs));
-              }
             }
-            last_issue[s] = T;
+          } else if (!paged) {
+            mbar_arrive_expect_tx(fb, K_BYTES);
+            for (int kc = 0; kc < KCH; ++kc)
+              tma_load_2d(stage + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), j0);
+          } else {                                          // one page of >= 128 rows
+            const int64_t blk = es->pages[pg0 - win0];
+            if (blk >= 0 && blk < p.num_blocks) {
+              mbar_arrive_expect_tx(fb, K_BYTES);
+              const int32_t row = (int32_t)(blk * bs + (j0 % bs));
+              for (int kc = 0; kc < KCH; ++kc)
+                tma_load_2d(stage + kc * K_CHUNK, &tm_k, fb, kc * (128 / ELT), row);
+            } else {
+              raise_error(DSA_DEVERR_INDEX);
+              mbar_arrive_expect_tx(fb, 0);
+            }
           }
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+        if (lane == 0) last_issue[s] = T;
+        if (++s_run == S) {
+          s_run = 0;
+          ph_run ^= 1u;
+        }
       }
       if (!ok) break;
       tiles_issued += it.ntiles;
@@ -913,8 +924,8 @@ template <bool kFP8, bool kTopk>
 static cudaError_t dispatch_nq(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& prm,
                                const IndexerPlan& pl, int grid, cudaStream_t st) {
   if constexpr (kFP8) {
-    if (pl.f4k) return pl.nq == 1 ? launch_one<true, 1, kTopk, 1, true>(mq, mk, prm, pl, grid, st)
-                                  : launch_one<true, 2, kTopk, 1, true>(mq, mk, prm, pl, grid, st);
+    if (pl.f4k) return pl.nq == 1 ? launch_one<true, 1, kTopk, 2, true>(mq, mk, prm, pl, grid, st)
+                                  : launch_one<true, 2, kTopk, 2, true>(mq, mk, prm, pl, grid, st);
   }
   switch (pl.nq * 2 + pl.eg) {
     case 3: return launch_one<kFP8, 1, kTopk, 1>(mq, mk, prm, pl, grid, st);
