@@ -108,6 +108,90 @@ __global__ void __launch_bounds__(kRowNT) topk_rows_kernel(const float* __restri
   }
 }
 
+// Writes every selected key out[0, m) (m <= 4 * NT, distinct unless the lists were stale)
+// at its rank, the number of larger keys.  The keys are binned by value image into kCutBins
+// linear bins over their range (as in a cut-back); a key's rank is the count in the bins
+// above its own plus the larger keys of its own bin, found by scanning that bin: a few
+// keys on average, all m at worst (then it costs what counting against every key costs).
+// Scratch: tmp (m slots), start and bins (kCutBins words each), red (2 * NT / 32 words).
+template <int NT>
+__device__ void merge_rank_binned(const uint64_t* out, int m, uint64_t* tmp, uint32_t* start, uint32_t* bins,
+                                  uint32_t* red, int tid, int topk, int32_t* row_idx, float* row_val) {
+  constexpr int NW = NT / 32, KPT = 4;
+  static_assert(kCutBins == NT, "one bin per thread in the scan");
+  const int lane = tid & 31, w = tid >> 5;
+  uint64_t key[KPT];
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+  for (int u = 0; u < KPT; ++u) {
+    const int e = tid + u * NT;
+    key[u] = e < m ? out[e] : 0ull;
+    if (key[u]) {
+      lo = min(lo, (uint32_t)(key[u] >> 32));
+      hi = max(hi, (uint32_t)(key[u] >> 32));
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+  }
+  if (lane == 0) {
+    red[w] = lo;
+    red[NW + w] = hi;
+  }
+  bins[tid] = 0u;
+  group_sync<NT>();
+  lo = 0xFFFFFFFFu;
+  hi = 0u;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    lo = min(lo, red[i]);
+    hi = max(hi, red[NW + i]);
+  }
+  const uint64_t span = hi >= lo ? (uint64_t)(hi - lo) + 1u : 1u;
+  const uint32_t mul = (uint32_t)min(((uint64_t)kCutBins << 32) / span, (uint64_t)0xFFFFFFFFu);
+  uint32_t bk[KPT];
+#pragma unroll
+  for (int u = 0; u < KPT; ++u) {
+    bk[u] = key[u] ? cut_bin((uint32_t)(key[u] >> 32), lo, mul) : 0u;
+    if (key[u]) atomicAdd(&bins[bk[u]], 1u);
+  }
+  group_sync<NT>();
+  // start[b]: the keys in the bins above b (thread tid scans bin kCutBins - 1 - tid)
+  const int b = kCutBins - 1 - tid;
+  const uint32_t c = bins[b];
+  uint32_t incl = c;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  group_sync<NT>();                              // red is rewritten
+  if (lane == 31) red[w] = incl;
+  group_sync<NT>();
+  uint32_t before = 0;
+  for (int i = 0; i < w; ++i) before += red[i];
+  start[b] = before + incl - c;
+  bins[b] = before + incl - c;                   // running slot of the scatter
+  group_sync<NT>();
+#pragma unroll
+  for (int u = 0; u < KPT; ++u)
+    if (key[u]) tmp[atomicAdd(&bins[bk[u]], 1u)] = key[u];
+  group_sync<NT>();
+#pragma unroll
+  for (int u = 0; u < KPT; ++u) {
+    if (!key[u]) continue;
+    const uint32_t s0 = start[bk[u]], s1 = bins[bk[u]];
+    uint32_t r = s0;
+    for (uint32_t j = s0; j < s1; ++j) r += tmp[j] > key[u] ? 1u : 0u;
+    if (r >= (uint32_t)topk) {                  // only if the lists held equal keys (stale lists
+      raise_error(DSA_DEVERR_OVERFLOW | (33u << 8));   // after an abandoned call): never write
+      continue;                                 // past the row
+    }
+    row_idx[r] = index_of_key(key[u]);
+    if (row_val) row_val[r] = value_of_key(key[u]);
+  }
+}
+
 constexpr int kMergeNT = 512;       // merge: threads per row
 constexpr int kMergeKeys = 24576;   // merge: candidates held in shared memory at once (two halves)
 
@@ -239,25 +323,9 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
   }
   group_sync<NT>();
   const int m = min((int)sh.cnt, P);
-  if (tid == 0 && (m & 1)) out[m] = 0ull;      // pairs below: a zero key ranks below all
-  group_sync<NT>();
   // 4. each selected key goes to its rank; the rest of the row is padding
-  const ulonglong2* out2 = reinterpret_cast<const ulonglong2*>(out);
-  const int pairs = (m + 1) >> 1;
-  for (int e = tid; e < m; e += NT) {
-    const uint64_t key = out[e];
-    int r = 0;
-    for (int f = 0; f < pairs; ++f) {
-      const ulonglong2 x = out2[f];
-      r += (x.x > key) + (x.y > key);
-    }
-    if (r >= topk) {                            // only if the lists held equal keys (stale lists
-      raise_error(DSA_DEVERR_OVERFLOW | (33u << 8));   // after an abandoned call): never write
-      continue;                                 // past the row
-    }
-    out_idx[t * topk + r] = index_of_key(key);
-    if (out_val) out_val[t * topk + r] = value_of_key(key);
-  }
+  merge_rank_binned<NT>(out, m, cur, reinterpret_cast<uint32_t*>(alt), mbins, reinterpret_cast<uint32_t*>(s_floor),
+                        tid, topk, out_idx + t * topk, out_val ? out_val + t * topk : nullptr);
   for (int s = m + tid; s < topk; s += NT) {
     out_idx[t * topk + s] = -1;
     if (out_val) out_val[t * topk + s] = -INFINITY;
