@@ -107,6 +107,15 @@ def test_fp8_paged_mtp():
     check_case(wl)
 
 
+def test_split_rows_with_tied_scores():
+    # every cached key equal: all of a row's scores tie, so its top-k follows the index.
+    # The merge of the split rows then finds all candidates in one value bin: the exact
+    # fallback where they outnumber its limit, the in-bin tie rule where they do not.
+    wl = parity.make_case(77, [20000, 9000, 3000, 700], next_n=1, block_size=64, topk=512)
+    wl.k_data[:] = wl.k_data[0]
+    check_case(wl, jaccard=False)
+
+
 def test_topk_ties_and_signed_zero():
     """Standalone top-k on crafted logits: heavy ties, -0.0 vs +0.0, -inf holes, rows with
     fewer candidates than k, all -inf rows."""
