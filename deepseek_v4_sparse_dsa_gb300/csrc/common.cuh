@@ -786,6 +786,123 @@ __device__ void engine_compact(uint64_t* buf, uint32_t* cnt, int n, uint64_t thr
   engine_scatter<NT, MAXPER, false>(buf, cnt, keep, thr, 0u, 0u, 0u, sc, tid, bar);
 }
 
+// The top k of a candidate set cand[0, n) (distinct nonzero keys; zero slots ignored), in
+// rank order, by value bins: the candidates are binned by value image (kCutBins linear bins
+// over their range, as in a cut-back); one scan from the top finds the bin b* that holds the
+// k-th largest (the lowest bin when there are fewer than k); the candidates of the bins at
+// or above b* are gathered in bin order, and each ranks as the count in the bins above its
+// own plus the larger keys of its own bin.  Key r goes to row_idx[r] / row_val[r] (nothing
+// is written when row_idx is null); *m_out = min(k, candidates).  Returns false, having
+// written nothing, when bin b* holds more than max_bin candidates (values crowded together):
+// the caller then selects exactly.  Scratch: tmp (k + max_bin slots), start and bins
+// (kCutBins words each), red (2 * NT / 32 words), pick (2 words).  Equal keys (possible only
+// in stale lists) raise DSA_DEVERR_OVERFLOW.
+template <int NT>
+__device__ bool engine_topk_binned(const uint64_t* cand, int n, int k, uint64_t* tmp, uint32_t max_bin,
+                                   uint32_t* start, uint32_t* bins, uint32_t* red, uint32_t* pick, int tid,
+                                   int32_t* row_idx, float* row_val, int* m_out, int bar = 1) {
+  constexpr int NW = NT / 32;
+  constexpr int BPT = kCutBins / NT;               // bins per thread in the scan
+  static_assert(kCutBins % NT == 0 && NW <= 16, "group size");
+  const int lane = tid & 31, w = tid >> 5;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int e = tid; e < n; e += NT) {
+    const uint64_t key = cand[e];
+    if (key) {
+      lo = min(lo, (uint32_t)(key >> 32));
+      hi = max(hi, (uint32_t)(key >> 32));
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+  }
+  if (lane == 0) {
+    red[w] = lo;
+    red[NW + w] = hi;
+  }
+  for (int i = tid; i < kCutBins; i += NT) bins[i] = 0u;
+  group_sync<NT>(bar);
+  lo = 0xFFFFFFFFu;
+  hi = 0u;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    lo = min(lo, red[i]);
+    hi = max(hi, red[NW + i]);
+  }
+  const uint64_t span = hi >= lo ? (uint64_t)(hi - lo) + 1u : 1u;
+  const uint32_t mul = (uint32_t)min(((uint64_t)kCutBins << 32) / span, (uint64_t)0xFFFFFFFFu);
+  for (int e = tid; e < n; e += NT) {
+    const uint64_t key = cand[e];
+    if (key) atomicAdd(&bins[cut_bin((uint32_t)(key >> 32), lo, mul)], 1u);
+  }
+  group_sync<NT>(bar);
+  // start[b]: the candidates in the bins above b; thread tid scans bins
+  // kCutBins - 1 - tid * BPT - i, i < BPT (top down)
+  uint32_t c[BPT], sum = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    c[i] = bins[kCutBins - 1 - tid * BPT - i];
+    sum += c[i];
+  }
+  uint32_t incl = sum;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  group_sync<NT>(bar);                             // red is rewritten
+  if (lane == 31) red[w] = incl;
+  group_sync<NT>(bar);
+  uint32_t st = incl - sum;
+  for (int i = 0; i < w; ++i) st += red[i];
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    const int b = kCutBins - 1 - tid * BPT - i;
+    start[b] = st;
+    bins[b] = st;                                  // running slot of the gather
+    if (st < (uint32_t)k && (uint32_t)k <= st + c[i]) {   // b* (one bin at most)
+      pick[0] = (uint32_t)b;
+      pick[1] = st + c[i];
+    }
+    if (b == 0 && st + c[i] < (uint32_t)k) {      // fewer than k candidates: every bin
+      pick[0] = 0u;
+      pick[1] = st + c[i];
+    }
+    st += c[i];
+  }
+  group_sync<NT>(bar);
+  const uint32_t bstar = pick[0], total = pick[1];   // total: the candidates in bins >= b*
+  const bool crowded = total - start[bstar] > max_bin;
+  group_sync<NT>(bar);                             // pick and start read before any reuse
+  if (crowded) return false;
+  for (int e = tid; e < n; e += NT) {
+    const uint64_t key = cand[e];
+    if (!key) continue;
+    const uint32_t kb = cut_bin((uint32_t)(key >> 32), lo, mul);
+    if (kb >= bstar) tmp[atomicAdd(&bins[kb], 1u)] = key;
+  }
+  group_sync<NT>(bar);
+  for (uint32_t q = (uint32_t)tid; q < total; q += NT) {
+    const uint64_t key = tmp[q];
+    const uint32_t kb = cut_bin((uint32_t)(key >> 32), lo, mul);
+    const uint32_t s1 = bins[kb];
+    uint32_t r = start[kb], eq = 0;
+    for (uint32_t j = start[kb]; j < s1; ++j) {
+      const uint64_t x = tmp[j];
+      r += x > key ? 1u : 0u;
+      eq += x == key ? 1u : 0u;
+    }
+    if (eq > 1) raise_error(DSA_DEVERR_OVERFLOW | (33u << 8));
+    if (r < (uint32_t)k && row_idx != nullptr) {
+      row_idx[r] = index_of_key(key);
+      if (row_val) row_val[r] = value_of_key(key);
+    }
+  }
+  *m_out = (int)min(total, (uint32_t)k);
+  group_sync<NT>(bar);                             // tmp, start and bins free again
+  return true;
+}
+
 // Copies the keys >= thr of src[0, n) to the front of dst (capacity dcap); *cnt becomes
 // their number.
 template <int NT>

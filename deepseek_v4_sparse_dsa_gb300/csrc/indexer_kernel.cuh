@@ -80,6 +80,7 @@ struct IndexerParams {
 };
 
 constexpr int kMaxPer = 10;        // candidate capacity per query <= 256 * kMaxPer
+constexpr uint32_t kItemMaxBin = 512;   // binned top k of a whole group: largest bin gathered
 
 struct ItemInfo {
   int32_t valid, b, g, L, nreal, vis_max;
@@ -283,6 +284,10 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
   const int NBARS = (2 * S + 16 + (kF4K ? 2 * CR : 0) + 1) & ~1;   // even: es stays 16-byte aligned
   EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + NBARS);
   uint64_t* ebuf = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(es) + (sizeof(EpiSmem<NQ>) + 15) / 16 * 16);
+  // top-k mode: the candidate buffers [NQ][cap], then the gather buffer of the binned top k
+  // (pow2 + kItemMaxBin keys) and its bin starts (kCutBins words)
+  uint64_t* tbuf = ebuf + (size_t)NQ * p.cap;
+  uint32_t* tstart = reinterpret_cast<uint32_t*>(tbuf + p.pow2 + kItemMaxBin);
 
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
   const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 4);
@@ -755,63 +760,49 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
         for (int q = 0; q < it.nreal; ++q)
           for (int jj = f0 + et; jj < f1; jj += NT) p.logits[(int64_t)(it.t0 + q) * p.ld + jj] = -INFINITY;
       } else if (!it.split) {
-        // the whole group in one item: cut each row's candidates back to at most SN
-        // (histogram first, the exact radix select only if that is not enough), then sort
-        // each row and write its first k
+        // the whole group in one item: each row's top k by value bins (the whole epilogue,
+        // one row after another; one warp per row sorting in registers took ~94 K cycles per
+        // four-row item); a row whose values crowd into one bin is cut back to SN
+        // candidates (histogram, then the exact select) and sorted by the bitonic network
         const int P = p.pow2;
         const int SN = P <= 128 ? 256 : (P <= 512 ? 2 * P : P);   // keys sorted per row (<= cap)
         group_sync<NT>();
 #pragma unroll 1
         for (int q = 0; q < NQ; ++q) {
-          uint32_t cn = min(es->cnt[q], (uint32_t)cap);
           uint64_t* buf = ebuf + (size_t)q * cap;
-          if (cn > (uint32_t)SN) {
-            engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, (uint32_t)SN, es->bins, &es->esc, et);
-            cn = es->cnt[q];
-          }
-          if (cn > (uint32_t)SN) {
-            const uint64_t thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
-            engine_compact<NT, MAXPER>(buf, &es->cnt[q], (int)cn, thr, &es->esc, et);
-          }
-        }
-        group_sync<NT>();
-        if constexpr (NQ >= 4) {
-          // four rows: one warp per row sorts its keys in registers (faster here than the
-          // network below: prefill 3.75 vs 3.80 ms)
-          for (int q = ew; q < NQ; q += 4 * EG) {
-            uint64_t* buf = ebuf + (size_t)q * cap;
-            const int cn = min((int)es->cnt[q], cap);
-            const int64_t t = it.t0 + q;
-            const bool real = q < it.nreal;
-            int32_t* oi = p.out_idx + t * p.topk;
-            float* ov = p.out_val ? p.out_val + t * p.topk : nullptr;
-            if (SN == 256) rank_row<8>(buf, cn, p.topk, real, oi, ov);
-            else if (SN == 512) rank_row<16>(buf, cn, p.topk, real, oi, ov);
-            else if (SN == 1024) rank_row<32>(buf, cn, p.topk, real, oi, ov);
-            else rank_row_smem(buf, cn, P, p.topk, real, oi, ov);
-          }
-        } else {
-          // one or two rows: the whole epilogue sorts every row's SN slots at once (a
-          // bitonic network in shared memory, one barrier per step); one warp per row left
-          // the other warps idle for tens of microseconds per item (FP4-key Flash decode
-          // 0.238 -> 0.150 ms)
-          for (int q = 0; q < NQ; ++q) {            // empty slots rank below every key
-            uint64_t* buf = ebuf + (size_t)q * cap;
-            for (int e = min((int)es->cnt[q], SN) + et; e < SN; e += NT) buf[e] = 0ull;
-          }
-          group_sync<NT>();
-          engine_sort<NT>(ebuf, cap, NQ, SN, et);
-          for (int q = 0; q < it.nreal; ++q) {
-            const uint64_t* buf = ebuf + (size_t)q * cap;
-            const int64_t t = it.t0 + q;
-            int32_t* oi = p.out_idx + t * p.topk;
-            float* ov = p.out_val ? p.out_val + t * p.topk : nullptr;
-            for (int r = et; r < p.topk; r += NT) {
-              const uint64_t key = buf[r];
-              oi[r] = key ? index_of_key(key) : -1;
-              if (ov) ov[r] = key ? value_of_key(key) : -INFINITY;
+          const bool real = q < it.nreal;
+          const int64_t t = it.t0 + q;
+          int32_t* oi = real ? p.out_idx + t * p.topk : nullptr;
+          float* ov = (real && p.out_val) ? p.out_val + t * p.topk : nullptr;
+          int m = 0;
+          if (!engine_topk_binned<NT>(buf, (int)min(es->cnt[q], (uint32_t)cap), p.topk, tbuf, kItemMaxBin, tstart,
+                                      es->bins, es->esc.hist, es->esc.pick, et, oi, ov, &m)) {
+            uint32_t cn = min(es->cnt[q], (uint32_t)cap);
+            if (cn > (uint32_t)SN) {
+              engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, (uint32_t)SN, es->bins, &es->esc, et);
+              cn = min(es->cnt[q], (uint32_t)cap);
             }
+            if (cn > (uint32_t)SN) {
+              const uint64_t thr = engine_select<NT>(buf, (int)cn, p.topk, &es->esc, et);
+              engine_compact<NT, MAXPER>(buf, &es->cnt[q], (int)cn, thr, &es->esc, et);
+            }
+            group_sync<NT>();
+            for (int e = min((int)es->cnt[q], SN) + et; e < SN; e += NT) buf[e] = 0ull;   // rank below all
+            group_sync<NT>();
+            engine_sort<NT>(buf, cap, 1, SN, et);
+            if (real)
+              for (int r = et; r < p.topk; r += NT) {
+                const uint64_t key = buf[r];
+                oi[r] = key ? index_of_key(key) : -1;
+                if (ov) ov[r] = key ? value_of_key(key) : -INFINITY;
+              }
+            m = p.topk;
           }
+          if (real)
+            for (int r = m + et; r < p.topk; r += NT) {   // fewer than k candidates
+              oi[r] = -1;
+              if (ov) ov[r] = -INFINITY;
+            }
         }
       } else {
         // a piece of a split group: its candidates as they stand (unsorted, at least

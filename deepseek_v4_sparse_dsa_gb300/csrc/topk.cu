@@ -192,110 +192,6 @@ __device__ void merge_rank_binned(const uint64_t* out, int m, uint64_t* tmp, uin
   }
 }
 
-// The row's top-k in rank order straight from its candidates cur[0, n): the candidates are
-// binned by value image (kCutBins linear bins over their range); one scan from the top
-// finds the bin b* that holds the k-th largest (the lowest bin when there are fewer than
-// k); the candidates in bins >= b* are gathered in bin order, and each ranks as the count
-// in the bins above its own plus the larger keys of its own bin.  Returns false, having
-// written nothing, when bin b* holds more than kMaxBin candidates (values crowded together;
-// the caller then selects exactly); *m_out = the number of keys written.  Scratch: tmp
-// (topk + kMaxBin slots), start and bins (kCutBins words each), red (2 * NT / 32 words).
-template <int NT>
-__device__ bool merge_select_binned(const uint64_t* cur, int n, uint64_t* tmp, uint32_t* start, uint32_t* bins,
-                                    uint32_t* red, uint32_t* pick, int tid, int topk, int32_t* row_idx,
-                                    float* row_val, int* m_out) {
-  constexpr int NW = NT / 32;
-  constexpr uint32_t kMaxBin = 2048;
-  static_assert(kCutBins == NT, "one bin per thread in the scan");
-  const int lane = tid & 31, w = tid >> 5;
-  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-  for (int e = tid; e < n; e += NT) {
-    const uint64_t key = cur[e];
-    if (key) {
-      lo = min(lo, (uint32_t)(key >> 32));
-      hi = max(hi, (uint32_t)(key >> 32));
-    }
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
-  }
-  if (lane == 0) {
-    red[w] = lo;
-    red[NW + w] = hi;
-  }
-  bins[tid] = 0u;
-  group_sync<NT>();
-  lo = 0xFFFFFFFFu;
-  hi = 0u;
-#pragma unroll
-  for (int i = 0; i < NW; ++i) {
-    lo = min(lo, red[i]);
-    hi = max(hi, red[NW + i]);
-  }
-  const uint64_t span = hi >= lo ? (uint64_t)(hi - lo) + 1u : 1u;
-  const uint32_t mul = (uint32_t)min(((uint64_t)kCutBins << 32) / span, (uint64_t)0xFFFFFFFFu);
-  for (int e = tid; e < n; e += NT) {
-    const uint64_t key = cur[e];
-    if (key) atomicAdd(&bins[cut_bin((uint32_t)(key >> 32), lo, mul)], 1u);
-  }
-  group_sync<NT>();
-  // start[b]: the candidates in the bins above b (thread tid scans bin kCutBins - 1 - tid)
-  const int b = kCutBins - 1 - tid;
-  const uint32_t c = bins[b];
-  uint32_t incl = c;
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  group_sync<NT>();                              // red is rewritten
-  if (lane == 31) red[w] = incl;
-  group_sync<NT>();
-  uint32_t before = 0;
-  for (int i = 0; i < w; ++i) before += red[i];
-  const uint32_t st = before + incl - c;
-  start[b] = st;
-  bins[b] = st;                                  // running slot of the gather
-  if (st < (uint32_t)topk && (uint32_t)topk <= st + c) {   // b* (at most one thread)
-    pick[0] = (uint32_t)b;
-    pick[1] = st + c;
-  }
-  if (b == 0 && st + c < (uint32_t)topk) {      // fewer than k candidates: every bin
-    pick[0] = 0u;
-    pick[1] = st + c;
-  }
-  group_sync<NT>();
-  const uint32_t bstar = pick[0], total = pick[1];   // total: the candidates in bins >= b*
-  const bool crowded = total - start[bstar] > kMaxBin;
-  group_sync<NT>();                              // pick is read before the caller reuses it
-  if (crowded) return false;
-  for (int e = tid; e < n; e += NT) {
-    const uint64_t key = cur[e];
-    if (!key) continue;
-    const uint32_t kb = cut_bin((uint32_t)(key >> 32), lo, mul);
-    if (kb >= bstar) tmp[atomicAdd(&bins[kb], 1u)] = key;
-  }
-  group_sync<NT>();
-  for (uint32_t q = (uint32_t)tid; q < total; q += NT) {
-    const uint64_t key = tmp[q];
-    const uint32_t kb = cut_bin((uint32_t)(key >> 32), lo, mul);
-    const uint32_t s1 = bins[kb];
-    uint32_t r = start[kb], eq = 0;
-    for (uint32_t j = start[kb]; j < s1; ++j) {
-      const uint64_t x = tmp[j];
-      r += x > key ? 1u : 0u;
-      eq += x == key ? 1u : 0u;
-    }
-    if (eq > 1) raise_error(DSA_DEVERR_OVERFLOW | (33u << 8));   // equal keys: stale lists
-    if (r < (uint32_t)topk) {
-      row_idx[r] = index_of_key(key);
-      if (row_val) row_val[r] = value_of_key(key);
-    }
-  }
-  *m_out = (int)min(total, (uint32_t)topk);
-  return true;
-}
-
 constexpr int kMergeNT = 512;       // merge: threads per row
 constexpr int kMergeKeys = 24576;   // merge: candidates held in shared memory at once (two halves)
 
@@ -416,8 +312,8 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
   int32_t* row_idx = out_idx + t * topk;
   float* row_val = out_val ? out_val + t * topk : nullptr;
   int m = 0;
-  if (!merge_select_binned<NT>(cur, (int)n, alt, reinterpret_cast<uint32_t*>(alt + 8192), mbins,
-                               reinterpret_cast<uint32_t*>(s_floor), sh.esc.pick, tid, topk, row_idx, row_val, &m)) {
+  if (!engine_topk_binned<NT>(cur, (int)n, topk, alt, 2048u, reinterpret_cast<uint32_t*>(alt + 8192), mbins,
+                              reinterpret_cast<uint32_t*>(s_floor), sh.esc.pick, tid, row_idx, row_val, &m)) {
     if (n > (uint32_t)topk) {
       engine_cut_approx<NT, kHalf / NT>(cur, &sh.cnt, (int)n, topk, n, mbins, &sh.esc, tid);
       n = min(sh.cnt, (uint32_t)kHalf);
