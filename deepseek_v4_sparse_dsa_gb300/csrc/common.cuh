@@ -942,27 +942,6 @@ __device__ void engine_sort(uint64_t* buf, int stride, int nlist, int P, int tid
   }
 }
 
-// As engine_sort for one list, run by a single warp (no block barrier): sorts the P
-// (power of two) keys at buf in descending order.
-__device__ __forceinline__ void warp_sort(uint64_t* buf, int P) {
-  const int lane = threadIdx.x & 31;
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int half = size >> 1; half > 0; half >>= 1) {
-      for (int t = lane; t < (P >> 1); t += 32) {
-        const int i = 2 * t - (t & (half - 1));
-        const int j = i + half;
-        const uint64_t x = buf[i], y = buf[j];
-        const bool desc = (i & size) == 0;
-        if ((x < y) == desc) {
-          buf[i] = y;
-          buf[j] = x;
-        }
-      }
-      __syncwarp();
-    }
-  }
-}
-
 // Sorts 32 * KPL keys held by one warp in registers in descending order; element
 // e = r * 32 + lane is x[r] of that lane.  Same bitonic network as engine_sort: pairs
 // closer than 32 exchange through shuffles, the others within a thread.
@@ -1091,46 +1070,6 @@ __device__ __forceinline__ uint4 decode8_exact(uint32_t w, uint32_t b) {
     o[k] = e2m1_bf16_general(byte & 0xFu, (int)b) | (e2m1_bf16_general(byte >> 4, (int)b) << 16);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// One warp: sorts the cn (<= 32 * KPL) keys at buf in registers and writes the first
-// k of them as the row's indices (and values), -1 / -inf past the candidates.
-template <int KPL>
-__device__ __forceinline__ void rank_row(const uint64_t* buf, int cn, int k, bool real, int32_t* out_idx,
-                                         float* out_val) {
-  const int lane = threadIdx.x & 31;
-  uint64_t x[KPL];
-#pragma unroll
-  for (int r = 0; r < KPL; ++r) {
-    const int e = r * 32 + lane;
-    x[r] = e < cn ? buf[e] : 0ull;
-  }
-  warp_sort_regs<KPL>(x);
-  if (!real) return;
-#pragma unroll
-  for (int r = 0; r < KPL; ++r) {
-    const int s = r * 32 + lane;
-    if (s < k) {
-      out_idx[s] = x[r] ? index_of_key(x[r]) : -1;
-      if (out_val) out_val[s] = x[r] ? value_of_key(x[r]) : -INFINITY;
-    }
-  }
-}
-
-// As rank_row for rows of more than 1024 keys: zero-pads buf to P, sorts it in shared
-// memory with one warp.
-__device__ __forceinline__ void rank_row_smem(uint64_t* buf, int cn, int P, int k, bool real, int32_t* out_idx,
-                                              float* out_val) {
-  const int lane = threadIdx.x & 31;
-  for (int e = cn + lane; e < P; e += 32) buf[e] = 0ull;
-  __syncwarp();
-  warp_sort(buf, P);
-  if (!real) return;
-  for (int s = lane; s < k; s += 32) {
-    const uint64_t key = buf[s];
-    out_idx[s] = key ? index_of_key(key) : -1;
-    if (out_val) out_val[s] = key ? value_of_key(key) : -INFINITY;
-  }
 }
 
 __host__ __device__ constexpr int next_pow2(int x) {
