@@ -199,27 +199,29 @@ constexpr size_t kSmemLimit = 232448;   // max dynamic shared memory per CTA (22
 constexpr size_t kSmemHalf = 115712;    // two CTAs per SM (228 KB per SM, 1 KB reserved per CTA)
 constexpr int64_t kSplitUnits = 1216;   // logits mode: fewer query groups than this: split key chunks
 
-size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap, int pow2) {
+size_t smem_bytes(bool fp8, int nq, int stages, bool topk, int cap, int pow2, bool binned = false) {
   const size_t elt = fp8 ? 1 : 2;
   size_t s = 1024;                                    // alignment slack
   s += (size_t)nq * 64 * 128 * elt;                  // Q tile
   s += (size_t)stages * 128 * 128 * elt;             // key ring
   s += (size_t)(2 * stages + 16) * 8;                // barriers
   s += sizeof(EpiSmem<4>) + 16;
-  if (topk) s += (size_t)nq * cap * 8 + (size_t)(pow2 + kItemMaxBin) * 8 + kCutBins * 4;   // candidates, binned top k
+  if (topk) s += (size_t)nq * cap * 8;                                     // candidate buffers
+  if (topk && binned) s += (size_t)(pow2 + kItemMaxBin) * 8 + kCutBins * 4;   // binned top k
   return s;
 }
 
 // FP4-key mode: `conv` padded E2M1 key tiles of 128 x 128 bytes, the E4M3 Q tile,
 // `stages` FP4 stages of 128 x (64 + 4) bytes.
-size_t smem_bytes_f4k(int nq, int stages, int conv, bool topk, int cap, int pow2) {
+size_t smem_bytes_f4k(int nq, int stages, int conv, bool topk, int cap, int pow2, bool binned = false) {
   size_t s = 1024;
   s += (size_t)conv * 128 * 128;                     // padded key tiles
   s += (size_t)nq * 64 * 128;                        // E4M3 Q tile
   s += (size_t)stages * 128 * 68;                    // FP4 stages
   s += (size_t)((2 * stages + 16 + 2 * conv + 1) & ~1) * 8;   // barriers (an even count)
   s += sizeof(EpiSmem<4>) + 16;
-  if (topk) s += (size_t)nq * cap * 8 + (size_t)(pow2 + kItemMaxBin) * 8 + kCutBins * 4;   // candidates, binned top k
+  if (topk) s += (size_t)nq * cap * 8;                                     // candidate buffers
+  if (topk && binned) s += (size_t)(pow2 + kItemMaxBin) * 8 + kCutBins * 4;   // binned top k
   return s;
 }
 
@@ -269,6 +271,14 @@ IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk) {
   if (pl.ctas_per_sm == 1 && pl.nq >= 2) pl.eg = 2;   // one CTA per SM: two groups take turns
   if (tk && (pl.cap < topk + 256 || pl.cap < pl.pow2)) pl.ok = false;
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap, pl.pow2);
+  // the binned top k's gather buffer, only where it changes neither depth nor occupancy
+  if (tk) {
+    const size_t sb = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap, pl.pow2, true);
+    if (sb <= (pl.ctas_per_sm == 2 ? kSmemHalf : kSmemLimit)) {
+      pl.binned = true;
+      pl.smem = sb;
+    }
+  }
   if (pl.f4k) {
     // one CTA per SM: two epilogue groups taking the tiles in turn, four converter warps,
     // a deep FP4 ring and as many padded key tiles (2..4) as shared memory holds
@@ -281,6 +291,11 @@ IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk) {
     while (pl.stages > 2 && smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap, pl.pow2) > kSmemLimit) --pl.stages;
     pl.smem = smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap, pl.pow2);
     if (pl.smem > kSmemLimit) pl.ok = false;
+    pl.binned = false;
+    if (tk && smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap, pl.pow2, true) <= kSmemLimit) {
+      pl.binned = true;
+      pl.smem = smem_bytes_f4k(pl.nq, pl.stages, pl.conv_slots, tk, pl.cap, pl.pow2, true);
+    }
     // Each CTA holds all 512 TMEM columns (accumulators and scale cells): the request is
     // kept above half an SM's shared memory, so no second CTA is placed beside it.
     if (pl.smem <= kSmemHalf) pl.smem = kSmemHalf + 1024;
@@ -372,6 +387,7 @@ cudaError_t launch_indexer(const IndexerArgs& a, const IndexerPlan& pl, cudaStre
   prm.topk = a.topk;
   prm.cap = pl.cap;
   prm.pow2 = pl.pow2;
+  prm.binned = pl.binned ? 1 : 0;
   prm.out_idx = a.out_idx;
   prm.out_val = a.out_val;
   const bool tk = a.topk > 0;

@@ -72,11 +72,12 @@ struct IndexerParams {
   int32_t ngroups, nchunks, chunk;  // static schedule (logits mode)
   int32_t topk, cap, pow2, stages;
   int32_t nbuf_log2;        // log2 of the TMEM accumulator buffers (1 or 2)
+  int32_t binned;           // top-k mode: whole groups ranked by value bins (gather buffer present)
   // FP4-key mode: keys read from the paged mxfp4 cache (nibble rows of 64 bytes, E8M0
-  // rows of 4 bytes), converted to bf16 tiles on chip by the converter warps
+  // rows of 4 bytes), repacked on chip for the block-scaled MMA by the converter warps
   const uint8_t* kv_fp4;
   const uint8_t* kv_e8m0;
-  int32_t conv_slots;       // converted bf16 key tiles in flight
+  int32_t conv_slots;       // padded E2M1 key tiles in flight
 };
 
 constexpr int kMaxPer = 10;        // candidate capacity per query <= 256 * kMaxPer
@@ -284,8 +285,8 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
   const int NBARS = (2 * S + 16 + (kF4K ? 2 * CR : 0) + 1) & ~1;   // even: es stays 16-byte aligned
   EpiSmem<NQ>* es = reinterpret_cast<EpiSmem<NQ>*>(bars + NBARS);
   uint64_t* ebuf = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(es) + (sizeof(EpiSmem<NQ>) + 15) / 16 * 16);
-  // top-k mode: the candidate buffers [NQ][cap], then the gather buffer of the binned top k
-  // (pow2 + kItemMaxBin keys) and its bin starts (kCutBins words)
+  // top-k mode: the candidate buffers [NQ][cap], then (p.binned) the gather buffer of the
+  // binned top k (pow2 + kItemMaxBin keys) and its bin starts (kCutBins words)
   uint64_t* tbuf = ebuf + (size_t)NQ * p.cap;
   uint32_t* tstart = reinterpret_cast<uint32_t*>(tbuf + p.pow2 + kItemMaxBin);
 
@@ -762,8 +763,9 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
       } else if (!it.split) {
         // the whole group in one item: each row's top k by value bins (the whole epilogue,
         // one row after another; one warp per row sorting in registers took ~94 K cycles per
-        // four-row item); a row whose values crowd into one bin is cut back to SN
-        // candidates (histogram, then the exact select) and sorted by the bitonic network
+        // four-row item); a row whose values crowd into one bin, or every row when the plan
+        // left no room for the gather buffer, is cut back to SN candidates (histogram, then
+        // the exact select) and sorted by the bitonic network
         const int P = p.pow2;
         const int SN = P <= 128 ? 256 : (P <= 512 ? 2 * P : P);   // keys sorted per row (<= cap)
         group_sync<NT>();
@@ -775,8 +777,11 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
           int32_t* oi = real ? p.out_idx + t * p.topk : nullptr;
           float* ov = (real && p.out_val) ? p.out_val + t * p.topk : nullptr;
           int m = 0;
-          if (!engine_topk_binned<NT>(buf, (int)min(es->cnt[q], (uint32_t)cap), p.topk, tbuf, kItemMaxBin, tstart,
-                                      es->bins, es->esc.hist, es->esc.pick, et, oi, ov, &m)) {
+          bool done = false;
+          if (p.binned)
+            done = engine_topk_binned<NT>(buf, (int)min(es->cnt[q], (uint32_t)cap), p.topk, tbuf, kItemMaxBin,
+                                          tstart, es->bins, es->esc.hist, es->esc.pick, et, oi, ov, &m);
+          if (!done) {
             uint32_t cn = min(es->cnt[q], (uint32_t)cap);
             if (cn > (uint32_t)SN) {
               engine_cut_approx<NT, MAXPER>(buf, &es->cnt[q], (int)cn, p.topk, (uint32_t)SN, es->bins, &es->esc, et);

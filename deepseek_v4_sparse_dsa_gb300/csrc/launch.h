@@ -27,12 +27,14 @@ struct IndexerPlan {
   int cost;          // top-k mode: fixed cost of one work item, in key tiles
   int cap;           // candidate-buffer capacity per query row (top-k mode)
   int pow2;          // next power of two >= topk
+  bool binned;       // top-k mode: whole groups ranked by value bins (gather buffer in shared
+                     // memory; only where it leaves the plan's depth and occupancy unchanged)
   size_t smem;       // dynamic shared memory per CTA
   int64_t items;     // logits mode: work items; top-k mode: query groups
   size_t ws_bytes;   // workspace bytes (top-k mode)
   size_t prefix_off, ufirst_off, split_off, order_off, partial_off, meta_off;   // byte offsets in ws
-  bool f4k;          // E4M3 queries, keys from the paged mxfp4 cache (converted on chip)
-  int conv_slots;    // FP4-key mode: converted bf16 key tiles in flight
+  bool f4k;          // E4M3 queries, keys from the paged mxfp4 cache (block-scaled MMA)
+  int conv_slots;    // FP4-key mode: padded E2M1 key tiles in flight
   bool ok;           // false: shape does not fit this build
 };
 

@@ -47,14 +47,14 @@ def test_noalloc_matches_workspace_call_twice():
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch():
-    # four query rows per sequence at k = 1024: the partial top-k lists alone need ~18 MB
+    # four query rows per sequence at k = 2048: the partial top-k lists alone need ~20 MB
     lens = torch.full((256,), 1 << 20, dtype=torch.int32, device="cuda")
     qs = dsa.make_queries(256, 4, lens, 1 << 20, True)
-    assert dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, qs, 1024) > 16 << 20
+    assert dsa.dsa_workspace_bytes(dsa.DSA_OP_LOGITS_TOPK, dsa.DSA_BF16, qs, 2048) > 16 << 20
     keys = dsa.dsa_keys(0x100000, None, 0x100000, 1 << 14, 64, 1 << 20)
     before = dsa.dsa_launch_count()
     with pytest.raises(dsa.DsaError) as e:
-        dsa.dsa_indexer_logits_topk_noalloc(0x100000, None, dsa.DSA_BF16, 0x100000, 64, 128, keys, qs, 1024,
+        dsa.dsa_indexer_logits_topk_noalloc(0x100000, None, dsa.DSA_BF16, 0x100000, 64, 128, keys, qs, 2048,
                                             0x100000, None)
     assert e.value.status == dsa.DSA_ERR_WORKSPACE
     assert dsa.dsa_launch_count() == before
