@@ -75,6 +75,36 @@ dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_E
 
 using namespace dsa;
 
+dsa_status dsa::logits_topk_call(const void* q, const float* q_scale, dsa_dtype dtype, const float* weights, int H,
+                                 int D, const dsa_keys& keys, const dsa_queries& qs, int topk, int32_t* out_idx,
+                                 float* out_val, void* ws, size_t ws_bytes, void* stream, bool wide) {
+  dsa_status s = check_indexer_common(q, q_scale, dtype, weights, H, D, keys, qs);
+  if (s != DSA_OK) return s;
+  if (topk < 1 || topk > 2048 || out_idx == nullptr) return DSA_ERR_INVALID_ARG;
+  if ((int64_t)qs.B * qs.next_n == 0) return DSA_OK;
+  const IndexerPlan pl = plan_indexer(dtype, qs, topk, wide);
+  if (!pl.ok) return DSA_ERR_UNSUPPORTED;
+  if (pl.ws_bytes > 0 && (ws == nullptr || ws_bytes < pl.ws_bytes || !aligned(ws, 8))) return DSA_ERR_WORKSPACE;
+  IndexerArgs a{};
+  a.q = q;
+  a.q_scale = q_scale;
+  a.fp8 = dtype != DSA_BF16;
+  a.weights = weights;
+  a.keys = keys;
+  a.qs = qs;
+  a.topk = topk;
+  a.out_idx = out_idx;
+  a.out_val = out_val;
+  a.ws = ws;
+  return cuda_status(launch_indexer(a, pl, static_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa::logits_topk_ws_bytes(dsa_dtype dtype, const dsa_queries& qs, int topk, bool wide) {
+  if (check_queries(qs) != DSA_OK || topk < 1 || topk > 2048) return 0;
+  const IndexerPlan pl = plan_indexer(dtype, qs, topk, wide);
+  return pl.ok ? pl.ws_bytes : 0;
+}
+
 extern "C" {
 
 dsa_status dsa_indexer_logits(const void* q, const float* q_scale, dsa_dtype dtype, const float* weights, int H,
@@ -116,25 +146,8 @@ dsa_status dsa_indexer_topk(const float* logits, int64_t ld_logits, dsa_queries 
 dsa_status dsa_indexer_logits_topk(const void* q, const float* q_scale, dsa_dtype dtype, const float* weights,
                                    int H, int D, dsa_keys keys, dsa_queries qs, int topk, int32_t* out_idx,
                                    float* out_val, void* ws, size_t ws_bytes, void* stream) {
-  dsa_status s = check_indexer_common(q, q_scale, dtype, weights, H, D, keys, qs);
-  if (s != DSA_OK) return s;
-  if (topk < 1 || topk > 2048 || out_idx == nullptr) return DSA_ERR_INVALID_ARG;
-  if ((int64_t)qs.B * qs.next_n == 0) return DSA_OK;
-  const IndexerPlan pl = plan_indexer(dtype, qs, topk);
-  if (!pl.ok) return DSA_ERR_UNSUPPORTED;
-  if (pl.ws_bytes > 0 && (ws == nullptr || ws_bytes < pl.ws_bytes || !aligned(ws, 8))) return DSA_ERR_WORKSPACE;
-  IndexerArgs a{};
-  a.q = q;
-  a.q_scale = q_scale;
-  a.fp8 = dtype != DSA_BF16;
-  a.weights = weights;
-  a.keys = keys;
-  a.qs = qs;
-  a.topk = topk;
-  a.out_idx = out_idx;
-  a.out_val = out_val;
-  a.ws = ws;
-  return cuda_status(launch_indexer(a, pl, static_cast<cudaStream_t>(stream)));
+  return logits_topk_call(q, q_scale, dtype, weights, H, D, keys, qs, topk, out_idx, out_val, ws, ws_bytes, stream,
+                          true);
 }
 
 dsa_status mxfp4_paged_gather(const uint8_t* kv_fp4, const uint8_t* kv_scale, int64_t num_blocks, int block_size,
@@ -200,10 +213,7 @@ dsa_status dsa_sparse_attn_mxfp4(const uint16_t* q, int64_t T, int H, int D, con
 size_t dsa_workspace_bytes(dsa_op op, dsa_dtype dtype, dsa_queries qs, int topk) {
   if (check_queries(qs) != DSA_OK || topk < 1 || topk > 2048) return 0;
   if (op == DSA_OP_TOPK) return plan_topk(qs, topk).ws_bytes;
-  if (op == DSA_OP_LOGITS_TOPK) {
-    const IndexerPlan pl = plan_indexer(dtype, qs, topk);
-    return pl.ok ? pl.ws_bytes : 0;
-  }
+  if (op == DSA_OP_LOGITS_TOPK) return logits_topk_ws_bytes(dtype, qs, topk, true);
   return 0;
 }
 

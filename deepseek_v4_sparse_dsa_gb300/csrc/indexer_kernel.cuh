@@ -73,6 +73,7 @@ struct IndexerParams {
   int32_t topk, cap, pow2, stages;
   int32_t nbuf_log2;        // log2 of the TMEM accumulator buffers (1 or 2)
   int32_t binned;           // top-k mode: whole groups ranked by value bins (gather buffer present)
+  int32_t check_every;      // top-k mode: tiles between buffer checks (1 or 2)
   // FP4-key mode: keys read from the paged mxfp4 cache (nibble rows of 64 bytes, E8M0
   // rows of 4 bytes), repacked on chip for the block-scaled MMA by the converter warps
   const uint8_t* kv_fp4;
@@ -667,9 +668,11 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
       if (kKeyScale && !paged && first < it.ntiles && it.ks + first * 128 + row < p.num_rows)
         ks_next = __ldg(p.k_scale + it.ks + first * 128 + row);
       for (int m = 0; m < niter; ++m) {
-        // One group checks its buffers every CI tiles (one barrier per check), leaving
-        // room for CI tiles of appends; two groups check at every tile.
-        constexpr int CI = EG == 1 ? 2 : 1;
+        // The buffers are checked every CI tiles (one barrier per check), leaving room for
+        // CI tiles of appends per group: every second tile for one group, and for two
+        // groups whose buffers hold k + 1536 keys; two groups with less room check at every
+        // tile.
+        const int CI = p.check_every;
         if (kTopk && m % CI == 0) {
           group_sync<NT>();
 #pragma unroll 1

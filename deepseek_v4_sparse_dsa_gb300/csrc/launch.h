@@ -27,6 +27,7 @@ struct IndexerPlan {
   int cost;          // top-k mode: fixed cost of one work item, in key tiles
   int cap;           // candidate-buffer capacity per query row (top-k mode)
   int pow2;          // next power of two >= topk
+  int check_every;   // top-k mode: tiles between the epilogue's buffer checks (1 or 2)
   bool binned;       // top-k mode: whole groups ranked by value bins (gather buffer in shared
                      // memory; only where it leaves the plan's depth and occupancy unchanged)
   size_t smem;       // dynamic shared memory per CTA
@@ -39,7 +40,16 @@ struct IndexerPlan {
 };
 
 // topk == 0 plans the logits-only kernel.
-IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk);
+// wide = false: no wider candidate buffers (the allocation-free entry, whose scratch is
+// bounded, plans without them; results are the same, exact top-k either way).
+IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk, bool wide = true);
+
+// The fused call and its workspace size with the plan's wider buffers allowed or not
+// (api.cu; the public entry points use wide = true).
+size_t logits_topk_ws_bytes(dsa_dtype dtype, const dsa_queries& qs, int topk, bool wide);
+dsa_status logits_topk_call(const void* q, const float* q_scale, dsa_dtype dtype, const float* weights, int H,
+                            int D, const dsa_keys& keys, const dsa_queries& qs, int topk, int32_t* out_idx,
+                            float* out_val, void* ws, size_t ws_bytes, void* stream, bool wide);
 
 struct IndexerArgs {
   const void* q;

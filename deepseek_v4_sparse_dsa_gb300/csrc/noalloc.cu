@@ -47,12 +47,13 @@ extern "C" dsa_status dsa_indexer_logits_topk_noalloc(const void* q, const float
                                                       void* stream) {
   // The regular call checks every argument before the workspace, so a bad argument is
   // reported as such whatever the batch size; a batch whose scratch exceeds the array is
-  // handed no workspace and gets DSA_ERR_WORKSPACE from that check.
-  const size_t need = dsa_workspace_bytes(DSA_OP_LOGITS_TOPK, dtype, qs, topk);
+  // handed no workspace and gets DSA_ERR_WORKSPACE from that check.  The plan here takes
+  // no wider candidate buffers (they would grow the scratch); the result is the same.
+  const size_t need = dsa::logits_topk_ws_bytes(dtype, qs, topk, false);
   void* scratch = nullptr;
   if (need > 0 && need <= dsa::kNoAllocScratchBytes) {
     if (dsa::scratch_on_current_device(&scratch) != cudaSuccess) return DSA_ERR_CUDA;
   }
-  return dsa_indexer_logits_topk(q, q_scale, dtype, weights, H, D, keys, qs, topk, out_idx, out_val, scratch,
-                                 scratch != nullptr ? dsa::kNoAllocScratchBytes : 0, stream);
+  return dsa::logits_topk_call(q, q_scale, dtype, weights, H, D, keys, qs, topk, out_idx, out_val, scratch,
+                               scratch != nullptr ? dsa::kNoAllocScratchBytes : 0, stream, false);
 }

@@ -281,8 +281,11 @@ dsa_status dsa_sparse_attn_mxfp4(const uint16_t* q, int64_t T, int H, int D, con
  * Same arguments and results as dsa_indexer_logits_topk, without ws / ws_bytes: the
  * scratch lives in a fixed 16 MiB array in the library's device image, which every
  * GPU that loads the library holds until the process exits.
- *  - A batch whose dsa_workspace_bytes(DSA_OP_LOGITS_TOPK, ...) exceeds 16 MiB is
- *    rejected with DSA_ERR_WORKSPACE before anything is launched.
+ *  - Its plan takes no wider candidate buffers than the batch needs (the regular call
+ *    widens them where shared memory allows, which grows its workspace); results are the
+ *    same.  A batch whose scratch under that plan exceeds 16 MiB is rejected with
+ *    DSA_ERR_WORKSPACE before anything is launched; that scratch is never more than
+ *    dsa_workspace_bytes(DSA_OP_LOGITS_TOPK, ...).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *    and keeps it for the process; make that first call before any stream capture, and do
  *    not use this call across a device reset (cudaDeviceReset may move the array).
