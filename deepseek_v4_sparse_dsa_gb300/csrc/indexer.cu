@@ -272,30 +272,36 @@ IndexerPlan plan_indexer(dsa_dtype dt, const dsa_queries& qs, int topk, bool wid
   if (pl.ctas_per_sm == 1 && pl.nq >= 2) pl.eg = 2;   // one CTA per SM: two groups take turns
   if (tk && (pl.cap < topk + 256 || pl.cap < pl.pow2)) pl.ok = false;
   pl.smem = smem_bytes(fp8, pl.nq, pl.stages, tk, pl.cap, pl.pow2);
-  // Two epilogue groups check their buffers at every tile unless the buffers hold k + 1536
-  // keys; then every second tile, with fewer cut-backs and group barriers (FP8 chunked
-  // 9.41 -> 8.32 ms).  Wider buffers are taken where they fit the plan as it stands, or
-  // (not in the FP4-key mode) at one pipeline stage less, two at least (bf16 prefill
-  // 2.87 -> 2.66 ms); the occupancy never changes.
+  // Two epilogue groups check their buffers at every tile unless the buffers are wider than
+  // k + 1024: with k + 512 + 512 c keys, every c-th tile (fewer cut-backs and group barriers).
+  // The plan takes, in this order, k + 2048 keys at its depth, k + 1536 at its depth, then
+  // the same at one pipeline stage less (two at least; not in the FP4-key mode); the
+  // occupancy never changes.  Measured: FP8 chunked 9.41 -> 8.00 ms (k + 2048, every third
+  // tile), bf16 prefill 2.87 -> 2.62 ms (k + 2048 at two stages), Pro decode MTP 0.170 ->
+  // 0.164 ms (k + 1536 at four stages; k + 2048 at three was slower).
   auto widen = [&](auto smem_of) {
     pl.check_every = pl.eg == 1 ? 2 : 1;
     if (!tk || pl.eg != 2 || !wide) return;
-    const int want = topk + 1536;
-    const int cap2 = std::min((want + 255) / 256 * 256, 256 * kMaxPer);
-    if (cap2 < want) return;
-    if (cap2 <= pl.cap) {
-      pl.check_every = 2;
-      return;
-    }
     const size_t lim = pl.ctas_per_sm == 2 ? kSmemHalf : kSmemLimit;
-    for (int st = pl.stages; st >= (pl.f4k ? pl.stages : std::max(2, pl.stages - 1)); --st) {
-      const size_t sb = smem_of(cap2, st);
-      if (sb <= lim) {
-        pl.cap = cap2;
-        pl.stages = st;
-        pl.smem = sb;
-        pl.check_every = 2;
-        return;
+    const int st0 = pl.stages, st_min = pl.f4k ? st0 : std::max(2, st0 - 1);
+    for (int st = st0; st >= st_min; --st) {
+      for (int extra = 2048; extra >= 1536; extra -= 512) {
+        const int want = topk + extra;
+        if (want > 256 * kMaxPer2) continue;
+        const int cap2 = (want + 255) / 256 * 256;
+        const int ci = (cap2 - topk - 512) / 512;
+        if (cap2 <= pl.cap) {                  // the buffers are that wide already
+          pl.check_every = std::max(1, (pl.cap - topk - 512) / 512);
+          return;
+        }
+        const size_t sb = smem_of(cap2, st);
+        if (sb <= lim) {
+          pl.cap = cap2;
+          pl.stages = st;
+          pl.smem = sb;
+          pl.check_every = ci;
+          return;
+        }
       }
     }
   };

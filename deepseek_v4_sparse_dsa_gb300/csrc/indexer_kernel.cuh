@@ -82,6 +82,7 @@ struct IndexerParams {
 };
 
 constexpr int kMaxPer = 10;        // candidate capacity per query <= 256 * kMaxPer
+constexpr int kMaxPer2 = 12;       // two epilogue groups: up to 256 * kMaxPer2 (wider buffers)
 constexpr uint32_t kItemMaxBin = 512;   // binned top k of a whole group: largest bin gathered
 
 struct ItemInfo {
@@ -611,7 +612,7 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
     // EG groups of 4 warps take the tiles in turn (global tile T goes to group T % EG);
     // all NT threads share the per-row candidate buffers and cut them back together.
     constexpr int NT = 128 * EG;
-    constexpr int MAXPER = kMaxPer * 2 / EG;     // candidate slots per thread in a cut-back
+    constexpr int MAXPER = EG == 2 ? kMaxPer2 : kMaxPer * 2 / EG;     // candidate slots per thread in a cut-back
     const int et = threadIdx.x - 64;             // 0..NT-1
     const int grp = (warp - 2) >> 2;
     const int ew = warp - 2;                     // epilogue warp 0..4*EG-1
@@ -669,9 +670,9 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
         ks_next = __ldg(p.k_scale + it.ks + first * 128 + row);
       for (int m = 0; m < niter; ++m) {
         // The buffers are checked every CI tiles (one barrier per check), leaving room for
-        // CI tiles of appends per group: every second tile for one group, and for two
-        // groups whose buffers hold k + 1536 keys; two groups with less room check at every
-        // tile.
+        // CI tiles of appends per group: every second tile for one group; for two groups,
+        // every (cap - k - 512) / 512 tiles where the plan gave them wider buffers, else at
+        // every tile.
         const int CI = p.check_every;
         if (kTopk && m % CI == 0) {
           group_sync<NT>();

@@ -58,11 +58,13 @@ def test_workspace_plans_are_host_only(lib):
     n = ws(flash, 512)
     assert n >= 148 * 2 * 512 * 8
     assert ws(dsa.make_queries(128, 1, 0x1000, 65536, True), 512) - n == 64 * 8
-    # the partial lists grow with k (not strictly where two epilogue groups take wider
-    # buffers of k + 1536 keys: the prefill shape's at k = 512 are as wide as at k = 1024)
+    # the partial lists grow with k for one epilogue group; two groups take buffers of up
+    # to k + 2048 keys where shared memory allows, so theirs need not (the prefill shape's
+    # at k = 512 are wider than at k = 1024)
     prefill = dsa.make_queries(1, 16384, 0x1000, 16384, True)
     assert ws(flash, 2048) > ws(flash, 1024) > ws(flash, 512) > ws(flash, 256) > 0
-    assert ws(prefill, 2048) >= ws(prefill, 1024) >= ws(prefill, 512) >= ws(prefill, 256) > 0
+    for k in (256, 512, 1024, 2048):
+        assert ws(prefill, k) > 4096 * 4
     assert ws(prefill, 512) > 4096 * 4
     # the standalone top-k needs no workspace at any shape
     assert dsa.dsa_workspace_bytes(dsa.DSA_OP_TOPK, dsa.DSA_BF16, prefill, 512) == 0
