@@ -889,13 +889,19 @@ __global__ void __launch_bounds__(64 + 128 * EG + (kF4K ? 128 : 0), (EG == 1 && 
         const uint8_t* f4 = f4_s + (size_t)s4 * F4_BYTES;
         const uint32_t* sc = reinterpret_cast<const uint32_t*>(f4 + 8192);
         const uint32_t sw = sc[ct];
+        // Step i handles group g = i ^ m with m = x * ((ct >> 1) & 3) in GF(4) (0, 2, 3, 1):
+        // over the 8 threads of a 16-byte access phase, both the row reads (unit 4 (ct & 1)
+        // + g of 8) and the swizzled stores (unit (2 g + h) ^ (ct & 7)) then fall in 8
+        // different bank groups; the same g for every thread made the reads 4-way conflicts.
+        const uint32_t m = (0x1320u >> (4 * ((ct >> 1) & 3))) & 3u;
         uint4 v[4];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) v[g] = *reinterpret_cast<const uint4*>(f4 + ct * 64 + g * 16);
+        for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4*>(f4 + ct * 64 + (((uint32_t)i ^ m) << 4));
         uint8_t* dst = k_s + (size_t)c * KT_BYTES + ct * 128;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {               // group g: codes 32 g .. 32 g + 31, pieces 2 g, 2 g + 1
-          const uint4 x = ((sw >> (8 * g)) & 0xFFu) == 0xFFu ? make_uint4(0u, 0u, 0u, 0u) : v[g];
+        for (int i = 0; i < 4; ++i) {               // group g: codes 32 g .. 32 g + 31, pieces 2 g, 2 g + 1
+          const uint32_t g = (uint32_t)i ^ m;
+          const uint4 x = ((sw >> (8 * g)) & 0xFFu) == 0xFFu ? make_uint4(0u, 0u, 0u, 0u) : v[i];
           *reinterpret_cast<uint4*>(dst + (((2 * g) ^ (ct & 7)) << 4)) = make_uint4(x.x, x.y, 0u, 0u);
           *reinterpret_cast<uint4*>(dst + (((2 * g + 1) ^ (ct & 7)) << 4)) = make_uint4(x.z, x.w, 0u, 0u);
         }
