@@ -30,11 +30,13 @@
 //   warp 1     TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 2..  EG epilogue groups of 4 warps; global tile T uses TMEM buffer T % NB and
 //              epilogue group T % EG
+//   (FP4 keys) four converter warps after them: padded E2M1 tiles and TMEM scale cells
+//              for the block-scaled MMA
 // Epilogue: tcgen05.ld of each query's 64 head sums, fp32 ReLU * weight head sum in a
 // fixed order, then a store of the score row (logits mode) or an insert into a per-query
 // candidate buffer in shared memory (top-k mode) that a histogram cut brings back to a
-// superset of the top-k whenever it fills.  Unsplit groups get their rows ranked here,
-// one warp per row.
+// superset of the top-k whenever it fills.  Unsplit groups get each row's top k here, by
+// value bins (engine_topk_binned), the whole epilogue on one row after another.
 //
 // Every wait is bounded (see common.cuh); a timeout abandons the work, flags
 // DSA_DEVERR_TIMEOUT, waits for this CTA's own copies and MMAs, frees TMEM and returns.

@@ -90,8 +90,9 @@ typedef enum { DSA_OP_TOPK = 1, DSA_OP_LOGITS_TOPK = 2 } dsa_op;
  * mxfp4_paged_gather reads: `data` holds D/2 nibble bytes per row (low nibble = even
  * element, E2M1), `scale_e8m0` D/32 E8M0 bytes per row (2^(b-127), 0xFF -> 0), both
  * 16-byte aligned; `scale` is unused; a contiguous key array needs num_rows % 4 == 0.
- * The key's value is E2M1 * 2^(b-127) exactly (scale bytes >= 254 overflow bf16 and
- * are outside this mode's domain).
+ * The key's value is E2M1 * 2^(b-127) exactly; the tensor cores take the codes and
+ * scale bytes as stored (block-scaled MMA, one scale per 32 elements).  Scale bytes
+ * >= 254 can overflow the fp32 scores and are outside this mode's domain.
  */
 typedef struct {
   const void* data;
