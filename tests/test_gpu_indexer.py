@@ -107,6 +107,17 @@ def test_fp8_paged_mtp():
     check_case(wl)
 
 
+@pytest.mark.parametrize("lens,next_n,topk", [
+    ([700, 1500, 30000, 5000], 1, 1024),   # one row per item, two CTAs per SM
+    ([3000, 2500], 4, 2048),               # four-row groups at k = 2048
+])
+def test_topk_where_the_plan_has_no_gather_buffer(lens, next_n, topk):
+    # shared memory leaves no room for the binned top-k's gather buffer in these plans:
+    # every whole-group row is cut back and sorted by the bitonic network instead
+    wl = parity.make_case(81 + next_n, lens, next_n=next_n, block_size=64, topk=topk)
+    check_case(wl)
+
+
 def test_split_rows_with_tied_scores():
     # every cached key equal: all of a row's scores tie, so its top-k follows the index.
     # The merge of the split rows then finds all candidates in one value bin: the exact

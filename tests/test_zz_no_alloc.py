@@ -5,6 +5,8 @@ is a fixed array inside the library, so it must give exactly what the regular ca
 caller-provided workspace gives -- also on a second call, when the array still holds the
 first call's contents.  (This file sorts last so a stop-at-first-failure run has already
 run every other test.)"""
+import gc
+
 import numpy as np
 import pytest
 
@@ -73,6 +75,10 @@ def test_noalloc_allocates_nothing():
                                             db.queries(), wl.topk, idx, val)
 
     call()
+    torch.cuda.synchronize()
+    # garbage left by earlier tests (tensors in reference cycles) is collected now, so the
+    # collector cannot free it while the calls below run and shift the baseline
+    gc.collect()
     torch.cuda.synchronize()
     alloc0 = torch.cuda.memory_allocated()
     free0, _ = torch.cuda.mem_get_info()
