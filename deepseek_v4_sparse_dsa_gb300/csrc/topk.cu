@@ -193,6 +193,7 @@ __device__ void merge_rank_binned(const uint64_t* out, int m, uint64_t* tmp, uin
 }
 
 constexpr int kMergeNT = 512;       // merge: threads per row
+constexpr int kMergeLoads = 8;      // merge: list keys each thread loads per round
 constexpr int kMergeKeys = 24576;   // merge: candidates held in shared memory at once (two halves)
 
 // One CTA per (split group, query row): block m handles row m % nq of the (m / nq)-th
@@ -231,19 +232,10 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
   const int s0 = first_tile_slice(a0, cost, Q);
   const int nl = last_tile_slice(a1, Q) - s0 + 1;
   auto list_of = [&](int l) -> size_t { return (size_t)split_slot(s0 + l, a0, cost, Q) * nq + q; };
-  // 1. the floor: the largest piece threshold
-  uint64_t fl = 0;
-  for (int l = tid; l < nl; l += NT) fl = max(fl, __ldcg(meta + 2 * list_of(l) + 1));
-  for (int o = 16; o > 0; o >>= 1) fl = max(fl, __shfl_xor_sync(0xFFFFFFFFu, fl, o));
-  if (lane == 0) s_floor[wid] = fl;
-  if (tid == 0) sh.cnt = 0;
-  group_sync<NT>();
-  fl = 0;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) fl = max(fl, s_floor[w]);
-  if (tid == 0) sh.thr = fl;
-  // 2. collect the keys at or above the running threshold, cutting back when full;
-  //    lists are taken 32 at a time, their keys as one flat range
+  // Collect the keys at or above the running threshold, cutting back when full; lists
+  // are taken 32 at a time, their keys as one flat range.  The threshold starts at the
+  // largest piece threshold of the lists read so far (each is at most the row's k-th key,
+  // so any of them is a floor), read with the lists' counts.
   uint64_t* cur = mbuf;
   uint64_t* alt = mbuf + kHalf;
   for (int c0 = 0; c0 < nl; c0 += 32) {
@@ -251,25 +243,32 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
     if (wid == 0) {
       uint32_t cn = 0;
       size_t li = 0;
+      uint64_t fl = 0;
       if (lane < nc) {
         li = list_of(c0 + lane);
         cn = (uint32_t)min((uint64_t)lcap, __ldcg(meta + 2 * li));
+        fl = __ldcg(meta + 2 * li + 1);
       }
       uint32_t incl = cn;
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += y;
       }
+      for (int o = 16; o > 0; o >>= 1) fl = max(fl, __shfl_xor_sync(0xFFFFFFFFu, fl, o));
       s_off[lane + 1] = incl;
       s_li[lane] = (uint32_t)li;
-      if (lane == 0) s_off[0] = 0;
+      if (lane == 0) {
+        s_off[0] = 0;
+        if (c0 == 0) sh.cnt = 0;
+        sh.thr = c0 == 0 ? fl : max(sh.thr, fl);
+      }
     }
     group_sync<NT>();
     const int total = (int)s_off[nc];
-    for (int base = 0; base < total; base += 4 * NT) {
-      uint64_t v[4];
+    for (int base = 0; base < total; base += kMergeLoads * NT) {
+      uint64_t v[kMergeLoads];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kMergeLoads; ++u) {
         const int e = base + u * NT + tid;
         v[u] = 0ull;
         if (e < total) {
@@ -285,7 +284,7 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
       // lists left stale by an abandoned call can hold thousands of equal keys, which no
       // cut can thin.  Nothing past the half is ever read.
       const uint32_t n = min(sh.cnt, (uint32_t)kHalf);
-      if (n > (uint32_t)(kHalf - 4 * NT)) {
+      if (n > (uint32_t)(kHalf - kMergeLoads * NT)) {
         uint64_t th = engine_cut_approx<NT, kHalf / NT>(cur, &sh.cnt, (int)n, topk, (uint32_t)(kHalf / 2), mbins,
                                                         &sh.esc, tid);
         if (th == 0ull) {
@@ -300,12 +299,12 @@ __global__ void __launch_bounds__(kMergeNT) merge_kernel(const uint64_t* __restr
       }
       const uint64_t th = sh.thr;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < kMergeLoads; ++u)
         engine_append(cur, &sh.cnt, v[u], v[u] != 0ull && v[u] >= th, (uint32_t)kHalf, 31u);
     }
     group_sync<NT>();                           // s_off / s_li are rewritten next round
   }
-  // 3. the row's top-k in rank order: by value bins straight from the candidates; when
+  // Then the row's top-k in rank order: by value bins straight from the candidates; when
   //    the values crowd into one bin, a histogram cut, the exact radix select, and the
   //    binned rank of the selected keys
   uint32_t n = min(sh.cnt, (uint32_t)kHalf);
